@@ -1,0 +1,376 @@
+"""Pins of the fp64 oracle against facts fixed by the pages and by mathematics.
+
+None of these re-types the oracle's formula: each checks a closed form, an
+invariant, a hand-derived worked example, a special case, or the gradient
+against finite differences of the loss, chosen so that a dropped term, a wrong
+sign, a wrong index or a transposed operand in ``oracle/rl_loss_oracle.c``
+fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import BF16, F32, F64, LossParams
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _batch(logits, targets, logp_old, logp_infer, mask, cu, rewards):
+    return dict(logits=np.ascontiguousarray(logits), targets=np.asarray(targets, np.int32),
+                logp_old=np.asarray(logp_old, np.float32), logp_infer=np.asarray(logp_infer, np.float32),
+                mask=np.asarray(mask, np.uint8), cu_seqlens=np.asarray(cu, np.int32),
+                rewards_or_adv=np.asarray(rewards, np.float32))
+
+
+def _row_logp(z, dtype=F64):
+    """Oracle log-prob of every vocabulary entry of one row (target = v)."""
+    V = z.shape[0]
+    T = V
+    b = _batch(np.tile(z, (T, 1)), np.arange(V), np.zeros(T), np.zeros(T), np.ones(T), [0, T], [1.0])
+    p = LossParams(group_size=1, adv_mode=1)
+    _, adv, w = oracle.seq_prep(b["cu_seqlens"], b["mask"], b["rewards_or_adv"], p)
+    return oracle.rows(np.arange(T), b["logits"], dtype, V, b["targets"], b["logp_old"], b["logp_infer"],
+                       b["mask"], b["cu_seqlens"], adv, w, p)
+
+
+# ----------------------------------------------------------------------------- log-softmax / entropy
+
+@pytest.mark.parametrize("V", [1, 2, 7, 4096])
+def test_uniform_row_closed_form(V):
+    out = _row_logp(np.zeros(V, np.float64)) if V <= 64 else None
+    if out is None:  # large V: one row, one target
+        b = _batch(np.zeros((1, V), np.float32), [3], [0], [0], [1], [0, 1], [1.0])
+        p = LossParams(group_size=1, adv_mode=1)
+        out = oracle.forward_backward(b, F32, V, p)
+    np.testing.assert_allclose(out["logp"], -math.log(V), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out["entropy"], math.log(V), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("a,b", [(0.0, 0.0), (0.3, -1.7), (5.0, -5.0), (-20.0, 3.0)])
+def test_two_value_closed_form(a, b):
+    out = _row_logp(np.array([a, b]))
+    p0 = 1.0 / (1.0 + math.exp(b - a))
+    np.testing.assert_allclose(out["logp"][0], -math.log1p(math.exp(b - a)), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(out["logp"][1], -math.log1p(math.exp(a - b)), rtol=1e-13, atol=1e-14)
+    h = -(p0 * math.log(p0) + (1 - p0) * math.log(1 - p0))
+    np.testing.assert_allclose(out["entropy"][0], h, rtol=1e-12, atol=1e-14)
+
+
+def test_logprobs_exponentiate_to_one_and_shift_invariance():
+    rng = np.random.default_rng(1)
+    z = rng.normal(0, 3, 300)
+    out = _row_logp(z)
+    assert abs(np.exp(out["logp"]).sum() - 1.0) < 1e-12
+    out2 = _row_logp(z + 123.25)
+    np.testing.assert_allclose(out2["logp"], out["logp"], rtol=0, atol=1e-11)
+    np.testing.assert_allclose(out2["entropy"], out["entropy"], rtol=0, atol=1e-11)
+    # the log-prob of entry v is attached to entry v (no off-by-one / transposition)
+    order = np.argsort(z)
+    assert np.all(np.diff(out["logp"][order]) >= 0)
+
+
+def test_dominant_logit_and_entropy_bounds():
+    z = np.zeros(50)
+    z[17] = 1e4
+    out = _row_logp(z)
+    assert abs(out["logp"][17]) < 1e-300 + 1e-12
+    assert abs(out["entropy"][0]) < 1e-12
+    rng = np.random.default_rng(2)
+    for V in (3, 40):
+        for _ in range(5):
+            o = _row_logp(rng.normal(0, 4, V))
+            assert np.all(o["entropy"] >= -1e-15) and np.all(o["entropy"] <= math.log(V) + 1e-12)
+
+
+def test_bf16_widening_is_exact():
+    # bf16 bit patterns of 1.0, -2.5, 0.15625 and 3.0 (upper halves of binary32 words)
+    bits = np.array([[0x3F80, 0xC020, 0x3E20, 0x4040]], np.uint16)
+    vals = np.array([1.0, -2.5, 0.15625, 3.0])
+    b = _batch(bits, [2], [0], [0], [1], [0, 1], [1.0])
+    p = LossParams(group_size=1, adv_mode=1)
+    out = oracle.forward_backward(b, BF16, 4, p)
+    ref = vals[2] - math.log(np.exp(vals).sum())
+    assert abs(out["logp"][0] - ref) < 1e-14
+
+
+# ----------------------------------------------------------------------------- advantages / weights
+
+@pytest.mark.parametrize("G,k", [(4, 1), (8, 3), (32, 16), (32, 31)])
+def test_bernoulli_group_advantage_closed_form(G, k):
+    R = np.zeros(G, np.float32)
+    R[:k] = 1.0
+    cu = np.arange(G + 1, dtype=np.int32)
+    for unbiased in (0, 1):
+        p = LossParams(group_size=G, adv_eps=0.0, std_unbiased=unbiased)
+        _, adv, _ = oracle.seq_prep(cu, np.ones(G), R, p)
+        mu = k / G
+        sd = math.sqrt(k * (G - k) / (G * (G - 1))) if unbiased else math.sqrt(mu * (1 - mu))
+        np.testing.assert_allclose(adv[:k], (1 - mu) / sd, rtol=1e-14)
+        np.testing.assert_allclose(adv[k:], -mu / sd, rtol=1e-14)
+
+
+def test_advantage_invariants():
+    rng = np.random.default_rng(3)
+    G, P = 8, 5
+    R = rng.normal(size=G * P).astype(np.float32)
+    cu = np.arange(G * P + 1, dtype=np.int32)
+    p = LossParams(group_size=G, adv_eps=0.0)
+    _, adv, _ = oracle.seq_prep(cu, np.ones(G * P), R, p)
+    grp = adv.reshape(P, G)
+    np.testing.assert_allclose(grp.sum(1), 0.0, atol=1e-12)            # centred per group
+    np.testing.assert_allclose((grp ** 2).mean(1), 1.0, rtol=1e-12)    # unit population std
+    # groups are consecutive responses: group 1's advantages depend on group 1 only
+    R2 = R.copy()
+    R2[:G] += 10.0
+    _, adv2, _ = oracle.seq_prep(cu, np.ones(G * P), R2, p)
+    np.testing.assert_array_equal(adv2[G:], adv[G:])
+    # all-equal rewards: exactly zero advantage
+    _, adv3, _ = oracle.seq_prep(cu[:G + 1], np.ones(G), np.full(G, 0.7, np.float32),
+                                 LossParams(group_size=G))
+    assert np.all(adv3 == 0.0)
+    # adv_eps enters the denominator: (R - mean) / (std + eps)
+    _, adv4, _ = oracle.seq_prep(cu[:3], np.ones(2), np.array([1, 0], np.float32),
+                                 LossParams(group_size=2, adv_eps=0.5))
+    np.testing.assert_allclose(adv4, [0.5, -0.5], rtol=1e-15)
+
+
+def test_token_counts_and_weights_follow_mask_table():
+    spec = json.load(open(os.path.join(GOLDEN, "mask_table.json")))
+    seg_masks = [s["loss_mask"] for s in spec["segments"]]
+    assert seg_masks == [1, 0, 0, 1]
+    # response 0: the four segments of 5, 7, 3, 4 tokens; response 1: one fully masked segment
+    mask = np.concatenate([np.full(n, m, np.uint8) for n, m in zip((5, 7, 3, 4), seg_masks)] +
+                          [np.zeros(6, np.uint8)])
+    cu = np.array([0, 19, 25], np.int32)
+    n, _, w = oracle.seq_prep(cu, mask, np.array([0.3, -0.2], np.float32), LossParams(group_size=1, adv_mode=1))
+    assert list(n) == [9, 0]
+    np.testing.assert_allclose(w, [1.0 / (2 * 9), 0.0], rtol=1e-15)
+
+
+# ----------------------------------------------------------------------------- the loss
+
+def test_worked_example_golden():
+    ex = json.load(open(os.path.join(GOLDEN, "eq1_worked_example.json")))
+    ln = math.log
+    lo = [ln(3 / 4) - ln(1.5), ln(1 / 4) - ln(0.9)]
+    li = [lo[0] - ln(1.25), lo[1] - ln(0.8)]
+    b = _batch(np.array([[0.0, ln(3)], [ln(3), 0.0]]), [1, 1], lo, li, [1, 1], [0, 1, 2], [1.0, 0.0])
+    p = LossParams(group_size=2, adv_eps=0.0)
+    out = oracle.forward_backward(b, F64, 2, p, want_dz=True)
+    e = ex["expected"]
+    assert abs(out["loss"] - e["loss"]) < 2e-6
+    np.testing.assert_allclose(out["logp"], [ln(3 / 4), ln(1 / 4)], rtol=1e-14)
+    h = -(0.25 * ln(0.25) + 0.75 * ln(0.75))
+    np.testing.assert_allclose(out["entropy"], [h, h], rtol=1e-14)
+    assert list(out["flags"] & 1) == e["pop_in_bounds"]
+    assert list((out["flags"] >> 1) & 1) == e["clip_active"]
+    np.testing.assert_allclose(out["g"], e["dlogp"], rtol=1e-6, atol=1e-12)
+    np.testing.assert_allclose(out["dz"], e["dlogits"], rtol=1e-6, atol=1e-12)
+
+
+def _onpolicy_batch(rng, lengths, V, adv, dtype=F64):
+    """Random logits; logp_old = the oracle's own log-prob (fl32), logp_infer = logp_old."""
+    T = sum(lengths)
+    z = rng.normal(0, 2, (T, V))
+    tg = rng.integers(0, V, T)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    b = _batch(z, tg, np.zeros(T), np.zeros(T), np.ones(T), cu, adv)
+    p = LossParams(group_size=1, adv_mode=1)
+    first = oracle.forward_backward(b, dtype, V, p)
+    b["logp_old"] = first["logp"].astype(np.float32)
+    b["logp_infer"] = b["logp_old"].copy()
+    return b
+
+
+def test_closed_form_on_policy_loss_is_minus_mean_advantage():
+    rng = np.random.default_rng(4)
+    lengths, A = [3, 7, 1, 5], [0.7, -1.3, 0.25, 2.0]
+    b = _onpolicy_batch(rng, lengths, 33, A)
+    p = LossParams(group_size=1, adv_mode=1)
+    out = oracle.forward_backward(b, F64, 33, p)
+    S = len(lengths)
+    # r = exp(logp - fl32(logp)) = 1 up to the fp32 rounding of logp_old (|logp| < 8: 4.8e-7)
+    assert abs(out["loss"] - (-sum(A) / S)) < 5e-7 * sum(map(abs, A))
+    want_g = np.concatenate([np.full(n, -a / (S * n)) for n, a in zip(lengths, A)])
+    np.testing.assert_allclose(out["g"], want_g, rtol=5e-7)
+    assert np.all(out["flags"] & 1) and not np.any(out["flags"] & 2)
+
+
+def test_closed_form_constant_rho():
+    rng = np.random.default_rng(5)
+    lengths, A = [4, 6], [1.5, -0.5]
+    b = _onpolicy_batch(rng, lengths, 17, A)
+    rho_in = np.array([1.3, 0.6, 1.9, 0.75, 1.1, 0.55, 1.0, 1.99, 0.51, 1.4])
+    b["logp_infer"] = (b["logp_old"].astype(np.float64) - np.log(rho_in)).astype(np.float32)
+    rho = np.exp(b["logp_old"].astype(np.float64) - b["logp_infer"].astype(np.float64))
+    p = LossParams(group_size=1, adv_mode=1)
+    out = oracle.forward_backward(b, F64, 17, p)
+    want = -(A[0] * rho[:4].mean() + A[1] * rho[4:].mean()) / 2
+    assert abs(out["loss"] - want) < 1e-6
+    p1 = LossParams(group_size=1, adv_mode=1, pop_indicator=1)
+    out1 = oracle.forward_backward(b, F64, 17, p1)
+    assert abs(out1["loss"] - (-sum(A) / 2)) < 1e-6
+
+
+def test_pop_out_of_bounds_contributes_exactly_zero_and_boundary_is_closed():
+    rng = np.random.default_rng(6)
+    b = _onpolicy_batch(rng, [5], 9, [1.0])
+    B = oracle.thresholds_f32(2.0, 0.2, 0.28)[0]
+    assert B == np.float32(math.log(2.0))
+    d = np.array([1.0, -1.0, 0.0, 0.5, -0.5], np.float32)
+    b["logp_infer"] = (b["logp_old"] - d).astype(np.float32)
+    p = LossParams(group_size=1, adv_mode=1)
+    out = oracle.forward_backward(b, F64, 9, p, want_dz=True)
+    assert list(out["flags"] & 1) == [0, 0, 1, 1, 1]
+    assert np.all(out["tok_obj"][:2] == 0.0) and np.all(out["g"][:2] == 0.0)
+    assert np.all(out["dz"][:2] == 0.0) and np.all(out["dz"][2:].any(axis=1))
+    # closed interval in fp32: d == fl32(ln 2) is in bounds, the next float up is out
+    lo = np.float32(-1.0)
+    for dd, want in ((B, True), (-B, True), (np.nextafter(B, np.float32(9)), False),
+                     (np.nextafter(-B, np.float32(-9)), False)):
+        li = np.float32(lo - dd)
+        if np.float32(lo - li) == dd:
+            assert oracle.pop_in_bounds(float(lo), float(li), 2.0) == want
+
+
+@pytest.mark.parametrize("A,r,clipped,value", [
+    (0.8, 1.5, True, 1.28), (-0.8, 1.5, False, 1.5), (0.8, 0.5, False, 0.5), (-0.8, 0.5, True, 0.8),
+    (0.8, 1.1, False, 1.1), (-0.8, 0.9, False, 0.9), (0.0, 1.5, False, 0.0)])
+def test_clip_sides(A, r, clipped, value):
+    rng = np.random.default_rng(7)
+    b = _onpolicy_batch(rng, [1], 12, [A])
+    b["logp_old"] = (b["logp_old"] - np.float32(math.log(r))).astype(np.float32)
+    b["logp_infer"] = b["logp_old"].copy()
+    p = LossParams(group_size=1, adv_mode=1)
+    out = oracle.forward_backward(b, F64, 12, p, want_dz=True)
+    assert bool(out["flags"][0] & 2) == clipped
+    np.testing.assert_allclose(out["tok_obj"][0], value * A, rtol=1e-6)
+    if clipped or A == 0.0:
+        assert out["g"][0] == 0.0 and np.all(out["dz"] == 0.0)
+    else:
+        np.testing.assert_allclose(out["g"][0], -A * r, rtol=1e-6)
+
+
+def test_masked_rows_have_zero_gradient_and_do_not_count():
+    rng = np.random.default_rng(8)
+    V = 11
+    b = _onpolicy_batch(rng, [6, 4], V, [1.0, -2.0])
+    b["mask"] = np.array([1, 0, 0, 1, 1, 0, 1, 1, 0, 1], np.uint8)
+    p = LossParams(group_size=1, adv_mode=1)
+    out = oracle.forward_backward(b, F64, V, p, want_dz=True)
+    assert list(out["n_tokens"]) == [3, 3]
+    m = b["mask"].astype(bool)
+    assert np.all(out["dz"][~m] == 0.0) and np.all(out["tok_obj"][~m] == 0.0)
+    assert list((out["flags"] >> 2) & 1) == list((~m).astype(int))
+    b2 = dict(b)
+    z2 = b["logits"].copy()
+    z2[~m] = rng.normal(0, 5, (int((~m).sum()), V))
+    b2["logits"] = z2
+    out2 = oracle.forward_backward(b2, F64, V, p)
+    assert out2["loss"] == out["loss"]
+
+
+def test_row_gradient_sums_to_zero_and_zero_advantage():
+    rng = np.random.default_rng(9)
+    b = _onpolicy_batch(rng, [5, 3], 21, [0.9, -0.4])
+    b["logp_infer"] = (b["logp_old"] + rng.normal(0, 0.3, 8)).astype(np.float32)
+    p = LossParams(group_size=1, adv_mode=1)
+    out = oracle.forward_backward(b, F64, 21, p, want_dz=True)
+    np.testing.assert_allclose(out["dz"].sum(1), 0.0, atol=1e-15)
+    b["rewards_or_adv"] = np.zeros(2, np.float32)
+    out0 = oracle.forward_backward(b, F64, 21, p, want_dz=True)
+    assert out0["loss"] == 0.0 and np.all(out0["dz"] == 0.0)
+
+
+def test_normalisation_invariants():
+    """1/|y_i|: repeating a response's tokens leaves L unchanged; 1/S: repeating
+    every group leaves L unchanged; L does not depend on the order of groups."""
+    rng = np.random.default_rng(10)
+    V, G = 13, 2
+    lengths = [3, 5, 2, 4]
+    T = sum(lengths)
+    z = rng.normal(0, 2, (T, V))
+    tg = rng.integers(0, V, T)
+    lo = rng.normal(-2.5, 0.5, T).astype(np.float32)
+    li = (lo + rng.normal(0, 0.3, T)).astype(np.float32)
+    R = np.array([1, 0, 0.3, 0.9], np.float32)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    p = LossParams(group_size=G)
+    base = oracle.forward_backward(_batch(z, tg, lo, li, np.ones(T), cu, R), F64, V, p)["loss"]
+    # every response's tokens repeated twice
+    idx = np.concatenate([np.tile(np.arange(cu[i], cu[i + 1]), 2) for i in range(4)])
+    cu2 = np.concatenate([[0], np.cumsum(np.array(lengths) * 2)]).astype(np.int32)
+    rep = oracle.forward_backward(_batch(z[idx], tg[idx], lo[idx], li[idx], np.ones(2 * T), cu2, R), F64, V, p)
+    assert abs(rep["loss"] - base) < 1e-12
+    # every group repeated (S doubles)
+    idx2 = np.concatenate([np.arange(T), np.arange(T)])
+    cu3 = np.concatenate([[0], np.cumsum(lengths + lengths)]).astype(np.int32)
+    dup = oracle.forward_backward(_batch(z[idx2], tg[idx2], lo[idx2], li[idx2], np.ones(2 * T), cu3,
+                                         np.concatenate([R, R])), F64, V, p)
+    assert abs(dup["loss"] - base) < 1e-12
+    # groups swapped
+    order = np.concatenate([np.arange(cu[2], cu[4]), np.arange(cu[0], cu[2])])
+    cu4 = np.concatenate([[0], np.cumsum(lengths[2:] + lengths[:2])]).astype(np.int32)
+    sw = oracle.forward_backward(_batch(z[order], tg[order], lo[order], li[order], np.ones(T), cu4,
+                                        np.concatenate([R[2:], R[:2]])), F64, V, p)
+    assert abs(sw["loss"] - base) < 1e-12
+
+
+def test_gradient_matches_finite_differences():
+    """dL/dz of every entry against central differences of the oracle's own
+    loss (catches sign, index and transposition mistakes in the backward)."""
+    rng = np.random.default_rng(11)
+    V, G = 7, 2
+    lengths = [3, 2, 2, 1]
+    T = sum(lengths)
+    z = rng.normal(0, 1.5, (T, V))
+    tg = rng.integers(0, V, T).astype(np.int32)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    R = np.array([1.0, 0.0, 0.2, 0.9], np.float32)
+    p = LossParams(group_size=G)
+    # exact log-probs, then move tokens onto chosen branches, away from every boundary
+    b = _batch(z, tg, np.zeros(T), np.zeros(T), np.ones(T), cu, R)
+    lp = oracle.forward_backward(b, F64, V, p)["logp"]
+    ln_r = np.array([0.05, 0.6, -0.5, 0.1, -0.03, 0.4, -0.6, 0.0])  # r = e^{ln_r}
+    lo = (lp - ln_r).astype(np.float32)
+    li = (lo.astype(np.float64) - np.array([0.1, -0.2, 0.3, 1.2, 0.0, -0.4, 0.2, 0.05])).astype(np.float32)
+    mask = np.array([1, 1, 1, 1, 0, 1, 1, 1], np.uint8)
+    b = _batch(z, tg, lo, li, mask, cu, R)
+    out = oracle.forward_backward(b, F64, V, p, want_dz=True)
+    flags = out["flags"]
+    assert (flags & 2).any() and not (flags & 1).all()  # some clipped, some popped
+    h = 1e-6
+    fd = np.zeros((T, V))
+    for t in range(T):
+        for v in range(V):
+            zp, zm = z.copy(), z.copy()
+            zp[t, v] += h
+            zm[t, v] -= h
+            Lp = oracle.forward_backward(_batch(zp, tg, lo, li, mask, cu, R), F64, V, p)["loss"]
+            Lm = oracle.forward_backward(_batch(zm, tg, lo, li, mask, cu, R), F64, V, p)["loss"]
+            fd[t, v] = (Lp - Lm) / (2 * h)
+    scale = np.abs(out["dz"]).max()
+    np.testing.assert_allclose(out["dz"], fd, rtol=1e-6, atol=1e-7 * scale)
+
+
+def test_bad_target_is_excluded():
+    z = np.zeros((2, 4))
+    b = _batch(z, [5, 1], [-1.4, -1.4], [-1.4, -1.4], [1, 1], [0, 2], [1.0])
+    p = LossParams(group_size=1, adv_mode=1)
+    out = oracle.forward_backward(b, F64, 4, p, want_dz=True)
+    assert out["flags"][0] & 8 and not out["flags"][1] & 8
+    assert math.isnan(out["logp"][0]) and out["tok_obj"][0] == 0.0 and np.all(out["dz"][0] == 0.0)
+
+
+def test_hyperparameters_match_the_page():
+    hp = json.load(open(os.path.join(GOLDEN, "eq1_hyperparams.json")))
+    p = LossParams(group_size=hp["group_size"])
+    assert (p.beta, p.eps_low, p.eps_high) == (hp["beta"], hp["eps_low"], hp["eps_high"])
+    from rl_post_loss_gb300 import synthetic
+    for cid in (0, 1, 2):
+        assert synthetic.CASES[cid]["beta"] == hp["beta"]
+    assert (synthetic.EPS_LOW, synthetic.EPS_HIGH) == (hp["eps_low"], hp["eps_high"])
