@@ -1,0 +1,360 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused GRPO + IcePop token-level loss (forward + backward).
+
+One step = one call of ``rl_loss_forward_backward`` over one batch of the
+chosen workload (per-response prep, the fused row kernel, two fixed-order
+reductions), inputs resident in HBM. Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--case C] [--impl ours|reference]
+
+Multi-GPU runs are replicas: every rank processes its own batch, no
+collective on the data path (``scaling: weak``); the timed region is bracketed
+by a barrier + synchronize and the maximum over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "response tokens/s & HBM GB/s (% of peak), fused logprob+IcePop loss fwd+bwd"
+SIDE_BYTES_PER_TOKEN = 22  # target 4, logp_old 4, logp_infer 4, mask 1, logp 4, entropy 4, flags 1
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--case", type=int, default=1, choices=[0, 1, 2, 3])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prompts", type=int, default=0,
+                    help="use only the first P prompts' responses (small profiling runs); 0 = the whole case")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_traffic(kernel: str, case_id: int):
+    """Per-launch DRAM bytes of ``kernel`` from the committed ncu summary, or
+    None when that summary was taken on another version of the kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_case{case_id}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_hash = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not (m_bytes and m_hash) or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rl_post_loss_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "no samples"}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[3][k].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+
+
+def algorithmic_bytes(batch) -> float:
+    es = 2 if batch.dtype == "bf16" else 4
+    return float(batch.num_tokens) * (2.0 * batch.vocab * es + SIDE_BYTES_PER_TOKEN)
+
+
+def oracle_sample_rate(batch, seconds: float):
+    """The fp64 oracle (as it stands) over a bounded sample of rows: forward +
+    backward (dL/dlogits into a fresh fp64 buffer). Returns tokens/s, cores,
+    sample description."""
+    import numpy as np
+    import torch
+    import oracle
+    p = oracle.LossParams(group_size=batch.group, eps_low=batch.eps_low, eps_high=batch.eps_high,
+                          beta=batch.beta, adv_eps=batch.adv_eps, adv_mode=batch.adv_mode)
+    odt = oracle.BF16 if batch.dtype == "bf16" else oracle.F32
+
+    def logits_rows_np(b, ids):
+        idx = torch.as_tensor(np.asarray(ids, np.int64), device=b.logits.device)
+        lg = b.logits.index_select(0, idx)[:, :b.vocab].contiguous().cpu()
+        return lg.view(torch.int16).numpy().view(np.uint16) if lg.dtype == torch.bfloat16 else lg.numpy()
+
+    a = {k: getattr(batch, k).cpu().numpy() for k in
+         ("targets", "logp_old", "logp_infer", "mask", "cu_seqlens", "rewards_or_adv")}
+    n, adv, w = oracle.seq_prep(a["cu_seqlens"], a["mask"], a["rewards_or_adv"], p)
+    T = batch.num_tokens
+    probe = np.arange(min(T, 32))
+    z = logits_rows_np(batch, probe)
+    t0 = time.perf_counter()
+    oracle.rows(probe, z, odt, batch.vocab, a["targets"], a["logp_old"], a["logp_infer"], a["mask"],
+                a["cu_seqlens"], adv, w, p, want_dz=True)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    # bounded by the time budget and by a 2 GB fp64 dL/dlogits buffer
+    nrows = int(max(32, min(T, seconds / max(per_row, 1e-9), 2e9 / (8.0 * batch.vocab))))
+    ids = np.linspace(0, T - 1, nrows).astype(np.int64)
+    z = logits_rows_np(batch, ids)
+    t0 = time.perf_counter()
+    oracle.seq_prep(a["cu_seqlens"], a["mask"], a["rewards_or_adv"], p)
+    oracle.rows(ids, z, odt, batch.vocab, a["targets"], a["logp_old"], a["logp_infer"], a["mask"],
+                a["cu_seqlens"], adv, w, p, want_dz=True)
+    dt = time.perf_counter() - t0
+    cores = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
+    return nrows / dt, cores, f"{nrows} of {T} rows (evenly spaced), V={batch.vocab}, fp64 fwd+bwd, {dt:.1f} s"
+
+
+def run_reference(args):
+    """The oracle on the host cores, on bounded samples of the same workload."""
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    from rl_post_loss_gb300 import synthetic
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    batch = make_case_batch(args.case, args.prompts, dev)
+    per_step = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    rates = []
+    desc, cores = "", 0
+    for k in range(args.warmup + args.steps):
+        rate, cores, desc = oracle_sample_rate(batch, per_step)
+        if k >= args.warmup:
+            rates.append(rate)
+    value = statistics.mean(rates)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * batch.num_tokens / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(batch, args.case),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+L2_BYTES = 129e6
+
+
+def make_case_batch(case_id: int, prompts: int, device, seed: int = 0):
+    from rl_post_loss_gb300 import synthetic
+    lengths = None
+    if prompts:
+        c = synthetic.CASES[case_id]
+        base = 20261202 + case_id + 1000 * seed
+        lengths = synthetic.make_lengths(c, base)[:prompts * c["group"]]
+    return synthetic.make_batch(case_id, device, seed=seed, lengths=lengths)
+
+
+def workload_config(batch, case_id):
+    from rl_post_loss_gb300 import synthetic
+    c = synthetic.CASES[case_id]
+    return {"workload": f"case {case_id}: {c['name']}", "tokens": batch.num_tokens, "responses": batch.num_seqs,
+            "group": batch.group, "vocab": batch.vocab, "logits_dtype": batch.dtype,
+            "mask1_tokens": int(batch.mask.sum().item()), "beta": batch.beta,
+            "eps": [batch.eps_low, batch.eps_high], "adv_mode": batch.adv_mode,
+            "parallelism": "replicas",
+            "l2": ("no flush: each step streams the whole logits and dlogits arrays (%.2f GB), larger than "
+                   "the 129 MB L2" % (algorithmic_bytes(batch) / 1e9)) if algorithmic_bytes(batch) > 2 * L2_BYTES
+            else "L2 flushed between steps (256 MB memset inside the timed region)"}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    from rl_post_loss_gb300 import build as nvbuild
+    from rl_post_loss_gb300 import capi, synthetic
+    if not os.path.exists(nvbuild.LIB_PATH):
+        if rank == 0:
+            nvbuild.build()
+        else:
+            for _ in range(600):
+                if os.path.exists(nvbuild.LIB_PATH):
+                    break
+                time.sleep(1)
+    capi.load()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    batch = make_case_batch(args.case, args.prompts, "cuda", seed=rank)
+    rl = capi.handle_for_batch(batch)
+    flush = None
+    if algorithmic_bytes(batch) <= 2 * L2_BYTES:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    out = capi.alloc_outputs(batch)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        capi.run_batch(rl, batch, out)
+    torch.cuda.synchronize()
+    bits = rl.device_status()
+
+    rl.profile_start(args.steps)
+    launches0 = rl.launch_count()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            capi.run_batch(rl, batch, out)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    ms = start.elapsed_time(stop)
+    launches = rl.launch_count() - launches0
+    prof = rl.profile_read()
+    if world > 1:
+        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    T = batch.num_tokens
+    value = world * args.steps * T / (ms / 1e3)
+    row_n, row_ms = prof["row_loss"]
+    row_avg_ms = row_ms / max(1, row_n)
+    bytes_per_launch = algorithmic_bytes(batch)
+    peak, peak_kind = measured_peaks()
+    achieved = bytes_per_launch / (row_avg_ms / 1e3) / 1e9
+    traffic = kernel_traffic("row_loss", args.case)
+
+    # end to end through the public API: pinned host inputs -> device, call, loss -> host
+    host = {k: getattr(batch, k).cpu().pin_memory() for k in
+            ("logits", "targets", "logp_old", "logp_infer", "mask", "cu_seqlens", "rewards_or_adv")}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    loss_host = torch.empty(1, dtype=torch.float64).pin_memory()
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for k in range(args.e2e_steps + 1):
+        if k == 1:
+            torch.cuda.synchronize()
+            e_start.record(stream)
+        for name, t in host.items():
+            getattr(batch, name).copy_(t, non_blocking=True)
+        capi.run_batch(rl, batch, out)
+        loss_host.copy_(out["loss_f64"], non_blocking=True)
+        stream.synchronize()
+        _ = float(loss_host[0])
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_stop) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * T / (e2e_ms / 1e3)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, cores, desc = oracle_sample_rate(batch, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": workload_config(batch, args.case),
+                "hbm_gbs": world * args.steps * bytes_per_launch / (ms / 1e3) / 1e9,
+                "roofline": {"bound": "hbm", "kernel": "row_loss", "achieved": achieved, "peak": peak,
+                             "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s", "frac": achieved / peak,
+                             "traffic": traffic, "algorithmic_bytes_per_launch": bytes_per_launch,
+                             "avg_launch_ms": row_avg_ms},
+                "kernel_ms": {k: v[1] / max(1, v[0]) for k, v in prof.items()},
+                "clocks": clocks.summary(),
+                "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": 8, "ms_per_step": e2e_ms},
+                "gpu_launches": launches, "device_status": capi.status_bits_to_names(bits),
+                "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,190 @@
+/*
+ * rl_loss.h — C ABI of the GB300 (sm_103a) fused token-level policy loss.
+ *
+ * What it computes: the GRPO objective with IcePop train/inference mismatch
+ * suppression and no KL term, forward and backward in one call, as written in
+ * "GLM-5: from Vibe Coding to Agentic Engineering", section 3.2 "Reasoning
+ * RL", Eq. (1):
+ *
+ *   L = -(1/S) sum_i (1/|y_i|) sum_{t in i} m_t * pop(rho_t, 1/beta, beta)
+ *                          * min(r_t A_i, clip(r_t, 1 - eps_low, 1 + eps_high) A_i)
+ *
+ *   rho_t = pi_old^train(y_t) / pi_old^infer(y_t)   = exp(logp_old - logp_infer)
+ *   pop(rho) = rho if 1/beta <= rho <= beta, else 0  (pop_indicator: 1 instead of rho)
+ *   r_t   = pi_theta^train(y_t) / pi_old^train(y_t) = exp(logp_t - logp_old)
+ *   A_i   = (R_i - mean(R_group)) / (std(R_group) + adv_eps)    (group = G consecutive responses)
+ *   logp_t = z_{t, y_t} - log sum_v exp(z_{t, v})   (log-softmax of the logits row z_t)
+ *
+ * with S responses in the batch (the expectation over prompts read as the
+ * mean over the batch's S/G prompts, so 1/(S/G) * 1/G = 1/S), |y_i| the number
+ * of mask=1 tokens of response i (tool/environment tokens carry mask 0:
+ * "Zhipu AI / GLM: From Blank Infilling to Compaction-Aware Agentic
+ * Reinforcement Learning", section 9.4), and m_t the loss mask. Alongside the
+ * loss it writes dL/dlogits, the per-token log-prob and entropy (the entropy
+ * collapse the GLM-5 page watches in section 3.2, "DSA RL insights"), the
+ * per-token pop/clip flags and counters.
+ *
+ * Every floating-point reduction runs in a fixed order that depends only on
+ * the shapes, so repeated calls on the same inputs give bit-identical outputs
+ * (the section-3.2 lesson that non-deterministic GPU kernels collapsed RL).
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers inside rl_loss_inputs / rl_loss_outputs are DEVICE pointers on
+ *    the handle's device; the caller owns them. The handle owns only its
+ *    workspace, allocated once by rl_loss_create and freed by rl_loss_destroy.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Work is enqueued asynchronously; no call below synchronises
+ *    except rl_loss_get_device_status and rl_loss_profile_read. One handle must
+ *    not be used on two streams at the same time (it has one workspace).
+ *  - Argument, shape, alignment and capacity errors are detected on the host
+ *    and returned before anything is launched; outputs are then untouched.
+ *  - Data-dependent problems (a target id outside [0, V), a response with no
+ *    mask=1 token, malformed cu_seqlens) are detected on the device and set
+ *    bits (1u << rl_status code) in the handle's device status word, read with
+ *    rl_loss_get_device_status. Kernels never trap.
+ */
+#ifndef RL_LOSS_H
+#define RL_LOSS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define RL_LOSS_API __attribute__((visibility("default")))
+#else
+#define RL_LOSS_API
+#endif
+
+typedef enum rl_status {
+    RL_OK = 0,
+    RL_ERR_INVALID_ARG = 1,   /* NULL handle / required pointer, bad hyper-parameter */
+    RL_ERR_SHAPE = 2,         /* num_tokens / num_seqs / ld out of range, S % G != 0 */
+    RL_ERR_DTYPE = 3,         /* unknown dtype code */
+    RL_ERR_ALIGNMENT = 4,     /* logits / dlogits base or row stride not 16-byte aligned */
+    RL_ERR_CAPACITY = 5,      /* num_tokens > max_tokens or num_seqs > max_seqs */
+    RL_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed */
+    RL_ERR_TARGET_RANGE = 7,  /* device bit: some target id outside [0, V) (token excluded) */
+    RL_ERR_NONFINITE = 8,     /* device bit: loss is not finite */
+    RL_ERR_EMPTY_SEQ = 9,     /* device bit (warning): a response has no mask=1 token; it adds 0 */
+    RL_ERR_TIMEOUT = 10,      /* device bit: a bounded wait ran out */
+    RL_ERR_UNSUPPORTED = 11,  /* valid request this build does not implement */
+    RL_ERR_SEQLENS = 12,      /* device bit: cu_seqlens not monotone or not ending at num_tokens */
+    RL_ERR_DEVICE = 13        /* called with another CUDA device current than the handle's */
+} rl_status;
+
+typedef enum rl_dtype { RL_F32 = 0, RL_BF16 = 1 } rl_dtype;
+
+typedef enum rl_adv_mode {
+    RL_ADV_GROUP_REWARDS = 0, /* rewards_or_adv = R [S]; A_i normalised per group of G */
+    RL_ADV_PER_SEQ = 1        /* rewards_or_adv = A [S] given, e.g. teacher_score - student_score
+                                 with G = 1 ("2.5 GLM-5 -- 异步 Agentic RL 工程", Cross-Stage Distillation) */
+} rl_adv_mode;
+
+/* Per-token flag bits written to rl_loss_outputs.flags. */
+#define RL_FLAG_POP_IN_BOUNDS 0x1u /* 1/beta <= rho <= beta (decided in fp32: -fl32(ln beta) <= fl32(lo - li) <= fl32(ln beta)) */
+#define RL_FLAG_CLIP_ACTIVE 0x2u   /* clipped branch of min() taken: A>0 and fl32(logp - lo) > fl32(ln(1+eps_high)),
+                                      or A<0 and fl32(logp - lo) < fl32(ln(1-eps_low)); its gradient is 0 */
+#define RL_FLAG_MASKED 0x4u        /* loss mask m_t == 0 */
+#define RL_FLAG_BAD_TARGET 0x8u    /* target id outside [0, V): token excluded, logp = NaN */
+
+typedef struct rl_loss_handle_s *rl_loss_t;
+
+/* Static configuration; fixed for the life of a handle. */
+typedef struct rl_loss_config {
+    int32_t vocab_size;    /* V >= 1 */
+    int32_t group_size;    /* G >= 1; responses of a group are consecutive */
+    int32_t max_tokens;    /* capacity: largest num_tokens a call may pass (>= 0) */
+    int32_t max_seqs;      /* capacity: largest num_seqs a call may pass (>= 1) */
+    float eps_low;         /* 0 <= eps_low < 1 (0.2 on the page) */
+    float eps_high;        /* eps_high >= 0 (0.28 on the page) */
+    float beta;            /* beta > 1 (2 on the page) */
+    float adv_eps;         /* >= 0, added to the group std (1e-6) */
+    int32_t adv_mode;      /* rl_adv_mode */
+    int32_t std_unbiased;  /* 0: population std (ddof 0), 1: ddof 1 (needs G >= 2) */
+    int32_t pop_indicator; /* 0: pop returns rho (the printed operator), 1: returns 1 */
+    int32_t logits_dtype;  /* rl_dtype of logits and of dlogits */
+} rl_loss_config;
+
+/* One batch of T packed response tokens in S responses. */
+typedef struct rl_loss_inputs {
+    int32_t num_tokens;           /* T, 0 <= T <= max_tokens */
+    int32_t num_seqs;             /* S, 1 <= S <= max_seqs, S % G == 0 */
+    int64_t ld_logits;            /* row stride in elements, >= V; ld * elem_size % 16 == 0 */
+    const void *logits;           /* [T, ld] logits_dtype, 16-byte aligned; rows are read up to V
+                                     rounded up to 16 bytes (<= ld), the padding is never used */
+    const int32_t *targets;       /* [T] sampled token ids y_t */
+    const float *logp_old;        /* [T] log pi_old^train(y_t) */
+    const float *logp_infer;      /* [T] log pi_old^infer(y_t), from the rollout engine */
+    const uint8_t *mask;          /* [T] loss mask, nonzero = 1 */
+    const int32_t *cu_seqlens;    /* [S+1] offsets: response i is tokens [cu[i], cu[i+1]); cu[0]=0, cu[S]=T */
+    const float *rewards_or_adv;  /* [S] rewards (RL_ADV_GROUP_REWARDS) or advantages (RL_ADV_PER_SEQ) */
+} rl_loss_inputs;
+
+/* Where results go. Only `loss` and `dlogits` are required; NULL skips an output. */
+typedef struct rl_loss_outputs {
+    float *loss;          /* [1] L (rounded from loss_f64) */
+    double *loss_f64;     /* [1] L accumulated in fp64, or NULL */
+    void *dlogits;        /* [T, ld_dlogits] logits_dtype, dL/dlogits (columns >= V untouched).
+                             May alias logits when ld_dlogits == ld_logits (in-place). */
+    int64_t ld_dlogits;   /* >= V; ld * elem_size % 16 == 0 */
+    float *logp;          /* [T] per-token log-prob, or NULL */
+    float *entropy;       /* [T] per-token entropy of softmax(z_t) in nats, or NULL */
+    uint8_t *flags;       /* [T] RL_FLAG_* bits, or NULL */
+    float *seq_adv;       /* [S] A_i as used, or NULL */
+    int32_t *counts;      /* [4] mask=1 tokens popped, mask=1 tokens clipped, mask=0 tokens,
+                             responses with no mask=1 token; or NULL */
+    float *mean_entropy;  /* [1] mean entropy over mask=1 tokens, or NULL */
+} rl_loss_outputs;
+
+/* Kernel timing collected with CUDA events (see rl_loss_profile_start). */
+#define RL_PROFILE_MAX_KERNELS 8
+typedef struct rl_loss_profile {
+    int32_t num_kernels;
+    char names[RL_PROFILE_MAX_KERNELS][32];
+    int64_t launches[RL_PROFILE_MAX_KERNELS];
+    double total_ms[RL_PROFILE_MAX_KERNELS];
+} rl_loss_profile;
+
+/* Validates `config`, binds the handle to the current CUDA device and
+ * allocates its workspace (O(max_tokens + max_seqs) bytes). On failure *out is
+ * NULL and nothing stays allocated. */
+RL_LOSS_API rl_status rl_loss_create(const rl_loss_config *config, rl_loss_t *out);
+
+/* Frees the workspace and the handle (synchronises the device first). NULL is a no-op. */
+RL_LOSS_API rl_status rl_loss_destroy(rl_loss_t handle);
+
+/* The fused forward + backward pass of Eq. (1) over one batch. Enqueues four
+ * kernels on `stream` (per-response prep, the fused row kernel, two
+ * fixed-order reductions) and returns without synchronising. */
+RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t handle, const rl_loss_inputs *inputs,
+                                               const rl_loss_outputs *outputs, void *stream);
+
+/* Synchronises `stream`, returns the accumulated device status bits
+ * (1u << code for each rl_status code raised) in *bits and clears them. */
+RL_LOSS_API rl_status rl_loss_get_device_status(rl_loss_t handle, void *stream, uint32_t *bits);
+
+/* Static, human-readable name of a status code. */
+RL_LOSS_API const char *rl_loss_status_string(rl_status status);
+
+/* Starts recording a CUDA event pair around every kernel of the next
+ * `max_calls` forward_backward calls (timing only; results are unchanged). */
+RL_LOSS_API rl_status rl_loss_profile_start(rl_loss_t handle, int32_t max_calls);
+
+/* Synchronises the recorded events, writes per-kernel launch counts and
+ * summed durations into *out and stops recording. */
+RL_LOSS_API rl_status rl_loss_profile_read(rl_loss_t handle, rl_loss_profile *out);
+
+/* Number of kernels this handle has launched since it was created. */
+RL_LOSS_API rl_status rl_loss_launch_count(rl_loss_t handle, int64_t *count);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+RL_LOSS_API int32_t rl_loss_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RL_LOSS_H */

@@ -1,0 +1,254 @@
+"""Thin ctypes binding of ``include/rl_loss.h`` (argument marshalling only).
+
+Every function of the C ABI is exposed under its own name; ``RlLoss`` wraps a
+handle and marshals torch tensors (device memory and the current stream come
+from PyTorch; every step of the computation runs in the CUDA library). The
+binding fails loudly when ``librl_loss.so`` is missing or a call returns an
+error: there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "librl_loss.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "rl_loss.h")
+
+RL_F32, RL_BF16 = 0, 1
+RL_ADV_GROUP_REWARDS, RL_ADV_PER_SEQ = 0, 1
+RL_FLAG_POP_IN_BOUNDS, RL_FLAG_CLIP_ACTIVE, RL_FLAG_MASKED, RL_FLAG_BAD_TARGET = 1, 2, 4, 8
+
+STATUS_NAMES = {0: "RL_OK", 1: "RL_ERR_INVALID_ARG", 2: "RL_ERR_SHAPE", 3: "RL_ERR_DTYPE",
+                4: "RL_ERR_ALIGNMENT", 5: "RL_ERR_CAPACITY", 6: "RL_ERR_CUDA", 7: "RL_ERR_TARGET_RANGE",
+                8: "RL_ERR_NONFINITE", 9: "RL_ERR_EMPTY_SEQ", 10: "RL_ERR_TIMEOUT", 11: "RL_ERR_UNSUPPORTED",
+                12: "RL_ERR_SEQLENS", 13: "RL_ERR_DEVICE"}
+CODES = {v: k for k, v in STATUS_NAMES.items()}
+
+
+class RlLossError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+class rl_loss_config(ctypes.Structure):
+    _fields_ = [("vocab_size", ctypes.c_int32), ("group_size", ctypes.c_int32),
+                ("max_tokens", ctypes.c_int32), ("max_seqs", ctypes.c_int32),
+                ("eps_low", ctypes.c_float), ("eps_high", ctypes.c_float), ("beta", ctypes.c_float),
+                ("adv_eps", ctypes.c_float), ("adv_mode", ctypes.c_int32), ("std_unbiased", ctypes.c_int32),
+                ("pop_indicator", ctypes.c_int32), ("logits_dtype", ctypes.c_int32)]
+
+
+class rl_loss_inputs(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int32), ("num_seqs", ctypes.c_int32), ("ld_logits", ctypes.c_int64),
+                ("logits", ctypes.c_void_p), ("targets", ctypes.c_void_p), ("logp_old", ctypes.c_void_p),
+                ("logp_infer", ctypes.c_void_p), ("mask", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
+                ("rewards_or_adv", ctypes.c_void_p)]
+
+
+class rl_loss_outputs(ctypes.Structure):
+    _fields_ = [("loss", ctypes.c_void_p), ("loss_f64", ctypes.c_void_p), ("dlogits", ctypes.c_void_p),
+                ("ld_dlogits", ctypes.c_int64), ("logp", ctypes.c_void_p), ("entropy", ctypes.c_void_p),
+                ("flags", ctypes.c_void_p), ("seq_adv", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+                ("mean_entropy", ctypes.c_void_p)]
+
+
+class rl_loss_profile(ctypes.Structure):
+    _fields_ = [("num_kernels", ctypes.c_int32), ("names", (ctypes.c_char * 32) * 8),
+                ("launches", ctypes.c_int64 * 8), ("total_ms", ctypes.c_double * 8)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library {path} is missing; build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    st = ctypes.c_int
+    sig = {
+        "rl_loss_create": ([ctypes.POINTER(rl_loss_config), ctypes.POINTER(P)], st),
+        "rl_loss_destroy": ([P], st),
+        "rl_loss_forward_backward": ([P, ctypes.POINTER(rl_loss_inputs), ctypes.POINTER(rl_loss_outputs), P], st),
+        "rl_loss_get_device_status": ([P, P, ctypes.POINTER(ctypes.c_uint32)], st),
+        "rl_loss_status_string": ([st], ctypes.c_char_p),
+        "rl_loss_profile_start": ([P, ctypes.c_int32], st),
+        "rl_loss_profile_read": ([P, ctypes.POINTER(rl_loss_profile)], st),
+        "rl_loss_launch_count": ([P, ctypes.POINTER(ctypes.c_int64)], st),
+        "rl_loss_version": ([], ctypes.c_int32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def header_functions(path: str = HEADER) -> list[str]:
+    """Names of every function the C header declares."""
+    text = open(path).read()
+    return sorted(set(re.findall(r"RL_LOSS_API\s+[\w\s\*]+?\b(rl_loss_\w+)\s*\(", text)))
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise RlLossError(code, what)
+
+
+# ------------------------------------------------------------------ the C names, one to one
+
+def rl_loss_create(config: rl_loss_config) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    _check(load().rl_loss_create(ctypes.byref(config), ctypes.byref(h)), "rl_loss_create")
+    return h
+
+
+def rl_loss_destroy(handle) -> None:
+    _check(load().rl_loss_destroy(handle), "rl_loss_destroy")
+
+
+def rl_loss_forward_backward(handle, inputs: rl_loss_inputs, outputs: rl_loss_outputs, stream: int) -> int:
+    return load().rl_loss_forward_backward(handle, ctypes.byref(inputs), ctypes.byref(outputs),
+                                           ctypes.c_void_p(stream))
+
+
+def rl_loss_get_device_status(handle, stream: int) -> int:
+    bits = ctypes.c_uint32(0)
+    _check(load().rl_loss_get_device_status(handle, ctypes.c_void_p(stream), ctypes.byref(bits)),
+           "rl_loss_get_device_status")
+    return int(bits.value)
+
+
+def rl_loss_status_string(code: int) -> str:
+    return load().rl_loss_status_string(code).decode()
+
+
+def rl_loss_profile_start(handle, max_calls: int) -> None:
+    _check(load().rl_loss_profile_start(handle, max_calls), "rl_loss_profile_start")
+
+
+def rl_loss_profile_read(handle) -> dict:
+    prof = rl_loss_profile()
+    _check(load().rl_loss_profile_read(handle, ctypes.byref(prof)), "rl_loss_profile_read")
+    return {prof.names[k].value.decode(): (int(prof.launches[k]), float(prof.total_ms[k]))
+            for k in range(prof.num_kernels)}
+
+
+def rl_loss_launch_count(handle) -> int:
+    n = ctypes.c_int64(0)
+    _check(load().rl_loss_launch_count(handle, ctypes.byref(n)), "rl_loss_launch_count")
+    return int(n.value)
+
+
+def rl_loss_version() -> int:
+    return int(load().rl_loss_version())
+
+
+# ------------------------------------------------------------------ torch-facing wrapper
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class RlLoss:
+    """One handle: fixed vocabulary, group size, hyper-parameters and capacity."""
+
+    def __init__(self, vocab_size: int, group_size: int, max_tokens: int, max_seqs: int, logits_dtype: int,
+                 eps_low: float = 0.2, eps_high: float = 0.28, beta: float = 2.0, adv_eps: float = 1e-6,
+                 adv_mode: int = RL_ADV_GROUP_REWARDS, std_unbiased: bool = False, pop_indicator: bool = False):
+        self.config = rl_loss_config(vocab_size, group_size, max_tokens, max_seqs, eps_low, eps_high, beta,
+                                     adv_eps, adv_mode, int(std_unbiased), int(pop_indicator), logits_dtype)
+        self.handle = rl_loss_create(self.config)
+
+    def close(self):
+        if self.handle:
+            rl_loss_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def forward_backward(self, logits, targets, logp_old, logp_infer, mask, cu_seqlens, rewards_or_adv, *,
+                         loss, dlogits, loss_f64=None, logp=None, entropy=None, flags=None, seq_adv=None,
+                         counts=None, mean_entropy=None, stream=None) -> None:
+        """Enqueue one forward+backward on ``stream`` (default: torch's current
+        stream). All tensors are caller-owned CUDA tensors."""
+        import torch
+        T = int(targets.shape[0])
+        S = int(cu_seqlens.shape[0]) - 1
+        inp = rl_loss_inputs(T, S, int(logits.stride(0)) if logits.dim() == 2 else 0, _ptr(logits), _ptr(targets),
+                             _ptr(logp_old), _ptr(logp_infer), _ptr(mask), _ptr(cu_seqlens), _ptr(rewards_or_adv))
+        out = rl_loss_outputs(_ptr(loss), _ptr(loss_f64), _ptr(dlogits),
+                              int(dlogits.stride(0)) if dlogits.dim() == 2 else 0, _ptr(logp), _ptr(entropy),
+                              _ptr(flags), _ptr(seq_adv), _ptr(counts), _ptr(mean_entropy))
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        _check(rl_loss_forward_backward(self.handle, inp, out, stream), "rl_loss_forward_backward")
+
+    def device_status(self, stream=None) -> int:
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        return rl_loss_get_device_status(self.handle, stream)
+
+    def profile_start(self, max_calls: int):
+        rl_loss_profile_start(self.handle, max_calls)
+
+    def profile_read(self) -> dict:
+        return rl_loss_profile_read(self.handle)
+
+    def launch_count(self) -> int:
+        return rl_loss_launch_count(self.handle)
+
+
+def status_bits_to_names(bits: int) -> list[str]:
+    return [STATUS_NAMES[c] for c in sorted(STATUS_NAMES) if c and bits & (1 << c)]
+
+
+# ------------------------------------------------------------------ batch helpers
+
+def handle_for_batch(batch, max_tokens: int | None = None, max_seqs: int | None = None, **overrides) -> RlLoss:
+    """A handle configured for a ``synthetic.Batch`` (capacity = the batch's size)."""
+    kw = dict(eps_low=batch.eps_low, eps_high=batch.eps_high, beta=batch.beta, adv_eps=batch.adv_eps,
+              adv_mode=batch.adv_mode)
+    kw.update(overrides)
+    return RlLoss(batch.vocab, batch.group, max(1, max_tokens or batch.num_tokens), max_seqs or batch.num_seqs,
+                  RL_BF16 if batch.dtype == "bf16" else RL_F32, **kw)
+
+
+def alloc_outputs(batch, in_place: bool = False, ld: int | None = None) -> dict:
+    """Caller-owned output tensors for one call on ``batch`` (on its device)."""
+    import torch
+    dev = batch.logits.device
+    T, S = batch.num_tokens, batch.num_seqs
+    if in_place:
+        dlogits = batch.logits
+    else:
+        ld = ld or batch.logits.stride(0)
+        dlogits = torch.empty((T, ld), dtype=batch.logits.dtype, device=dev)
+    return dict(loss=torch.empty(1, dtype=torch.float32, device=dev),
+                loss_f64=torch.empty(1, dtype=torch.float64, device=dev), dlogits=dlogits,
+                logp=torch.empty(T, dtype=torch.float32, device=dev),
+                entropy=torch.empty(T, dtype=torch.float32, device=dev),
+                flags=torch.empty(T, dtype=torch.uint8, device=dev),
+                seq_adv=torch.empty(S, dtype=torch.float32, device=dev),
+                counts=torch.empty(4, dtype=torch.int32, device=dev),
+                mean_entropy=torch.empty(1, dtype=torch.float32, device=dev))
+
+
+def run_batch(rl: RlLoss, batch, outputs: dict, stream=None) -> dict:
+    """One forward+backward of ``batch`` into ``outputs`` (asynchronous)."""
+    rl.forward_backward(batch.logits, batch.targets, batch.logp_old, batch.logp_infer, batch.mask,
+                        batch.cu_seqlens, batch.rewards_or_adv, stream=stream, **outputs)
+    return outputs

@@ -1,0 +1,328 @@
+// C ABI of the fused GRPO + IcePop loss (declared in include/rl_loss.h):
+// handle life cycle, host-side validation, workspace layout, launches,
+// device status and event-based kernel timing.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kNumKernels = 4;
+const char *const kKernelNames[kNumKernels] = {"seg_prep", "row_loss", "seg_reduce", "final_reduce"};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+struct rl_loss_handle_s {
+    rl_loss_config cfg;
+    int device;
+    rlk::LossConsts consts;
+    // workspace (one cudaMalloc, carved below)
+    void *ws;
+    size_t ws_bytes;
+    uint32_t *status;
+    float *seq_adv, *seq_w;
+    double *seq_w64, *seq_obj, *seq_ent;
+    int32_t *seq_n, *seq_cnt;
+    float *tok_obj, *tok_ent;
+    uint8_t *tok_flags;
+    float *loss_scratch;
+    // bookkeeping
+    int64_t launches;
+    // profiling
+    int32_t prof_capacity, prof_calls;
+    std::vector<cudaEvent_t> prof_events;  // [capacity][kernels][2]
+};
+
+static size_t workspace_layout(const rl_loss_config &c, rl_loss_handle_s *h, char *base) {
+    const size_t S = (size_t)c.max_seqs, T = (size_t)c.max_tokens;
+    size_t off = 0;
+    auto carve = [&](size_t bytes) {
+        off = align_up(off, 256);
+        char *p = base ? base + off : nullptr;
+        off += bytes;
+        return p;
+    };
+    char *status = carve(sizeof(uint32_t));
+    char *seq_adv = carve(S * sizeof(float));
+    char *seq_w = carve(S * sizeof(float));
+    char *seq_w64 = carve(S * sizeof(double));
+    char *seq_obj = carve(S * sizeof(double));
+    char *seq_ent = carve(S * sizeof(double));
+    char *seq_n = carve(S * sizeof(int32_t));
+    char *seq_cnt = carve(S * 4 * sizeof(int32_t));
+    char *tok_obj = carve(T * sizeof(float));
+    char *tok_ent = carve(T * sizeof(float));
+    char *tok_flags = carve(T * sizeof(uint8_t));
+    char *loss_scratch = carve(4 * sizeof(float));
+    if (h) {
+        h->status = reinterpret_cast<uint32_t *>(status);
+        h->seq_adv = reinterpret_cast<float *>(seq_adv);
+        h->seq_w = reinterpret_cast<float *>(seq_w);
+        h->seq_w64 = reinterpret_cast<double *>(seq_w64);
+        h->seq_obj = reinterpret_cast<double *>(seq_obj);
+        h->seq_ent = reinterpret_cast<double *>(seq_ent);
+        h->seq_n = reinterpret_cast<int32_t *>(seq_n);
+        h->seq_cnt = reinterpret_cast<int32_t *>(seq_cnt);
+        h->tok_obj = reinterpret_cast<float *>(tok_obj);
+        h->tok_ent = reinterpret_cast<float *>(tok_ent);
+        h->tok_flags = reinterpret_cast<uint8_t *>(tok_flags);
+        h->loss_scratch = reinterpret_cast<float *>(loss_scratch);
+    }
+    return align_up(off, 256);
+}
+
+static int elem_size(int32_t dtype) { return dtype == RL_F32 ? 4 : 2; }
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+extern "C" {
+
+RL_LOSS_API int32_t rl_loss_version(void) { return 100; }
+
+RL_LOSS_API const char *rl_loss_status_string(rl_status s) {
+    switch (s) {
+        case RL_OK: return "ok";
+        case RL_ERR_INVALID_ARG: return "invalid argument";
+        case RL_ERR_SHAPE: return "bad shape";
+        case RL_ERR_DTYPE: return "unsupported dtype";
+        case RL_ERR_ALIGNMENT: return "pointer or row stride not 16-byte aligned";
+        case RL_ERR_CAPACITY: return "batch exceeds the handle's capacity";
+        case RL_ERR_CUDA: return "CUDA error";
+        case RL_ERR_TARGET_RANGE: return "target id outside [0, V)";
+        case RL_ERR_NONFINITE: return "non-finite loss";
+        case RL_ERR_EMPTY_SEQ: return "response without mask=1 tokens";
+        case RL_ERR_TIMEOUT: return "bounded wait ran out";
+        case RL_ERR_UNSUPPORTED: return "unsupported request";
+        case RL_ERR_SEQLENS: return "malformed cu_seqlens";
+        case RL_ERR_DEVICE: return "handle used on another device";
+    }
+    return "unknown status";
+}
+
+RL_LOSS_API rl_status rl_loss_create(const rl_loss_config *config, rl_loss_t *out) {
+    if (!out) return RL_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!config) return RL_ERR_INVALID_ARG;
+    const rl_loss_config &c = *config;
+    if (c.logits_dtype != RL_F32 && c.logits_dtype != RL_BF16) return RL_ERR_DTYPE;
+    if (c.vocab_size < 1 || c.group_size < 1 || c.max_tokens < 0 || c.max_seqs < 1) return RL_ERR_SHAPE;
+    if (!(c.beta > 1.f) || !std::isfinite(c.beta)) return RL_ERR_INVALID_ARG;
+    if (!(c.eps_low >= 0.f && c.eps_low < 1.f) || !(c.eps_high >= 0.f) || !std::isfinite(c.eps_high))
+        return RL_ERR_INVALID_ARG;
+    if (!(c.adv_eps >= 0.f) || !std::isfinite(c.adv_eps)) return RL_ERR_INVALID_ARG;
+    if (c.adv_mode != RL_ADV_GROUP_REWARDS && c.adv_mode != RL_ADV_PER_SEQ) return RL_ERR_INVALID_ARG;
+    if (c.std_unbiased && c.adv_mode == RL_ADV_GROUP_REWARDS && c.group_size < 2) return RL_ERR_INVALID_ARG;
+
+    rl_loss_handle_s *h = new (std::nothrow) rl_loss_handle_s();
+    if (!h) return RL_ERR_INVALID_ARG;
+    h->cfg = c;
+    if (cudaGetDevice(&h->device) != cudaSuccess) {
+        delete h;
+        return RL_ERR_CUDA;
+    }
+    // fp32 decision thresholds, each rounded once from a double
+    h->consts.ln_beta = (float)std::log((double)c.beta);
+    h->consts.clip_hi = (float)std::log1p((double)c.eps_high);
+    h->consts.clip_lo = (float)std::log1p(-(double)c.eps_low);
+    h->consts.one_plus_eps_high = 1.f + c.eps_high;
+    h->consts.one_minus_eps_low = 1.f - c.eps_low;
+    h->consts.pop_indicator = c.pop_indicator ? 1 : 0;
+
+    h->ws_bytes = workspace_layout(c, nullptr, nullptr);
+    if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return RL_ERR_CUDA;
+    }
+    workspace_layout(c, h, reinterpret_cast<char *>(h->ws));
+    if (cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess) {
+        cudaFree(h->ws);
+        delete h;
+        return RL_ERR_CUDA;
+    }
+    h->launches = 0;
+    h->prof_capacity = 0;
+    h->prof_calls = 0;
+    *out = h;
+    return RL_OK;
+}
+
+RL_LOSS_API rl_status rl_loss_destroy(rl_loss_t h) {
+    if (!h) return RL_OK;
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != h->device) cudaSetDevice(h->device);
+    cudaDeviceSynchronize();
+    for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
+    cudaError_t err = cudaFree(h->ws);
+    if (cur != h->device && cur >= 0) cudaSetDevice(cur);
+    delete h;
+    return err == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
+RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t h, const rl_loss_inputs *in, const rl_loss_outputs *out,
+                                               void *stream_ptr) {
+    if (!h || !in || !out) return RL_ERR_INVALID_ARG;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return RL_ERR_CUDA;
+    if (cur != h->device) return RL_ERR_DEVICE;
+    const rl_loss_config &c = h->cfg;
+    const int T = in->num_tokens, S = in->num_seqs, V = c.vocab_size;
+    const int es = elem_size(c.logits_dtype);
+    if (T < 0 || S < 1 || S % c.group_size != 0) return RL_ERR_SHAPE;
+    if (T > c.max_tokens || S > c.max_seqs) return RL_ERR_CAPACITY;
+    if (!in->cu_seqlens || !in->rewards_or_adv || !out->loss) return RL_ERR_INVALID_ARG;
+    if (T > 0) {
+        if (!in->logits || !in->targets || !in->logp_old || !in->logp_infer || !in->mask || !out->dlogits)
+            return RL_ERR_INVALID_ARG;
+        if (in->ld_logits < V || out->ld_dlogits < V) return RL_ERR_SHAPE;
+        if (!aligned16(in->logits) || !aligned16(out->dlogits) || (in->ld_logits * es) % 16 != 0 ||
+            (out->ld_dlogits * es) % 16 != 0)
+            return RL_ERR_ALIGNMENT;
+        if (in->logits == out->dlogits && in->ld_logits != out->ld_dlogits) return RL_ERR_INVALID_ARG;
+    }
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+
+    const bool prof = h->prof_calls < h->prof_capacity;
+    cudaEvent_t *ev = prof ? &h->prof_events[(size_t)h->prof_calls * kNumKernels * 2] : nullptr;
+    auto mark = [&](int k, int which) {
+        if (prof) cudaEventRecord(ev[2 * k + which], stream);
+    };
+
+    rlk::SeqPrepParams sp{};
+    sp.cu_seqlens = in->cu_seqlens;
+    sp.mask = in->mask;
+    sp.rewards_or_adv = in->rewards_or_adv;
+    sp.num_seqs = S;
+    sp.num_tokens = T;
+    sp.group_size = c.group_size;
+    sp.adv_mode = c.adv_mode;
+    sp.std_unbiased = c.std_unbiased;
+    sp.adv_eps = c.adv_eps;
+    sp.seq_adv = h->seq_adv;
+    sp.seq_w = h->seq_w;
+    sp.seq_w64 = h->seq_w64;
+    sp.seq_n = h->seq_n;
+    sp.seq_adv_out = out->seq_adv;
+    sp.status = h->status;
+
+    rlk::RowParams rp{};
+    rp.logits = in->logits;
+    rp.ld_logits = in->ld_logits;
+    rp.dlogits = out->dlogits;
+    rp.ld_dlogits = out->ld_dlogits;
+    rp.targets = in->targets;
+    rp.logp_old = in->logp_old;
+    rp.logp_infer = in->logp_infer;
+    rp.mask = in->mask;
+    rp.cu_seqlens = in->cu_seqlens;
+    rp.num_seqs = S;
+    rp.num_tokens = T;
+    rp.vocab = V;
+    rp.seq_adv = h->seq_adv;
+    rp.seq_w = h->seq_w;
+    rp.c = h->consts;
+    rp.logp_out = out->logp;
+    rp.entropy_out = out->entropy ? out->entropy : h->tok_ent;
+    rp.flags_out = out->flags ? out->flags : h->tok_flags;
+    rp.tok_obj = h->tok_obj;
+    rp.status = h->status;
+
+    rlk::ReduceParams rd{};
+    rd.cu_seqlens = in->cu_seqlens;
+    rd.num_seqs = S;
+    rd.num_tokens = T;
+    rd.tok_obj = h->tok_obj;
+    rd.entropy = rp.entropy_out;
+    rd.flags = rp.flags_out;
+    rd.seq_w64 = h->seq_w64;
+    rd.seq_n = h->seq_n;
+    rd.seq_obj = h->seq_obj;
+    rd.seq_ent = h->seq_ent;
+    rd.seq_cnt = h->seq_cnt;
+    rd.loss = out->loss;
+    rd.loss_f64 = out->loss_f64;
+    rd.counts = out->counts;
+    rd.mean_entropy = out->mean_entropy;
+    rd.status = h->status;
+
+    cudaError_t err;
+    mark(0, 0);
+    err = rlk::launch_seg_prep(sp, stream);
+    mark(0, 1);
+    if (err != cudaSuccess) return RL_ERR_CUDA;
+    mark(1, 0);
+    err = rlk::launch_row_loss(rp, c.logits_dtype, stream);
+    mark(1, 1);
+    if (err != cudaSuccess) return RL_ERR_CUDA;
+    mark(2, 0);
+    err = rlk::launch_seg_reduce(rd, stream);
+    mark(2, 1);
+    if (err != cudaSuccess) return RL_ERR_CUDA;
+    mark(3, 0);
+    err = rlk::launch_final_reduce(rd, stream);
+    mark(3, 1);
+    if (err != cudaSuccess) return RL_ERR_CUDA;
+    h->launches += (T > 0) ? 4 : 3;
+    if (prof) h->prof_calls++;
+    return RL_OK;
+}
+
+RL_LOSS_API rl_status rl_loss_get_device_status(rl_loss_t h, void *stream_ptr, uint32_t *bits) {
+    if (!h || !bits) return RL_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+    uint32_t v = 0;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return RL_ERR_CUDA;
+    if (cudaMemcpy(&v, h->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return RL_ERR_CUDA;
+    if (cudaMemset(h->status, 0, sizeof v) != cudaSuccess) return RL_ERR_CUDA;
+    *bits = v;
+    return RL_OK;
+}
+
+RL_LOSS_API rl_status rl_loss_profile_start(rl_loss_t h, int32_t max_calls) {
+    if (!h || max_calls < 0) return RL_ERR_INVALID_ARG;
+    for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
+    h->prof_events.clear();
+    h->prof_capacity = 0;
+    h->prof_calls = 0;
+    h->prof_events.resize((size_t)max_calls * kNumKernels * 2, nullptr);
+    for (auto &e : h->prof_events)
+        if (cudaEventCreate(&e) != cudaSuccess) return RL_ERR_CUDA;
+    h->prof_capacity = max_calls;
+    return RL_OK;
+}
+
+RL_LOSS_API rl_status rl_loss_profile_read(rl_loss_t h, rl_loss_profile *out) {
+    if (!h || !out) return RL_ERR_INVALID_ARG;
+    std::memset(out, 0, sizeof *out);
+    out->num_kernels = kNumKernels;
+    for (int k = 0; k < kNumKernels; ++k) std::snprintf(out->names[k], sizeof out->names[k], "%s", kKernelNames[k]);
+    for (int call = 0; call < h->prof_calls; ++call) {
+        for (int k = 0; k < kNumKernels; ++k) {
+            cudaEvent_t a = h->prof_events[((size_t)call * kNumKernels + k) * 2];
+            cudaEvent_t b = h->prof_events[((size_t)call * kNumKernels + k) * 2 + 1];
+            if (cudaEventSynchronize(b) != cudaSuccess) return RL_ERR_CUDA;
+            float ms = 0.f;
+            if (cudaEventElapsedTime(&ms, a, b) != cudaSuccess) return RL_ERR_CUDA;
+            out->launches[k] += 1;
+            out->total_ms[k] += ms;
+        }
+    }
+    h->prof_capacity = 0;
+    h->prof_calls = 0;
+    return RL_OK;
+}
+
+RL_LOSS_API rl_status rl_loss_launch_count(rl_loss_t h, int64_t *count) {
+    if (!h || !count) return RL_ERR_INVALID_ARG;
+    *count = h->launches;
+    return RL_OK;
+}
+
+}  // extern "C"
