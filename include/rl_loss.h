@@ -180,6 +180,30 @@ RL_LOSS_API rl_status rl_loss_profile_read(rl_loss_t handle, rl_loss_profile *ou
 /* Number of kernels this handle has launched since it was created. */
 RL_LOSS_API rl_status rl_loss_launch_count(rl_loss_t handle, int64_t *count);
 
+/* Allocation-free variant of rl_loss_forward_backward, for callers that cannot
+ * call cudaMalloc when they need the loss: code running while a CUDA graph is
+ * captured, inside a framework whose caching allocator owns all device memory,
+ * or in a serving process with a fixed memory budget. (The pages describe no
+ * such entry point; it has no counterpart there.)
+ *
+ * It needs no handle and allocates nothing: its workspace is one static
+ * 16 MiB device array of this library, which every GPU that loads the library
+ * holds until the process exits. `config` is read as for rl_loss_create except
+ * that max_tokens / max_seqs are ignored: calls accept at most 262144 tokens
+ * and 8192 responses and return RL_ERR_CAPACITY beyond that, before launching
+ * anything. The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture. Every call on a device shares the one array and leaves
+ * its contents behind (the status word is cleared at the start of each call),
+ * so calls that overlap on the GPU (two streams, two threads) race and must be
+ * serialised by the caller. `device_status` (optional, a device pointer to one
+ * uint32) receives this call's status bits as rl_loss_get_device_status would
+ * report them. Everything else (arguments, layouts, outputs, errors) is as for
+ * rl_loss_forward_backward. */
+RL_LOSS_API rl_status rl_loss_forward_backward_noalloc(const rl_loss_config *config, const rl_loss_inputs *inputs,
+                                                       const rl_loss_outputs *outputs, uint32_t *device_status,
+                                                       void *stream);
+
 /* Library version as major * 10000 + minor * 100 + patch. */
 RL_LOSS_API int32_t rl_loss_version(void);
 

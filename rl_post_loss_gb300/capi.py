@@ -83,6 +83,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "rl_loss_profile_read": ([P, ctypes.POINTER(rl_loss_profile)], st),
         "rl_loss_launch_count": ([P, ctypes.POINTER(ctypes.c_int64)], st),
         "rl_loss_version": ([], ctypes.c_int32),
+        "rl_loss_forward_backward_noalloc": ([ctypes.POINTER(rl_loss_config), ctypes.POINTER(rl_loss_inputs),
+                                              ctypes.POINTER(rl_loss_outputs), P, P], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -146,6 +148,14 @@ def rl_loss_launch_count(handle) -> int:
     n = ctypes.c_int64(0)
     _check(load().rl_loss_launch_count(handle, ctypes.byref(n)), "rl_loss_launch_count")
     return int(n.value)
+
+
+def rl_loss_forward_backward_noalloc(config: rl_loss_config, inputs: rl_loss_inputs, outputs: rl_loss_outputs,
+                                     device_status_ptr: int | None, stream: int) -> int:
+    """The allocation-free entry point (no handle; static device workspace)."""
+    return load().rl_loss_forward_backward_noalloc(ctypes.byref(config), ctypes.byref(inputs),
+                                                   ctypes.byref(outputs), ctypes.c_void_p(device_status_ptr),
+                                                   ctypes.c_void_p(stream))
 
 
 def rl_loss_version() -> int:

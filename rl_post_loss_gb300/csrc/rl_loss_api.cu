@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -326,3 +327,93 @@ RL_LOSS_API rl_status rl_loss_launch_count(rl_loss_t h, int64_t *count) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free entry point
+//
+// Some callers cannot call cudaMalloc at the moment they need the loss: code
+// that runs while a CUDA graph is being captured, inside a framework whose
+// caching allocator owns all device memory, or in a serving process with a
+// fixed memory budget where an allocation could fail or synchronise the
+// device. rl_loss_forward_backward_noalloc serves them without a handle: its
+// workspace is one statically sized device array of this library, which every
+// GPU that loads the library holds until the process exits.
+namespace {
+
+constexpr int32_t kNoAllocMaxTokens = 262144;
+constexpr int32_t kNoAllocMaxSeqs = 8192;
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the static scratch on `device` (the current device),
+// looked up once per device.
+rl_status noalloc_scratch(int device, void **ptr) {
+    if (device < 0 || device >= kNoAllocMaxDevices) return RL_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[device]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return RL_ERR_CUDA;
+        }
+        g_noalloc_ptr[device] = p;
+    }
+    *ptr = g_noalloc_ptr[device];
+    return RL_OK;
+}
+
+}  // namespace
+
+extern "C" RL_LOSS_API rl_status rl_loss_forward_backward_noalloc(const rl_loss_config *config,
+                                                                  const rl_loss_inputs *inputs,
+                                                                  const rl_loss_outputs *outputs,
+                                                                  uint32_t *device_status, void *stream_ptr) {
+    if (!config || !inputs || !outputs) return RL_ERR_INVALID_ARG;
+    const rl_loss_config &c = *config;
+    if (c.logits_dtype != RL_F32 && c.logits_dtype != RL_BF16) return RL_ERR_DTYPE;
+    if (c.vocab_size < 1 || c.group_size < 1) return RL_ERR_SHAPE;
+    if (!(c.beta > 1.f) || !std::isfinite(c.beta)) return RL_ERR_INVALID_ARG;
+    if (!(c.eps_low >= 0.f && c.eps_low < 1.f) || !(c.eps_high >= 0.f) || !std::isfinite(c.eps_high))
+        return RL_ERR_INVALID_ARG;
+    if (!(c.adv_eps >= 0.f) || !std::isfinite(c.adv_eps)) return RL_ERR_INVALID_ARG;
+    if (c.adv_mode != RL_ADV_GROUP_REWARDS && c.adv_mode != RL_ADV_PER_SEQ) return RL_ERR_INVALID_ARG;
+    if (c.std_unbiased && c.adv_mode == RL_ADV_GROUP_REWARDS && c.group_size < 2) return RL_ERR_INVALID_ARG;
+    if (inputs->num_tokens > kNoAllocMaxTokens || inputs->num_seqs > kNoAllocMaxSeqs) return RL_ERR_CAPACITY;
+
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) return RL_ERR_CUDA;
+    void *scratch = nullptr;
+    rl_status st = noalloc_scratch(device, &scratch);
+    if (st != RL_OK) return st;
+
+    // A handle that lives on the stack and points into the static scratch.
+    rl_loss_handle_s h{};
+    h.cfg = c;
+    h.cfg.max_tokens = kNoAllocMaxTokens;
+    h.cfg.max_seqs = kNoAllocMaxSeqs;
+    h.device = device;
+    h.consts.ln_beta = (float)std::log((double)c.beta);
+    h.consts.clip_hi = (float)std::log1p((double)c.eps_high);
+    h.consts.clip_lo = (float)std::log1p(-(double)c.eps_low);
+    h.consts.one_plus_eps_high = 1.f + c.eps_high;
+    h.consts.one_minus_eps_low = 1.f - c.eps_low;
+    h.consts.pop_indicator = c.pop_indicator ? 1 : 0;
+    h.ws_bytes = workspace_layout(h.cfg, nullptr, nullptr);
+    if (h.ws_bytes > kNoAllocScratchBytes) return RL_ERR_CAPACITY;
+    h.ws = scratch;
+    workspace_layout(h.cfg, &h, reinterpret_cast<char *>(scratch));
+
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+    // the scratch keeps the previous call's contents: the status word must start at zero
+    if (cudaMemsetAsync(h.status, 0, sizeof(uint32_t), stream) != cudaSuccess) return RL_ERR_CUDA;
+    st = rl_loss_forward_backward(&h, inputs, outputs, stream_ptr);
+    if (st != RL_OK) return st;
+    if (device_status &&
+        cudaMemcpyAsync(device_status, h.status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+        return RL_ERR_CUDA;
+    return RL_OK;
+}
