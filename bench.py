@@ -43,6 +43,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prompts", type=int, default=0,
                     help="use only the first P prompts' responses (small profiling runs); 0 = the whole case")
+    ap.add_argument("--max-len", type=int, default=0, help="cap every response length (small profiling runs)")
     return ap.parse_args()
 
 
@@ -198,7 +199,7 @@ def run_reference(args):
     import torch
     from rl_post_loss_gb300 import synthetic
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    batch = make_case_batch(args.case, args.prompts, dev)
+    batch = make_case_batch(args.case, args.prompts, dev, max_len=args.max_len)
     per_step = max(2.0, 150.0 / max(1, args.steps + args.warmup))
     rates = []
     desc, cores = "", 0
@@ -220,13 +221,17 @@ def run_reference(args):
 L2_BYTES = 129e6
 
 
-def make_case_batch(case_id: int, prompts: int, device, seed: int = 0):
+def make_case_batch(case_id: int, prompts: int, device, seed: int = 0, max_len: int = 0):
     from rl_post_loss_gb300 import synthetic
     lengths = None
-    if prompts:
+    if prompts or max_len:
         c = synthetic.CASES[case_id]
         base = 20261202 + case_id + 1000 * seed
-        lengths = synthetic.make_lengths(c, base)[:prompts * c["group"]]
+        lengths = synthetic.make_lengths(c, base)
+        if prompts:
+            lengths = lengths[:prompts * c["group"]]
+        if max_len:
+            lengths = [min(n, max_len) for n in lengths]
     return synthetic.make_batch(case_id, device, seed=seed, lengths=lengths)
 
 
@@ -265,7 +270,7 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    batch = make_case_batch(args.case, args.prompts, "cuda", seed=rank)
+    batch = make_case_batch(args.case, args.prompts, "cuda", seed=rank, max_len=args.max_len)
     rl = capi.handle_for_batch(batch)
     flush = None
     if algorithmic_bytes(batch) <= 2 * L2_BYTES:

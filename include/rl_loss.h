@@ -67,7 +67,7 @@ typedef enum rl_status {
     RL_ERR_CAPACITY = 5,      /* num_tokens > max_tokens or num_seqs > max_seqs */
     RL_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed */
     RL_ERR_TARGET_RANGE = 7,  /* device bit: some target id outside [0, V) (token excluded) */
-    RL_ERR_NONFINITE = 8,     /* device bit: loss is not finite */
+    RL_ERR_NONFINITE = 8,     /* device bit: a logits row holds NaN or +inf, or the loss is not finite */
     RL_ERR_EMPTY_SEQ = 9,     /* device bit (warning): a response has no mask=1 token; it adds 0 */
     RL_ERR_TIMEOUT = 10,      /* device bit: a bounded wait ran out */
     RL_ERR_UNSUPPORTED = 11,  /* valid request this build does not implement */
@@ -176,6 +176,11 @@ RL_LOSS_API rl_status rl_loss_profile_start(rl_loss_t handle, int32_t max_calls)
 /* Synchronises the recorded events, writes per-kernel launch counts and
  * summed durations into *out and stops recording. */
 RL_LOSS_API rl_status rl_loss_profile_read(rl_loss_t handle, rl_loss_profile *out);
+
+/* Name of the CUDA error (e.g. "cudaErrorInvalidValue") behind the most recent
+ * RL_ERR_CUDA returned for this handle, "cudaSuccess" if there was none.
+ * Static string; never NULL. */
+RL_LOSS_API const char *rl_loss_last_cuda_error(rl_loss_t handle);
 
 /* Number of kernels this handle has launched since it was created. */
 RL_LOSS_API rl_status rl_loss_launch_count(rl_loss_t handle, int64_t *count);

@@ -82,6 +82,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "rl_loss_profile_start": ([P, ctypes.c_int32], st),
         "rl_loss_profile_read": ([P, ctypes.POINTER(rl_loss_profile)], st),
         "rl_loss_launch_count": ([P, ctypes.POINTER(ctypes.c_int64)], st),
+        "rl_loss_last_cuda_error": ([P], ctypes.c_char_p),
         "rl_loss_version": ([], ctypes.c_int32),
         "rl_loss_forward_backward_noalloc": ([ctypes.POINTER(rl_loss_config), ctypes.POINTER(rl_loss_inputs),
                                               ctypes.POINTER(rl_loss_outputs), P, P], st),
@@ -158,6 +159,10 @@ def rl_loss_forward_backward_noalloc(config: rl_loss_config, inputs: rl_loss_inp
                                                    ctypes.c_void_p(stream))
 
 
+def rl_loss_last_cuda_error(handle) -> str:
+    return load().rl_loss_last_cuda_error(handle).decode()
+
+
 def rl_loss_version() -> int:
     return int(load().rl_loss_version())
 
@@ -204,7 +209,10 @@ class RlLoss:
                               _ptr(flags), _ptr(seq_adv), _ptr(counts), _ptr(mean_entropy))
         if stream is None:
             stream = torch.cuda.current_stream().cuda_stream
-        _check(rl_loss_forward_backward(self.handle, inp, out, stream), "rl_loss_forward_backward")
+        code = rl_loss_forward_backward(self.handle, inp, out, stream)
+        if code == CODES["RL_ERR_CUDA"]:
+            raise RlLossError(code, "rl_loss_forward_backward (%s)" % rl_loss_last_cuda_error(self.handle))
+        _check(code, "rl_loss_forward_backward")
 
     def device_status(self, stream=None) -> int:
         import torch

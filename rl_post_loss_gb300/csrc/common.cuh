@@ -10,6 +10,7 @@
 namespace rlk {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 // 2^x on the MUFU unit (PTX ex2.approx.ftz.f32: relative error about 2^-22).
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -37,36 +38,93 @@ struct LossConsts {
     int32_t pop_indicator;
 };
 
-struct TokenResult {
+// ---------------------------------------------------------------- per-token record
+//
+// Everything a row kernel needs about token t besides its logits row, prepared
+// once per call by token_prep (the parts of Eq. (1) of the GLM-5 report page,
+// section 3.2, that do not depend on the row's softmax):
+//   rec[t]  = {z_y, logp_old, pop*A*m, w*pop*A*m}   (the last two 0 when the token is masked,
+//                                                    popped or has a bad target)
+//   meta[t] = y (low 24 bits) | pre-flags << 24
+// pre-flags: RL_FLAG_POP_IN_BOUNDS, RL_FLAG_MASKED, RL_FLAG_BAD_TARGET, and the
+// sign of A in the two internal bits below (stripped from the output flags).
+constexpr uint32_t kMetaYMask = 0x00FFFFFFu;
+constexpr uint32_t kPreAPos = 0x10u;
+constexpr uint32_t kPreANeg = 0x20u;
+constexpr uint32_t kPreOut = RL_FLAG_POP_IN_BOUNDS | RL_FLAG_MASKED | RL_FLAG_BAD_TARGET;
+constexpr int32_t kMaxVocab = 1 << 24;
+
+// ---------------------------------------------------------------- row statistics (base 2)
+//
+// Running softmax statistics of part of a row, with exponents in log2 units:
+//   m2 = a reference point (the part's max of z * log2 e), s = sum 2^{z log2e - m2},
+//   u2 = sum 2^{z log2e - m2} (z log2e - m2).
+// For a whole row with M2, S2, U2: logZ = (M2 + log2 S2) ln 2 and the entropy
+// H = -sum p ln p = (log2 S2 - U2 / S2) ln 2.
+struct RowStats2 {
+    float m2, s, u2;
+};
+
+__device__ __forceinline__ RowStats2 empty_stats() { return RowStats2{-INFINITY, 0.f, 0.f}; }
+
+// Merge two partial statistics. Symmetric in its arguments (explicit _rn
+// operations, no FMA contraction), so a butterfly gives every lane bit-identical
+// results, and exact for empty parts.
+__device__ __forceinline__ RowStats2 merge_stats2(RowStats2 a, RowStats2 b) {
+    const float M = fmaxf(a.m2, b.m2);
+    if (M == -INFINITY) return empty_stats();
+    const bool ea = a.m2 == -INFINITY, eb = b.m2 == -INFINITY;
+    const float da = ea ? 0.f : __fsub_rn(a.m2, M), db = eb ? 0.f : __fsub_rn(b.m2, M);
+    const float fa = ea ? 0.f : ex2_approx(da), fb = eb ? 0.f : ex2_approx(db);
+    const float ua = ea ? 0.f : __fmul_rn(fa, __fadd_rn(a.u2, __fmul_rn(da, a.s)));
+    const float ub = eb ? 0.f : __fmul_rn(fb, __fadd_rn(b.u2, __fmul_rn(db, b.s)));
+    return RowStats2{M, __fadd_rn(__fmul_rn(a.s, fa), __fmul_rn(b.s, fb)), __fadd_rn(ua, ub)};
+}
+
+__device__ __forceinline__ RowStats2 warp_merge_stats2(RowStats2 r) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        RowStats2 o{__shfl_xor_sync(0xffffffffu, r.m2, off), __shfl_xor_sync(0xffffffffu, r.s, off),
+                    __shfl_xor_sync(0xffffffffu, r.u2, off)};
+        r = merge_stats2(r, o);
+    }
+    return r;
+}
+
+// Per-row results of the token objective ("GLM-5: from Vibe Coding to Agentic
+// Engineering", section 3.2, Eq. (1)) from the row's statistics and record.
+struct RowOut {
     float logp;   // z_y - logZ (NaN for a bad target)
+    float H;      // entropy of softmax(z)
     float g;      // dL/dlogp_t
     float obj;    // m * pop * min(r A, clip(r) A)
+    float logZ2;  // logZ in log2 units
+    uint32_t y;
     uint32_t flags;
 };
 
-// Per-token part of Eq. (1) of the GLM-5 report page, section 3.2: rho, pop,
-// r, the clipped min and dL/dlogp. `w` is 1/(S |y_i|) of the token's response.
-__device__ __forceinline__ TokenResult token_objective(float zy, float logZ, bool target_ok, float logp_old,
-                                                       float logp_infer, bool m, float A, float w,
-                                                       const LossConsts &c) {
-    TokenResult r;
-    const float d = __fsub_rn(logp_old, logp_infer);  // ln rho, one fp32 subtraction
-    const bool in_bounds = (-c.ln_beta <= d) && (d <= c.ln_beta);
-    r.logp = target_ok ? __fsub_rn(zy, logZ) : __int_as_float(0x7fc00000);
-    const float e = __fsub_rn(r.logp, logp_old);      // ln r, one fp32 subtraction
-    const bool clip = target_ok && ((A > 0.f && e > c.clip_hi) || (A < 0.f && e < c.clip_lo));
-    r.flags = (in_bounds ? RL_FLAG_POP_IN_BOUNDS : 0u) | (clip ? RL_FLAG_CLIP_ACTIVE : 0u) |
-              (m ? 0u : RL_FLAG_MASKED) | (target_ok ? 0u : RL_FLAG_BAD_TARGET);
-    r.obj = 0.f;
-    r.g = 0.f;
-    if (m && target_ok && in_bounds) {
-        const float pop = c.pop_indicator ? 1.f : expf(d);
+__device__ __forceinline__ RowOut finish_row(RowStats2 st, float4 rec, uint32_t meta, const LossConsts &c) {
+    RowOut o;
+    const float log2S = log2f(st.s);
+    o.logZ2 = st.m2 + log2S;
+    const float logZ = o.logZ2 * kLn2;
+    o.H = (log2S - st.u2 / st.s) * kLn2;
+    const uint32_t pre = meta >> 24;
+    o.y = meta & kMetaYMask;
+    const bool ok = !(pre & RL_FLAG_BAD_TARGET);
+    o.logp = ok ? __fsub_rn(rec.x, logZ) : __int_as_float(0x7fc00000);
+    const float e = __fsub_rn(o.logp, rec.y);  // ln r, one fp32 subtraction
+    const bool clip = ok && (((pre & kPreAPos) && e > c.clip_hi) || ((pre & kPreANeg) && e < c.clip_lo));
+    o.flags = (pre & kPreOut) | (clip ? RL_FLAG_CLIP_ACTIVE : 0u);
+    o.obj = 0.f;
+    o.g = 0.f;
+    if (rec.z != 0.f) {  // m * pop * A != 0
         const float ratio = expf(e);
-        const float branch = clip ? (A > 0.f ? c.one_plus_eps_high : c.one_minus_eps_low) : ratio;
-        r.obj = pop * A * branch;
-        r.g = clip ? 0.f : -w * pop * A * ratio;
+        const float branch = clip ? ((pre & kPreAPos) ? c.one_plus_eps_high : c.one_minus_eps_low) : ratio;
+        o.obj = rec.z * branch;
+        o.g = clip ? 0.f : -rec.w * ratio;
     }
-    return r;
+    return o;
 }
 
 // Index i with cu[i] <= t < cu[i+1], or -1 (binary search over S+1 offsets).
@@ -77,36 +135,6 @@ __device__ __forceinline__ int find_seq(const int32_t *__restrict__ cu, int S, i
         if (__ldg(cu + mid) <= t) lo = mid; else hi = mid;
     }
     return (__ldg(cu + lo) <= t && t < __ldg(cu + lo + 1)) ? lo : -1;
-}
-
-// Running softmax statistics of part of a row: M = max, S = sum e^{z-M},
-// U = sum e^{z-M} (z-M).
-struct RowStats {
-    float m, s, u;
-};
-
-// Merge two partial statistics. Symmetric in its arguments (so a butterfly
-// gives every lane bit-identical results) and exact for empty parts.
-__device__ __forceinline__ RowStats merge_stats(RowStats a, RowStats b) {
-    const float M = fmaxf(a.m, b.m);
-    if (M == -INFINITY) return RowStats{M, 0.f, 0.f};
-    const float da = a.m - M, db = b.m - M;
-    const float fa = (a.m == -INFINITY) ? 0.f : ex2_approx(da * kLog2e);
-    const float fb = (b.m == -INFINITY) ? 0.f : ex2_approx(db * kLog2e);
-    // explicit _rn operations: no FMA contraction, so merge(a, b) == merge(b, a) bitwise
-    const float ua = (a.m == -INFINITY) ? 0.f : __fmul_rn(fa, fmaf(da, a.s, a.u));
-    const float ub = (b.m == -INFINITY) ? 0.f : __fmul_rn(fb, fmaf(db, b.s, b.u));
-    return RowStats{M, __fadd_rn(__fmul_rn(a.s, fa), __fmul_rn(b.s, fb)), __fadd_rn(ua, ub)};
-}
-
-__device__ __forceinline__ RowStats warp_merge_stats(RowStats r) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        RowStats o{__shfl_xor_sync(0xffffffffu, r.m, off), __shfl_xor_sync(0xffffffffu, r.s, off),
-                   __shfl_xor_sync(0xffffffffu, r.u, off)};
-        r = merge_stats(r, o);
-    }
-    return r;
 }
 
 __device__ __forceinline__ double warp_sum_f64(double v) {
@@ -144,6 +172,10 @@ __device__ __forceinline__ int block_sum_i32(int v, int *scratch) {
     return warp_sum_i32(t);
 }
 
+__device__ __forceinline__ void raise_status(uint32_t *status, rl_status code) {
+    atomicOr(status, 1u << static_cast<int>(code));
+}
+
 // ---------------------------------------------------------------- kernel parameters
 
 struct SeqPrepParams {
@@ -160,11 +192,10 @@ struct SeqPrepParams {
     uint32_t *status;
 };
 
-struct RowParams {
+struct TokenPrepParams {
     const void *logits;
     int64_t ld_logits;
-    void *dlogits;
-    int64_t ld_dlogits;
+    int32_t logits_dtype;
     const int32_t *targets;
     const float *logp_old;
     const float *logp_infer;
@@ -174,7 +205,21 @@ struct RowParams {
     const float *seq_adv;
     const float *seq_w;
     LossConsts c;
-    float *logp_out;
+    float4 *rec;     // workspace [T]
+    uint32_t *meta;  // workspace [T]
+    uint32_t *status;
+};
+
+struct RowParams {
+    const void *logits;
+    int64_t ld_logits;
+    void *dlogits;
+    int64_t ld_dlogits;
+    const float4 *rec;
+    const uint32_t *meta;
+    int32_t num_tokens, vocab;
+    LossConsts c;
+    float *logp_out;     // optional
     float *entropy_out;
     uint8_t *flags_out;
     float *tok_obj;
@@ -199,13 +244,12 @@ struct ReduceParams {
     uint32_t *status;
 };
 
-__device__ __forceinline__ void raise_status(uint32_t *status, rl_status code) {
-    atomicOr(status, 1u << static_cast<int>(code));
-}
-
 cudaError_t launch_seg_prep(const SeqPrepParams &p, cudaStream_t stream);
-cudaError_t launch_row_loss(const RowParams &p, int dtype, cudaStream_t stream);
+cudaError_t launch_token_prep(const TokenPrepParams &p, cudaStream_t stream);
 cudaError_t launch_seg_reduce(const ReduceParams &p, cudaStream_t stream);
 cudaError_t launch_final_reduce(const ReduceParams &p, cudaStream_t stream);
+
+// The fused row kernel (one block per logits row).
+cudaError_t launch_row_loss(const RowParams &p, int dtype, cudaStream_t stream);
 
 }  // namespace rlk

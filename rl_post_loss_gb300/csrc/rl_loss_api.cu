@@ -12,8 +12,8 @@
 
 namespace {
 
-constexpr int kNumKernels = 4;
-const char *const kKernelNames[kNumKernels] = {"seg_prep", "row_loss", "seg_reduce", "final_reduce"};
+constexpr int kNumKernels = 5;
+const char *const kKernelNames[kNumKernels] = {"seg_prep", "token_prep", "row_loss", "seg_reduce", "final_reduce"};
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -32,9 +32,12 @@ struct rl_loss_handle_s {
     int32_t *seq_n, *seq_cnt;
     float *tok_obj, *tok_ent;
     uint8_t *tok_flags;
+    float4 *tok_rec;
+    uint32_t *tok_meta;
     float *loss_scratch;
     // bookkeeping
     int64_t launches;
+    cudaError_t last_cuda_error;  // the CUDA error behind the last RL_ERR_CUDA of this handle
     // profiling
     int32_t prof_capacity, prof_calls;
     std::vector<cudaEvent_t> prof_events;  // [capacity][kernels][2]
@@ -60,6 +63,8 @@ static size_t workspace_layout(const rl_loss_config &c, rl_loss_handle_s *h, cha
     char *tok_obj = carve(T * sizeof(float));
     char *tok_ent = carve(T * sizeof(float));
     char *tok_flags = carve(T * sizeof(uint8_t));
+    char *tok_rec = carve(T * sizeof(float4));
+    char *tok_meta = carve(T * sizeof(uint32_t));
     char *loss_scratch = carve(4 * sizeof(float));
     if (h) {
         h->status = reinterpret_cast<uint32_t *>(status);
@@ -73,6 +78,8 @@ static size_t workspace_layout(const rl_loss_config &c, rl_loss_handle_s *h, cha
         h->tok_obj = reinterpret_cast<float *>(tok_obj);
         h->tok_ent = reinterpret_cast<float *>(tok_ent);
         h->tok_flags = reinterpret_cast<uint8_t *>(tok_flags);
+        h->tok_rec = reinterpret_cast<float4 *>(tok_rec);
+        h->tok_meta = reinterpret_cast<uint32_t *>(tok_meta);
         h->loss_scratch = reinterpret_cast<float *>(loss_scratch);
     }
     return align_up(off, 256);
@@ -96,7 +103,7 @@ RL_LOSS_API const char *rl_loss_status_string(rl_status s) {
         case RL_ERR_CAPACITY: return "batch exceeds the handle's capacity";
         case RL_ERR_CUDA: return "CUDA error";
         case RL_ERR_TARGET_RANGE: return "target id outside [0, V)";
-        case RL_ERR_NONFINITE: return "non-finite loss";
+        case RL_ERR_NONFINITE: return "non-finite logits or loss";
         case RL_ERR_EMPTY_SEQ: return "response without mask=1 tokens";
         case RL_ERR_TIMEOUT: return "bounded wait ran out";
         case RL_ERR_UNSUPPORTED: return "unsupported request";
@@ -112,7 +119,9 @@ RL_LOSS_API rl_status rl_loss_create(const rl_loss_config *config, rl_loss_t *ou
     if (!config) return RL_ERR_INVALID_ARG;
     const rl_loss_config &c = *config;
     if (c.logits_dtype != RL_F32 && c.logits_dtype != RL_BF16) return RL_ERR_DTYPE;
-    if (c.vocab_size < 1 || c.group_size < 1 || c.max_tokens < 0 || c.max_seqs < 1) return RL_ERR_SHAPE;
+    if (c.vocab_size < 1 || c.vocab_size >= rlk::kMaxVocab || c.group_size < 1 || c.max_tokens < 0 ||
+        c.max_seqs < 1)
+        return RL_ERR_SHAPE;
     if (!(c.beta > 1.f) || !std::isfinite(c.beta)) return RL_ERR_INVALID_ARG;
     if (!(c.eps_low >= 0.f && c.eps_low < 1.f) || !(c.eps_high >= 0.f) || !std::isfinite(c.eps_high))
         return RL_ERR_INVALID_ARG;
@@ -148,6 +157,7 @@ RL_LOSS_API rl_status rl_loss_create(const rl_loss_config *config, rl_loss_t *ou
         return RL_ERR_CUDA;
     }
     h->launches = 0;
+    h->last_cuda_error = cudaSuccess;
     h->prof_capacity = 0;
     h->prof_calls = 0;
     *out = h;
@@ -171,7 +181,10 @@ RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t h, const rl_loss_inputs
                                                void *stream_ptr) {
     if (!h || !in || !out) return RL_ERR_INVALID_ARG;
     int cur = -1;
-    if (cudaGetDevice(&cur) != cudaSuccess) return RL_ERR_CUDA;
+    if (cudaError_t e0 = cudaGetDevice(&cur); e0 != cudaSuccess) {
+        h->last_cuda_error = e0;
+        return RL_ERR_CUDA;
+    }
     if (cur != h->device) return RL_ERR_DEVICE;
     const rl_loss_config &c = h->cfg;
     const int T = in->num_tokens, S = in->num_seqs, V = c.vocab_size;
@@ -213,21 +226,34 @@ RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t h, const rl_loss_inputs
     sp.seq_adv_out = out->seq_adv;
     sp.status = h->status;
 
+    rlk::TokenPrepParams tp{};
+    tp.logits = in->logits;
+    tp.ld_logits = in->ld_logits;
+    tp.logits_dtype = c.logits_dtype;
+    tp.targets = in->targets;
+    tp.logp_old = in->logp_old;
+    tp.logp_infer = in->logp_infer;
+    tp.mask = in->mask;
+    tp.cu_seqlens = in->cu_seqlens;
+    tp.num_seqs = S;
+    tp.num_tokens = T;
+    tp.vocab = V;
+    tp.seq_adv = h->seq_adv;
+    tp.seq_w = h->seq_w;
+    tp.c = h->consts;
+    tp.rec = h->tok_rec;
+    tp.meta = h->tok_meta;
+    tp.status = h->status;
+
     rlk::RowParams rp{};
     rp.logits = in->logits;
     rp.ld_logits = in->ld_logits;
     rp.dlogits = out->dlogits;
     rp.ld_dlogits = out->ld_dlogits;
-    rp.targets = in->targets;
-    rp.logp_old = in->logp_old;
-    rp.logp_infer = in->logp_infer;
-    rp.mask = in->mask;
-    rp.cu_seqlens = in->cu_seqlens;
-    rp.num_seqs = S;
+    rp.rec = h->tok_rec;
+    rp.meta = h->tok_meta;
     rp.num_tokens = T;
     rp.vocab = V;
-    rp.seq_adv = h->seq_adv;
-    rp.seq_w = h->seq_w;
     rp.c = h->consts;
     rp.logp_out = out->logp;
     rp.entropy_out = out->entropy ? out->entropy : h->tok_ent;
@@ -254,23 +280,31 @@ RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t h, const rl_loss_inputs
     rd.status = h->status;
 
     cudaError_t err;
+    auto failed = [&](cudaError_t e) {
+        h->last_cuda_error = e;
+        return RL_ERR_CUDA;
+    };
     mark(0, 0);
     err = rlk::launch_seg_prep(sp, stream);
     mark(0, 1);
-    if (err != cudaSuccess) return RL_ERR_CUDA;
+    if (err != cudaSuccess) return failed(err);
     mark(1, 0);
-    err = rlk::launch_row_loss(rp, c.logits_dtype, stream);
+    err = rlk::launch_token_prep(tp, stream);
     mark(1, 1);
-    if (err != cudaSuccess) return RL_ERR_CUDA;
+    if (err != cudaSuccess) return failed(err);
     mark(2, 0);
-    err = rlk::launch_seg_reduce(rd, stream);
+    err = rlk::launch_row_loss(rp, c.logits_dtype, stream);
     mark(2, 1);
-    if (err != cudaSuccess) return RL_ERR_CUDA;
+    if (err != cudaSuccess) return failed(err);
     mark(3, 0);
-    err = rlk::launch_final_reduce(rd, stream);
+    err = rlk::launch_seg_reduce(rd, stream);
     mark(3, 1);
-    if (err != cudaSuccess) return RL_ERR_CUDA;
-    h->launches += (T > 0) ? 4 : 3;
+    if (err != cudaSuccess) return failed(err);
+    mark(4, 0);
+    err = rlk::launch_final_reduce(rd, stream);
+    mark(4, 1);
+    if (err != cudaSuccess) return failed(err);
+    h->launches += (T > 0) ? 5 : 3;
     if (prof) h->prof_calls++;
     return RL_OK;
 }
@@ -279,9 +313,13 @@ RL_LOSS_API rl_status rl_loss_get_device_status(rl_loss_t h, void *stream_ptr, u
     if (!h || !bits) return RL_ERR_INVALID_ARG;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
     uint32_t v = 0;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return RL_ERR_CUDA;
-    if (cudaMemcpy(&v, h->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return RL_ERR_CUDA;
-    if (cudaMemset(h->status, 0, sizeof v) != cudaSuccess) return RL_ERR_CUDA;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) e = cudaMemcpy(&v, h->status, sizeof v, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof v);
+    if (e != cudaSuccess) {
+        h->last_cuda_error = e;
+        return RL_ERR_CUDA;
+    }
     *bits = v;
     return RL_OK;
 }
@@ -318,6 +356,11 @@ RL_LOSS_API rl_status rl_loss_profile_read(rl_loss_t h, rl_loss_profile *out) {
     h->prof_capacity = 0;
     h->prof_calls = 0;
     return RL_OK;
+}
+
+RL_LOSS_API const char *rl_loss_last_cuda_error(rl_loss_t h) {
+    if (!h) return "no handle";
+    return cudaGetErrorName(h->last_cuda_error);
 }
 
 RL_LOSS_API rl_status rl_loss_launch_count(rl_loss_t h, int64_t *count) {
@@ -375,7 +418,7 @@ extern "C" RL_LOSS_API rl_status rl_loss_forward_backward_noalloc(const rl_loss_
     if (!config || !inputs || !outputs) return RL_ERR_INVALID_ARG;
     const rl_loss_config &c = *config;
     if (c.logits_dtype != RL_F32 && c.logits_dtype != RL_BF16) return RL_ERR_DTYPE;
-    if (c.vocab_size < 1 || c.group_size < 1) return RL_ERR_SHAPE;
+    if (c.vocab_size < 1 || c.vocab_size >= rlk::kMaxVocab || c.group_size < 1) return RL_ERR_SHAPE;
     if (!(c.beta > 1.f) || !std::isfinite(c.beta)) return RL_ERR_INVALID_ARG;
     if (!(c.eps_low >= 0.f && c.eps_low < 1.f) || !(c.eps_high >= 0.f) || !std::isfinite(c.eps_high))
         return RL_ERR_INVALID_ARG;

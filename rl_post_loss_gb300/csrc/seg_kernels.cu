@@ -1,8 +1,10 @@
-// Per-response preparation and the fixed-order reductions of the loss.
+// Per-response preparation, per-token records and the fixed-order reductions.
 //
 // seg_prep:     |y_i|, A_i and w_i = 1/(S |y_i|) per response ("GLM-5: from
 //               Vibe Coding to Agentic Engineering", section 3.2: the
 //               group-normalised advantage and the 1/G, 1/|y_i| factors of Eq. (1)).
+// token_prep:   the row-independent part of each token's objective (rho, pop,
+//               mask, the advantage sign, z_y) packed for the row kernel.
 // seg_reduce:   per-response sums of the token objectives, in token order.
 // final_reduce: L = -sum_i w_i * (sum over response i), in response order.
 //
@@ -16,59 +18,85 @@ namespace rlk {
 namespace {
 
 constexpr int kPrepThreads = 256;
+constexpr int kTokenThreads = 256;
 constexpr int kReduceThreads = 256;
 
-// One block per group of G consecutive responses.
+// One block per response.
 __global__ void __launch_bounds__(kPrepThreads) seg_prep_kernel(SeqPrepParams p) {
     __shared__ int iscratch[32];
-    const int G = p.group_size;
-    const int g0 = blockIdx.x * G;
+    const int i = blockIdx.x;
     const int T = p.num_tokens;
-    for (int k = 0; k < G; ++k) {
-        const int i = g0 + k;
-        int b = __ldg(p.cu_seqlens + i), e = __ldg(p.cu_seqlens + i + 1);
-        const bool bad = (b < 0) || (e < b) || (e > T) || (i == 0 && b != 0) ||
-                         (i == p.num_seqs - 1 && e != T);
-        if (bad) {
-            if (threadIdx.x == 0) raise_status(p.status, RL_ERR_SEQLENS);
-            b = min(max(b, 0), T);
-            e = min(max(e, b), T);
-        }
-        int n = 0;
-        for (int t = b + threadIdx.x; t < e; t += blockDim.x) n += __ldg(p.mask + t) ? 1 : 0;
-        n = block_sum_i32(n, iscratch);
-        if (threadIdx.x == 0) {
-            p.seq_n[i] = n;
-            const double w = n > 0 ? 1.0 / ((double)p.num_seqs * (double)n) : 0.0;
-            p.seq_w64[i] = w;
-            p.seq_w[i] = (float)w;
-            if (n == 0) raise_status(p.status, RL_ERR_EMPTY_SEQ);
-        }
+    int b = __ldg(p.cu_seqlens + i), e = __ldg(p.cu_seqlens + i + 1);
+    const bool bad = (b < 0) || (e < b) || (e > T) || (i == 0 && b != 0) || (i == p.num_seqs - 1 && e != T);
+    if (bad) {
+        if (threadIdx.x == 0) raise_status(p.status, RL_ERR_SEQLENS);
+        b = min(max(b, 0), T);
+        e = min(max(e, b), T);
     }
+    int n = 0;
+#pragma unroll 4
+    for (int t = b + threadIdx.x; t < e; t += kPrepThreads) n += __ldg(p.mask + t) ? 1 : 0;
+    n = block_sum_i32(n, iscratch);
     if (threadIdx.x != 0) return;
-    // advantages in double, fixed order over the group, rounded once to fp32
+    p.seq_n[i] = n;
+    const double w = n > 0 ? 1.0 / ((double)p.num_seqs * (double)n) : 0.0;
+    p.seq_w64[i] = w;
+    p.seq_w[i] = (float)w;
+    if (n == 0) raise_status(p.status, RL_ERR_EMPTY_SEQ);
+    float a;
     if (p.adv_mode == RL_ADV_PER_SEQ) {
+        a = p.rewards_or_adv[i];
+    } else {
+        // group statistics in double, fixed order over the group's G rewards;
+        // every response of the group computes the same values
+        const int G = p.group_size;
+        const int g0 = (i / G) * G;
+        double mean = 0.0;
+        for (int k = 0; k < G; ++k) mean += (double)p.rewards_or_adv[g0 + k];
+        mean /= (double)G;
+        double ss = 0.0;
         for (int k = 0; k < G; ++k) {
-            const float a = p.rewards_or_adv[g0 + k];
-            p.seq_adv[g0 + k] = a;
-            if (p.seq_adv_out) p.seq_adv_out[g0 + k] = a;
+            const double c = (double)p.rewards_or_adv[g0 + k] - mean;
+            ss += c * c;
         }
-        return;
+        const double sd = sqrt(ss / (double)(p.std_unbiased ? G - 1 : G));
+        a = (float)(((double)p.rewards_or_adv[i] - mean) / (sd + (double)p.adv_eps));
     }
-    double mean = 0.0;
-    for (int k = 0; k < G; ++k) mean += (double)p.rewards_or_adv[g0 + k];
-    mean /= (double)G;
-    double ss = 0.0;
-    for (int k = 0; k < G; ++k) {
-        const double c = (double)p.rewards_or_adv[g0 + k] - mean;
-        ss += c * c;
+    p.seq_adv[i] = a;
+    if (p.seq_adv_out) p.seq_adv_out[i] = a;
+}
+
+// One thread per token.
+__global__ void __launch_bounds__(kTokenThreads) token_prep_kernel(TokenPrepParams p) {
+    const int t = blockIdx.x * kTokenThreads + threadIdx.x;
+    if (t >= p.num_tokens) return;
+    const int i = find_seq(p.cu_seqlens, p.num_seqs, t);
+    if (i < 0) raise_status(p.status, RL_ERR_SEQLENS);
+    const float A = i >= 0 ? p.seq_adv[i] : 0.f;
+    const float w = i >= 0 ? p.seq_w[i] : 0.f;
+    const int y = __ldg(p.targets + t);
+    const bool ok = (y >= 0) && (y < p.vocab);
+    if (!ok) raise_status(p.status, RL_ERR_TARGET_RANGE);
+    const bool m = (i >= 0) && (__ldg(p.mask + t) != 0);
+    const float lo = __ldg(p.logp_old + t);
+    const float d = __fsub_rn(lo, __ldg(p.logp_infer + t));  // ln rho, one fp32 subtraction
+    const bool in_bounds = (-p.c.ln_beta <= d) && (d <= p.c.ln_beta);
+    float zy = 0.f;
+    if (ok) {
+        const size_t off = (size_t)t * (size_t)p.ld_logits + (size_t)y;
+        if (p.logits_dtype == RL_F32) {
+            zy = __ldg(reinterpret_cast<const float *>(p.logits) + off);
+        } else {
+            const unsigned short b = __ldg(reinterpret_cast<const unsigned short *>(p.logits) + off);
+            zy = __uint_as_float(static_cast<uint32_t>(b) << 16);
+        }
     }
-    const double sd = sqrt(ss / (double)(p.std_unbiased ? G - 1 : G));
-    for (int k = 0; k < G; ++k) {
-        const float a = (float)(((double)p.rewards_or_adv[g0 + k] - mean) / (sd + (double)p.adv_eps));
-        p.seq_adv[g0 + k] = a;
-        if (p.seq_adv_out) p.seq_adv_out[g0 + k] = a;
-    }
+    float popA = 0.f;
+    if (m && ok && in_bounds) popA = (p.c.pop_indicator ? 1.f : expf(d)) * A;
+    const uint32_t pre = (in_bounds ? RL_FLAG_POP_IN_BOUNDS : 0u) | (m ? 0u : RL_FLAG_MASKED) |
+                         (ok ? 0u : RL_FLAG_BAD_TARGET) | (A > 0.f ? kPreAPos : 0u) | (A < 0.f ? kPreANeg : 0u);
+    p.rec[t] = make_float4(zy, lo, popA, w * popA);
+    p.meta[t] = (ok ? (uint32_t)y : 0u) | (pre << 24);
 }
 
 // One block per response: sums over its tokens in token order (strided per
@@ -83,7 +111,8 @@ __global__ void __launch_bounds__(kReduceThreads) seg_reduce_kernel(ReduceParams
     e = min(max(e, b), T);
     double obj = 0.0, ent = 0.0;
     int popped = 0, clipped = 0, masked = 0;
-    for (int t = b + threadIdx.x; t < e; t += blockDim.x) {
+#pragma unroll 4
+    for (int t = b + threadIdx.x; t < e; t += kReduceThreads) {
         const uint32_t f = p.flags[t];
         obj += (double)p.tok_obj[t];
         const bool m = !(f & RL_FLAG_MASKED);
@@ -146,7 +175,13 @@ __global__ void __launch_bounds__(kReduceThreads) final_reduce_kernel(ReducePara
 }  // namespace
 
 cudaError_t launch_seg_prep(const SeqPrepParams &p, cudaStream_t stream) {
-    seg_prep_kernel<<<p.num_seqs / p.group_size, kPrepThreads, 0, stream>>>(p);
+    seg_prep_kernel<<<p.num_seqs, kPrepThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_token_prep(const TokenPrepParams &p, cudaStream_t stream) {
+    if (p.num_tokens == 0) return cudaSuccess;
+    token_prep_kernel<<<(p.num_tokens + kTokenThreads - 1) / kTokenThreads, kTokenThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -57,8 +57,10 @@ def test_cases_reduced_length_full_vocab(case_id, n_prompts, lo, hi, dz_rows):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("V", [1, 2, 13, 1001, 4097, 40000])
+@pytest.mark.parametrize("V", [1, 2, 13, 1001, 4097, 8961, 40000, 70001, 151553, 200003])
 def test_ragged_vocab_and_padded_rows(dtype, V):
+    # covers every single-read configuration (C = 1, 2, 4, 8) and, at V = 200003,
+    # the two-pass kernel used beyond them
     lengths = _lengths(0, 1, 3, 40)
     ld = synthetic.padded_ld(V, dtype) + (64 if V % 2 else 0)
     b = synthetic.make_batch(0, "cuda", lengths=lengths, vocab=V, ld=ld, case_overrides={"dtype": dtype})
@@ -139,10 +141,14 @@ def test_bad_targets_are_flagged_and_excluded():
 
 
 def test_nonfinite_and_malformed_offsets_raise_device_bits():
-    b = synthetic.make_batch(0, "cuda", lengths=_lengths(0, 1, 4, 20))
-    b.logits[2, 5] = float("nan")
-    _, out, bits = _run(b)
-    assert bits & (1 << capi.CODES["RL_ERR_NONFINITE"])
+    for dtype, V in (("f32", 4096), ("bf16", 200003)):  # single-read and two-pass kernels
+        for bad in (float("nan"), float("inf")):
+            b = synthetic.make_batch(0, "cuda", lengths=_lengths(0, 1, 4, 20), vocab=V,
+                                     case_overrides={"dtype": dtype})
+            b.rewards_or_adv.fill_(1.0)  # zero advantages: the row adds nothing to the loss
+            b.logits[2, 5] = bad
+            _, out, bits = _run(b)
+            assert bits & (1 << capi.CODES["RL_ERR_NONFINITE"]), (dtype, bad)
     b = synthetic.make_batch(0, "cuda", lengths=_lengths(0, 1, 4, 20))
     b.cu_seqlens[-1] -= 1  # last response ends before num_tokens
     _, out, bits = _run(b)
@@ -200,6 +206,16 @@ def test_profile_and_launch_count():
     for _ in range(3):
         capi.run_batch(rl, b, out)
     prof = rl.profile_read()
-    assert set(prof) == {"seg_prep", "row_loss", "seg_reduce", "final_reduce"}
+    assert set(prof) == {"seg_prep", "token_prep", "row_loss", "seg_reduce", "final_reduce"}
     assert all(n == 3 and ms > 0 for n, ms in prof.values())
-    assert rl.launch_count() == 12
+    assert rl.launch_count() == 15
+
+
+def test_alternating_vocab_sizes_on_one_kernel_configuration():
+    # the same cluster configuration serves V = 151552 and V = 70001 with different
+    # shared-memory sizes; launching them in turn must keep working
+    for V in (151552, 70001, 151552, 70001):
+        b = synthetic.make_batch(2, "cuda", lengths=_lengths(2, 1, 8, 24), vocab=V)
+        _, out, bits = _run(b)
+        assert bits & ~(1 << capi.CODES["RL_ERR_EMPTY_SEQ"]) == 0
+        check_all(b, out, dz_rows=16)
