@@ -36,7 +36,7 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--case", type=int, default=1, choices=[0, 1, 2, 3])
+    ap.add_argument("--case", type=int, default=1, choices=[0, 1, 2, 3, 4])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -54,14 +54,15 @@ def dist_env():
     return rank, world, local
 
 
-def measured_peaks():
+def measured_peaks(key: str = "hbm_gbs"):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    fallback = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d[key]), "measured"
     except Exception:
-        return 6800.0, "fallback"
+        return fallback[key], "fallback"
 
 
 def kernel_traffic(kernel: str, case_id: int):
@@ -252,6 +253,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.case == 4:
+        return main_projection(args)
     import torch
     import torch.distributed as dist
     rank, world, local = dist_env()
@@ -362,6 +365,156 @@ def main():
                         "d2h_bytes_per_step": 8, "ms_per_step": e2e_ms},
                 "gpu_launches": launches, "device_status": capi.status_bits_to_names(bits),
                 "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def projection_sample_rate(pb, seconds: float):
+    """The fp64 oracle of the fused path on a bounded sample of rows: the
+    projection of each row (a float64 matmul), its loss terms, dL/dz and
+    dL/dh. Returns tokens/s, cores, sample description."""
+    import numpy as np
+    import oracle
+    b = pb.batch
+    H = pb.hidden_dim
+    p = oracle.LossParams(group_size=b.group, eps_low=b.eps_low, eps_high=b.eps_high, beta=b.beta,
+                          adv_eps=b.adv_eps, adv_mode=b.adv_mode)
+    a = {k: getattr(b, k).cpu().numpy() for k in
+         ("targets", "logp_old", "logp_infer", "mask", "cu_seqlens", "rewards_or_adv")}
+    bits = lambda t: t.contiguous().cpu().view(__import__("torch").int16).numpy().view(np.uint16)
+    w64 = oracle.bf16_bits_to_f64(bits(pb.w[:, :H]))
+    hb = bits(pb.hidden[:, :H])
+    n, adv, w = oracle.seq_prep(a["cu_seqlens"], a["mask"], a["rewards_or_adv"], p)
+    T = b.num_tokens
+    done, reps, k = 0, 0, 16
+    t0 = time.perf_counter()
+    while True:
+        ids = (np.arange(k) * 997 + reps * 131) % T
+        oracle.projection_rows(ids, hb, None, a["targets"], a["logp_old"], a["logp_infer"], a["mask"],
+                               a["cu_seqlens"], adv, w, p, want_dh=True, w64=w64)
+        done += k
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    cores = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
+    return done / dt, cores, (f"{done} rows of {T} (16 per batch, spread), fp64 projection + loss + dL/dz + dL/dh "
+                              f"per row (dL/dW excluded), {dt:.1f} s")
+
+
+def main_projection(args):
+    """Case 4: the fused sequence-chunked projection + loss, forward and backward."""
+    import torch
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    from rl_post_loss_gb300 import build as nvbuild
+    from rl_post_loss_gb300 import capi, synthetic
+    if not os.path.exists(nvbuild.LIB_PATH):
+        if rank == 0:
+            nvbuild.build()
+        else:
+            for _ in range(600):
+                if os.path.exists(nvbuild.LIB_PATH):
+                    break
+                time.sleep(1)
+    capi.load()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    over = {}
+    if args.prompts:
+        over["prompts"] = args.prompts
+    pb = synthetic.make_projection_batch("cuda", seed=rank, **over)
+    b = pb.batch
+    rl = capi.projection_handle(pb)
+    out = capi.alloc_projection_outputs(pb)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        capi.run_projection(rl, pb, out)
+    torch.cuda.synchronize()
+    bits = rl.device_status()
+    rl.profile_start(args.steps)
+    launches0 = rl.launch_count()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            capi.run_projection(rl, pb, out)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    ms = start.elapsed_time(stop)
+    launches = rl.launch_count() - launches0
+    prof = rl.profile_read()
+    if world > 1:
+        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    T, H, V = b.num_tokens, pb.hidden_dim, b.vocab
+    value = world * args.steps * T / (ms / 1e3)
+    flops_alg = 6.0 * T * V * H  # projection, dL/dh and dL/dW GEMMs
+    g_n, g_ms = prof["proj_gemm"]
+    gemm_flops = 2.0 * T * V * H / max(1, g_n // args.steps)  # per launch (one chunk)
+    peak, peak_kind = measured_peaks("bf16_tflops_sustained")
+    achieved = gemm_flops / (g_ms / max(1, g_n) / 1e3) / 1e12
+    step_tflops = flops_alg / (ms / args.steps / 1e3) / 1e12
+
+    host = {"hidden": pb.hidden.cpu().pin_memory(), "w": pb.w.cpu().pin_memory()}
+    host.update({k: getattr(b, k).cpu().pin_memory() for k in
+                 ("targets", "logp_old", "logp_infer", "mask", "cu_seqlens", "rewards_or_adv")})
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    loss_host = torch.empty(1, dtype=torch.float64).pin_memory()
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for k in range(args.e2e_steps + 1):
+        if k == 1:
+            torch.cuda.synchronize()
+            e_start.record(stream)
+        pb.hidden.copy_(host["hidden"], non_blocking=True)
+        pb.w.copy_(host["w"], non_blocking=True)
+        for name in ("targets", "logp_old", "logp_infer", "mask", "cu_seqlens", "rewards_or_adv"):
+            getattr(b, name).copy_(host[name], non_blocking=True)
+        capi.run_projection(rl, pb, out)
+        loss_host.copy_(out["loss_f64"], non_blocking=True)
+        stream.synchronize()
+        _ = float(loss_host[0])
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_stop) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, cores, desc = projection_sample_rate(pb, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        c = synthetic.PROJ_CASE
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": f"case 4: {c['name']}", "tokens": T, "responses": b.num_seqs,
+                           "group": b.group, "vocab": V, "hidden": H, "chunk_tokens": pb.chunk,
+                           "mask1_tokens": int(b.mask.sum().item()), "parallelism": "replicas",
+                           "l2": "no flush: each step streams W (1.9 GB) once per chunk and writes 3.7 GB of fp32 "
+                                 "logits per chunk, far larger than the 129 MB L2"},
+                "roofline": {"bound": "tensor", "kernel": "proj_gemm", "achieved": achieved, "peak": peak,
+                             "peak_kind": f"{peak_kind} sustained cuBLAS bf16 TFLOP/s", "unit": "TFLOP/s",
+                             "frac": achieved / peak, "traffic": kernel_traffic("proj_gemm", 4),
+                             "algorithmic_flops_per_launch": gemm_flops, "avg_launch_ms": g_ms / max(1, g_n)},
+                "step_tensor": {"algorithmic_tflops": step_tflops, "frac": step_tflops / peak,
+                                "executed_flops_per_step": flops_alg, "note": "6 N V H per step"},
+                "kernel_ms": {k: v[1] / args.steps for k, v in prof.items() if v[0]},
+                "clocks": clocks.summary(),
+                "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": 8, "ms_per_step": e2e_ms},
+                "gpu_launches": launches, "device_status": capi.status_bits_to_names(bits), "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -162,6 +162,48 @@ RL_LOSS_API rl_status rl_loss_destroy(rl_loss_t handle);
 RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t handle, const rl_loss_inputs *inputs,
                                                const rl_loss_outputs *outputs, void *stream);
 
+/* ---- Sequence-chunked output projection + loss ------------------------------
+ * "GLM-5: from Vibe Coding to Agentic Engineering", section 2.4.1, "Sequence-
+ * chunked output projection for peak memory reduction" (also "GLM-5 Notes",
+ * infrastructure item 5): the hidden states are split into chunks of rows; per
+ * chunk the output projection z = h W^T, the loss above and their backward run
+ * to completion before the next chunk reuses the buffers, so the logits of the
+ * whole sequence never exist at once. The projection runs on the tensor cores
+ * (tcgen05, bf16 inputs, fp32 accumulation) fused with the per-row softmax
+ * statistics; dZ is formed once per chunk in bf16; dH = dZ W and dW += dZ^T H
+ * are plain GEMMs computed with cuBLAS. */
+
+/* Allocates the fused projection path's buffers for hidden size `hidden_dim`
+ * (a multiple of 8) and chunks of `chunk_tokens` rows: a chunk_tokens x V fp32
+ * logits buffer, a chunk_tokens x V bf16 dL/dlogits buffer, the per-row
+ * statistics, and a cuBLAS handle with its own 64 MiB workspace. Requires a
+ * handle with logits_dtype RL_BF16 (else RL_ERR_UNSUPPORTED). Calling it again
+ * replaces the buffers. Synchronises the device. */
+RL_LOSS_API rl_status rl_loss_projection_setup(rl_loss_t handle, int32_t hidden_dim, int32_t chunk_tokens);
+
+/* logits[rows x V] (fp32, row stride ld_logits >= V, 16-byte aligned rows) =
+ * hidden[rows x H] (bf16, row stride ld_hidden) * w_lm[V x H]^T (bf16, row
+ * stride ld_w), the projection of the fused path on the tensor cores, for
+ * callers that want a chunk's logits themselves. Needs rl_loss_projection_setup
+ * (for H). Device pointers, 16-byte aligned, row strides a multiple of 16 bytes. */
+RL_LOSS_API rl_status rl_loss_projection_logits(rl_loss_t handle, const void *hidden, int64_t ld_hidden,
+                                                const void *w_lm, int64_t ld_w, int32_t rows, float *logits,
+                                                int64_t ld_logits, void *stream);
+
+/* The fused forward + backward over T = inputs->num_tokens rows of hidden
+ * states: hidden [T x H] bf16 (row stride ld_hidden), w_lm [V x H] bf16
+ * (row stride ld_w). Writes dhidden [T x H] bf16 (row stride ld_dhidden) =
+ * dL/dhidden and dw_lm [V x H] fp32 (row stride ld_dw, overwritten) = dL/dW.
+ * inputs->logits / ld_logits and outputs->dlogits / ld_dlogits are ignored;
+ * every other field of inputs / outputs means what it means for
+ * rl_loss_forward_backward. Needs rl_loss_projection_setup; allocates nothing.
+ * Device pointers, 16-byte aligned, row strides a multiple of 16 bytes. */
+RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(rl_loss_t handle, const void *hidden,
+                                                                int64_t ld_hidden, const void *w_lm, int64_t ld_w,
+                                                                const rl_loss_inputs *inputs, void *dhidden,
+                                                                int64_t ld_dhidden, float *dw_lm, int64_t ld_dw,
+                                                                const rl_loss_outputs *outputs, void *stream);
+
 /* Synchronises `stream`, returns the accumulated device status bits
  * (1u << code for each rl_status code raised) in *bits and clears them. */
 RL_LOSS_API rl_status rl_loss_get_device_status(rl_loss_t handle, void *stream, uint32_t *bits);

@@ -203,3 +203,48 @@ def thresholds_f32(beta: float, eps_low: float, eps_high: float):
     """(fl32(ln beta), fl32(ln(1 + eps_high)), fl32(ln(1 - eps_low)))."""
     lib = _load()
     return lib.oracle_ln_beta_f32(beta), lib.oracle_clip_hi_f32(eps_high), lib.oracle_clip_lo_f32(eps_low)
+
+
+# ---------------------------------------------------------------------------- fused projection
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) as float64 (exact: bf16 is the top half of binary32)."""
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def projection_logits(hidden_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
+    """z = h W^T in float64 from bf16 inputs ("GLM-5: from Vibe Coding to
+    Agentic Engineering", section 2.4.1: the output projection the chunked path
+    computes). A plain library matmul: the products of bf16 values are exact in
+    float64."""
+    return bf16_bits_to_f64(hidden_bits) @ bf16_bits_to_f64(w_bits).T
+
+
+def projection_rows(row_ids, hidden_bits, w_bits, targets, logp_old, logp_infer, mask, cu_seqlens, adv, w,
+                    p: LossParams, want_dz: bool = False, want_dh: bool = False, w64: np.ndarray | None = None):
+    """Per-token results of the loss on projected logits for ``row_ids``;
+    with ``want_dh`` also dL/dh_t = sum_v dL/dz_{t,v} W_v for those rows."""
+    ids = np.asarray(row_ids, np.int64)
+    W = bf16_bits_to_f64(w_bits) if w64 is None else w64
+    z = bf16_bits_to_f64(hidden_bits[ids]) @ W.T
+    out = rows(ids, np.ascontiguousarray(z), F64, W.shape[0], targets, logp_old, logp_infer, mask, cu_seqlens,
+               adv, w, p, want_dz=want_dz or want_dh)
+    if want_dh:
+        out["dh"] = out["dz"] @ W
+    return out
+
+
+def projection_forward_backward(hidden_bits, w_bits, batch: dict, p: LossParams) -> dict:
+    """Whole-batch oracle of the fused path (small sizes): loss, per-token
+    results, dL/dh = dZ W and dL/dW = dZ^T h, all in float64."""
+    cu = batch["cu_seqlens"]
+    T = int(cu[-1])
+    n, adv, w = seq_prep(cu, batch["mask"], batch["rewards_or_adv"], p)
+    W = bf16_bits_to_f64(w_bits)
+    h = bf16_bits_to_f64(hidden_bits[:T])
+    out = projection_rows(np.arange(T), hidden_bits, w_bits, batch["targets"], batch["logp_old"],
+                          batch["logp_infer"], batch["mask"], cu, adv, w, p, want_dh=True, w64=W)
+    out["dW"] = out["dz"].T @ h
+    out["loss"] = loss(cu, w, out["tok_obj"])
+    out["n_tokens"], out["adv"], out["w"] = n, adv, w
+    return out

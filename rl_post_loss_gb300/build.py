@@ -30,6 +30,12 @@ def nvcc() -> str:
     return "nvcc"
 
 
+def nvcc_path() -> str:
+    import shutil
+    n = nvcc()
+    return n if os.path.isabs(n) else (shutil.which(n) or "/usr/local/cuda/bin/nvcc")
+
+
 def sources() -> list[str]:
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
@@ -67,7 +73,9 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
         raise RuntimeError("nvcc failed:\n" + "\n".join(f"--- {s}\n{o}" for s, o in failed))
     if force or procs or _stale(LIB_PATH, objs):
         tmp = LIB_PATH + ".tmp%d" % os.getpid()
-        cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + ["-lcuda"]
+        cudalib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc_path()))), "lib64")
+        cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + [
+            "-lcublas", "-Xlinker", "-rpath=" + cudalib]
         subprocess.check_call(cmd)
         os.replace(tmp, LIB_PATH)
     return LIB_PATH

@@ -86,6 +86,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "rl_loss_version": ([], ctypes.c_int32),
         "rl_loss_forward_backward_noalloc": ([ctypes.POINTER(rl_loss_config), ctypes.POINTER(rl_loss_inputs),
                                               ctypes.POINTER(rl_loss_outputs), P, P], st),
+        "rl_loss_projection_setup": ([P, ctypes.c_int32, ctypes.c_int32], st),
+        "rl_loss_projection_logits": ([P, P, ctypes.c_int64, P, ctypes.c_int64, ctypes.c_int32, P, ctypes.c_int64,
+                                       P], st),
+        "rl_loss_fused_projection_forward_backward": ([P, P, ctypes.c_int64, P, ctypes.c_int64,
+                                                       ctypes.POINTER(rl_loss_inputs), P, ctypes.c_int64, P,
+                                                       ctypes.c_int64, ctypes.POINTER(rl_loss_outputs), P], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -163,6 +169,22 @@ def rl_loss_last_cuda_error(handle) -> str:
     return load().rl_loss_last_cuda_error(handle).decode()
 
 
+def rl_loss_projection_setup(handle, hidden_dim: int, chunk_tokens: int) -> None:
+    _check(load().rl_loss_projection_setup(handle, hidden_dim, chunk_tokens), "rl_loss_projection_setup")
+
+
+def rl_loss_projection_logits(handle, hidden, ld_hidden, w_lm, ld_w, rows, logits, ld_logits, stream) -> int:
+    return load().rl_loss_projection_logits(handle, hidden, ld_hidden, w_lm, ld_w, rows, logits, ld_logits,
+                                            ctypes.c_void_p(stream))
+
+
+def rl_loss_fused_projection_forward_backward(handle, hidden, ld_hidden, w_lm, ld_w, inputs, dhidden, ld_dhidden,
+                                              dw_lm, ld_dw, outputs, stream) -> int:
+    return load().rl_loss_fused_projection_forward_backward(handle, hidden, ld_hidden, w_lm, ld_w,
+                                                            ctypes.byref(inputs), dhidden, ld_dhidden, dw_lm, ld_dw,
+                                                            ctypes.byref(outputs), ctypes.c_void_p(stream))
+
+
 def rl_loss_version() -> int:
     return int(load().rl_loss_version())
 
@@ -213,6 +235,40 @@ class RlLoss:
         if code == CODES["RL_ERR_CUDA"]:
             raise RlLossError(code, "rl_loss_forward_backward (%s)" % rl_loss_last_cuda_error(self.handle))
         _check(code, "rl_loss_forward_backward")
+
+    def _raise(self, code: int, what: str):
+        if code == CODES["RL_ERR_CUDA"]:
+            raise RlLossError(code, "%s (%s)" % (what, rl_loss_last_cuda_error(self.handle)))
+        _check(code, what)
+
+    def projection_setup(self, hidden_dim: int, chunk_tokens: int) -> None:
+        rl_loss_projection_setup(self.handle, hidden_dim, chunk_tokens)
+
+    def projection_logits(self, hidden, w_lm, rows: int, logits, stream=None) -> None:
+        """logits[:rows] (fp32) = hidden[:rows] @ w_lm^T on the tensor cores."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        self._raise(rl_loss_projection_logits(self.handle, _ptr(hidden), hidden.stride(0), _ptr(w_lm), w_lm.stride(0),
+                                              rows, _ptr(logits), logits.stride(0), stream),
+                    "rl_loss_projection_logits")
+
+    def fused_projection_forward_backward(self, hidden, w_lm, targets, logp_old, logp_infer, mask, cu_seqlens,
+                                          rewards_or_adv, *, loss, dhidden, dw_lm, loss_f64=None, logp=None,
+                                          entropy=None, flags=None, seq_adv=None, counts=None, mean_entropy=None,
+                                          stream=None) -> None:
+        import torch
+        T = int(targets.shape[0])
+        S = int(cu_seqlens.shape[0]) - 1
+        inp = rl_loss_inputs(T, S, 0, None, _ptr(targets), _ptr(logp_old), _ptr(logp_infer), _ptr(mask),
+                             _ptr(cu_seqlens), _ptr(rewards_or_adv))
+        out = rl_loss_outputs(_ptr(loss), _ptr(loss_f64), None, 0, _ptr(logp), _ptr(entropy), _ptr(flags),
+                              _ptr(seq_adv), _ptr(counts), _ptr(mean_entropy))
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        self._raise(rl_loss_fused_projection_forward_backward(
+            self.handle, _ptr(hidden), hidden.stride(0), _ptr(w_lm), w_lm.stride(0), inp, _ptr(dhidden),
+            dhidden.stride(0), _ptr(dw_lm), dw_lm.stride(0), out, stream), "rl_loss_fused_projection_forward_backward")
 
     def device_status(self, stream=None) -> int:
         import torch
@@ -269,4 +325,29 @@ def run_batch(rl: RlLoss, batch, outputs: dict, stream=None) -> dict:
     """One forward+backward of ``batch`` into ``outputs`` (asynchronous)."""
     rl.forward_backward(batch.logits, batch.targets, batch.logp_old, batch.logp_infer, batch.mask,
                         batch.cu_seqlens, batch.rewards_or_adv, stream=stream, **outputs)
+    return outputs
+
+
+def projection_handle(pb, max_tokens: int | None = None, **overrides) -> RlLoss:
+    """A bf16 handle with the fused projection path set up for a ``synthetic.ProjBatch``."""
+    rl = handle_for_batch(pb.batch, max_tokens=max_tokens, **overrides)
+    rl.projection_setup(pb.hidden_dim, pb.chunk)
+    return rl
+
+
+def alloc_projection_outputs(pb) -> dict:
+    import torch
+    b = pb.batch
+    out = alloc_outputs(b, ld=8)
+    del out["dlogits"]
+    dev = pb.hidden.device
+    out["dhidden"] = torch.empty_like(pb.hidden)
+    out["dw_lm"] = torch.empty((pb.w.shape[0], pb.w.shape[1]), dtype=torch.float32, device=dev)
+    return out
+
+
+def run_projection(rl: RlLoss, pb, outputs: dict, stream=None) -> dict:
+    b = pb.batch
+    rl.fused_projection_forward_backward(pb.hidden, pb.w, b.targets, b.logp_old, b.logp_infer, b.mask, b.cu_seqlens,
+                                         b.rewards_or_adv, stream=stream, **outputs)
     return outputs

@@ -193,8 +193,9 @@ struct SeqPrepParams {
 };
 
 struct TokenPrepParams {
-    const void *logits;
+    const void *logits;  // row i holds token row0 + i
     int64_t ld_logits;
+    int32_t row0, rows;  // tokens [row0, row0 + rows) are prepared
     int32_t logits_dtype;
     const int32_t *targets;
     const float *logp_old;

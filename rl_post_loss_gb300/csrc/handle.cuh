@@ -1,0 +1,87 @@
+// The library handle behind rl_loss_t (internal; shared by the C-ABI files).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <vector>
+
+#include "common.cuh"
+
+// Kernel classes timed by rl_loss_profile_start / rl_loss_profile_read.
+enum RlKernelClass {
+    kSegPrep = 0,
+    kTokenPrep,
+    kRowLoss,
+    kSegReduce,
+    kFinalReduce,
+    kProjGemm,
+    kProjRows,
+    kLibGemm,  // the two cuBLAS GEMMs of the projection backward
+    kNumKernels
+};
+static const char *const kKernelNames[kNumKernels] = {"seg_prep",     "token_prep", "row_loss",  "seg_reduce",
+                                                      "final_reduce", "proj_gemm",  "proj_rows", "cublas_gemm"};
+constexpr size_t kProfSlotsPerCall = 160;  // enough for a projection call of 32 chunks
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct rl_loss_handle_s {
+    rl_loss_config cfg;
+    int device;
+    rlk::LossConsts consts;
+    // workspace (one cudaMalloc, carved below)
+    void *ws;
+    size_t ws_bytes;
+    uint32_t *status;
+    float *seq_adv, *seq_w;
+    double *seq_w64, *seq_obj, *seq_ent;
+    int32_t *seq_n, *seq_cnt;
+    float *tok_obj, *tok_ent;
+    uint8_t *tok_flags;
+    float4 *tok_rec;
+    uint32_t *tok_meta;
+    float *loss_scratch;
+    // bookkeeping
+    int64_t launches;
+    cudaError_t last_cuda_error;  // the CUDA error behind the last RL_ERR_CUDA of this handle
+
+    // profiling: one event pair per timed launch
+    std::vector<cudaEvent_t> prof_events;  // [capacity][2]
+    std::vector<int> prof_cls;             // kernel class of each used slot
+    int prof_capacity = 0, prof_used = 0;
+
+    // fused projection path (rl_loss_projection_setup)
+    int32_t proj_hidden = 0, proj_chunk = 0, proj_n_tiles = 0;
+    int64_t proj_ldz = 0, proj_lddz = 0;
+    void *proj_ws = nullptr;  // one cudaMalloc: logits chunk, dZ chunk, statistics
+    float *proj_z = nullptr;
+    void *proj_dz = nullptr;
+    float4 *proj_stats = nullptr;
+    void *cublas = nullptr;     // cublasHandle_t
+    void *cublas_ws = nullptr;  // its workspace
+    size_t cublas_ws_bytes = 0;
+
+    bool prof_reset(size_t slots) {
+        for (cudaEvent_t e : prof_events) cudaEventDestroy(e);
+        prof_events.assign(2 * slots, nullptr);
+        prof_cls.assign(slots, 0);
+        prof_capacity = 0;
+        prof_used = 0;
+        for (auto &e : prof_events)
+            if (cudaEventCreate(&e) != cudaSuccess) return false;
+        prof_capacity = (int)slots;
+        return true;
+    }
+    // Returns the slot to close with prof_end, or -1 when not recording.
+    int prof_begin(int cls, cudaStream_t stream) {
+        if (prof_used >= prof_capacity) return -1;
+        const int s = prof_used++;
+        prof_cls[s] = cls;
+        cudaEventRecord(prof_events[2 * (size_t)s], stream);
+        return s;
+    }
+    void prof_end(int slot, cudaStream_t stream) {
+        if (slot >= 0) cudaEventRecord(prof_events[2 * (size_t)slot + 1], stream);
+    }
+    void proj_release();  // defined with the projection path
+};

@@ -1,0 +1,290 @@
+// C ABI of the fused sequence-chunked output projection + loss ("GLM-5: from
+// Vibe Coding to Agentic Engineering", section 2.4.1, "Sequence-chunked output
+// projection for peak memory reduction"; "GLM-5 Notes", infrastructure item 5):
+// the hidden states are split into chunks of rows; per chunk the projection,
+// the loss of Eq. (1) (section 3.2) and its backward are computed and the
+// chunk's buffers reused, so logits for the whole sequence never exist.
+//
+// Per chunk c of rows [r0, r0 + m):
+//   proj_gemm   Z_c = H_c W^T (tcgen05, fp32) + per-row, per-256-column softmax statistics
+//   token_prep  per-token records (z_y read from Z_c)
+//   proj_rows   statistics merged per row in tile order, token objective, dZ_c (bf16)
+//   cuBLAS      dH_c = dZ_c W (bf16 out)        -- plain GEMMs: library routines
+//               dW  (+)= dZ_c^T H_c (fp32; overwritten by chunk 0, accumulated after)
+// then the fixed-order per-response and batch reductions give the loss.
+#include <cublas_v2.h>
+
+#include <cmath>
+
+#include "handle.cuh"
+#include "proj.cuh"
+
+void rl_loss_handle_s::proj_release() {
+    if (cublas) cublasDestroy(reinterpret_cast<cublasHandle_t>(cublas));
+    if (cublas_ws) cudaFree(cublas_ws);
+    if (proj_ws) cudaFree(proj_ws);
+    cublas = nullptr;
+    cublas_ws = nullptr;
+    proj_ws = nullptr;
+    proj_z = nullptr;
+    proj_dz = nullptr;
+    proj_stats = nullptr;
+    proj_hidden = proj_chunk = proj_n_tiles = 0;
+}
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+rl_status cuda_fail(rl_loss_handle_s *h, cudaError_t e) {
+    h->last_cuda_error = e;
+    return RL_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+RL_LOSS_API rl_status rl_loss_projection_setup(rl_loss_t h, int32_t hidden_dim, int32_t chunk_tokens) {
+    if (!h) return RL_ERR_INVALID_ARG;
+    if (hidden_dim < 1 || hidden_dim % 8 != 0 || chunk_tokens < 1) return RL_ERR_SHAPE;
+    if (h->cfg.logits_dtype != RL_BF16) return RL_ERR_UNSUPPORTED;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) return RL_ERR_DEVICE;
+    cudaDeviceSynchronize();
+    h->proj_release();
+    const int64_t V = h->cfg.vocab_size;
+    const int tile = rlk::proj_gemm_tile_cols();
+    const int n_tiles = (int)((V + tile - 1) / tile);
+    const int64_t ldz = (V + 3) / 4 * 4, lddz = (V + 7) / 8 * 8;
+    const size_t z_bytes = align_up((size_t)chunk_tokens * ldz * 4, 256);
+    const size_t dz_bytes = align_up((size_t)chunk_tokens * lddz * 2, 256);
+    const size_t st_bytes = align_up((size_t)chunk_tokens * n_tiles * sizeof(float4), 256);
+    void *ws = nullptr;
+    cudaError_t e = cudaMalloc(&ws, z_bytes + dz_bytes + st_bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return cuda_fail(h, e);
+    }
+    h->proj_ws = ws;
+    h->proj_z = reinterpret_cast<float *>(ws);
+    h->proj_dz = reinterpret_cast<char *>(ws) + z_bytes;
+    h->proj_stats = reinterpret_cast<float4 *>(reinterpret_cast<char *>(ws) + z_bytes + dz_bytes);
+    cublasHandle_t cb = nullptr;
+    if (cublasCreate(&cb) != CUBLAS_STATUS_SUCCESS) {
+        h->proj_release();
+        return RL_ERR_CUDA;
+    }
+    h->cublas = cb;
+    // a workspace of its own, so that later calls allocate nothing
+    h->cublas_ws_bytes = size_t(64) << 20;
+    e = cudaMalloc(&h->cublas_ws, h->cublas_ws_bytes);
+    if (e != cudaSuccess || cublasSetWorkspace(cb, h->cublas_ws, h->cublas_ws_bytes) != CUBLAS_STATUS_SUCCESS ||
+        cublasSetMathMode(cb, CUBLAS_DEFAULT_MATH) != CUBLAS_STATUS_SUCCESS) {
+        cudaGetLastError();
+        h->proj_release();
+        return RL_ERR_CUDA;
+    }
+    h->proj_hidden = hidden_dim;
+    h->proj_chunk = chunk_tokens;
+    h->proj_n_tiles = n_tiles;
+    h->proj_ldz = ldz;
+    h->proj_lddz = lddz;
+    return RL_OK;
+}
+
+RL_LOSS_API rl_status rl_loss_projection_logits(rl_loss_t h, const void *hidden, int64_t ld_hidden, const void *w_lm,
+                                                int64_t ld_w, int32_t rows, float *logits, int64_t ld_logits,
+                                                void *stream_ptr) {
+    if (!h || !hidden || !w_lm || !logits) return RL_ERR_INVALID_ARG;
+    if (h->proj_hidden == 0) return RL_ERR_INVALID_ARG;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) return RL_ERR_DEVICE;
+    const int H = h->proj_hidden, V = h->cfg.vocab_size;
+    if (rows < 0 || ld_hidden < H || ld_w < H || ld_logits < V) return RL_ERR_SHAPE;
+    if (!aligned16(hidden) || !aligned16(w_lm) || (ld_hidden * 2) % 16 || (ld_w * 2) % 16 ||
+        (reinterpret_cast<uintptr_t>(logits) & 15u) || (ld_logits * 4) % 16)
+        return RL_ERR_ALIGNMENT;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+    rlk::ProjGemmParams gp{};
+    gp.M = rows;
+    gp.N = V;
+    gp.K = H;
+    gp.z = logits;
+    gp.ldz = ld_logits;
+    gp.stats = nullptr;
+    gp.status = h->status;
+    const int slot = h->prof_begin(kProjGemm, stream);
+    cudaError_t e = rlk::launch_proj_gemm(hidden, ld_hidden, w_lm, ld_w, gp, stream);
+    h->prof_end(slot, stream);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+    h->launches += rows > 0 ? 1 : 0;
+    return RL_OK;
+}
+
+RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(
+    rl_loss_t h, const void *hidden, int64_t ld_hidden, const void *w_lm, int64_t ld_w, const rl_loss_inputs *in,
+    void *dhidden, int64_t ld_dhidden, float *dw_lm, int64_t ld_dw, const rl_loss_outputs *out, void *stream_ptr) {
+    if (!h || !in || !out) return RL_ERR_INVALID_ARG;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) return RL_ERR_DEVICE;
+    if (h->proj_hidden == 0) return RL_ERR_INVALID_ARG;
+    const rl_loss_config &c = h->cfg;
+    const int T = in->num_tokens, S = in->num_seqs, V = c.vocab_size, H = h->proj_hidden;
+    if (T < 0 || S < 1 || S % c.group_size != 0) return RL_ERR_SHAPE;
+    if (T > c.max_tokens || S > c.max_seqs) return RL_ERR_CAPACITY;
+    if (!in->cu_seqlens || !in->rewards_or_adv || !out->loss) return RL_ERR_INVALID_ARG;
+    if (T > 0) {
+        if (!hidden || !w_lm || !dhidden || !dw_lm || !in->targets || !in->logp_old || !in->logp_infer || !in->mask)
+            return RL_ERR_INVALID_ARG;
+        if (ld_hidden < H || ld_w < H || ld_dhidden < H || ld_dw < H) return RL_ERR_SHAPE;
+        if (!aligned16(hidden) || !aligned16(w_lm) || !aligned16(dhidden) || !aligned16(dw_lm) ||
+            (ld_hidden * 2) % 16 || (ld_w * 2) % 16 || (ld_dhidden * 2) % 16 || (ld_dw * 4) % 16)
+            return RL_ERR_ALIGNMENT;
+    }
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+    cublasHandle_t cb = reinterpret_cast<cublasHandle_t>(h->cublas);
+    if (cublasSetStream(cb, stream) != CUBLAS_STATUS_SUCCESS) return RL_ERR_CUDA;
+
+    rlk::SeqPrepParams sp{};
+    sp.cu_seqlens = in->cu_seqlens;
+    sp.mask = in->mask;
+    sp.rewards_or_adv = in->rewards_or_adv;
+    sp.num_seqs = S;
+    sp.num_tokens = T;
+    sp.group_size = c.group_size;
+    sp.adv_mode = c.adv_mode;
+    sp.std_unbiased = c.std_unbiased;
+    sp.adv_eps = c.adv_eps;
+    sp.seq_adv = h->seq_adv;
+    sp.seq_w = h->seq_w;
+    sp.seq_w64 = h->seq_w64;
+    sp.seq_n = h->seq_n;
+    sp.seq_adv_out = out->seq_adv;
+    sp.status = h->status;
+    int slot = h->prof_begin(kSegPrep, stream);
+    cudaError_t e = rlk::launch_seg_prep(sp, stream);
+    h->prof_end(slot, stream);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+    int64_t launches = 1;
+
+    float *entropy = out->entropy ? out->entropy : h->tok_ent;
+    uint8_t *flags = out->flags ? out->flags : h->tok_flags;
+    const float one = 1.f, zero = 0.f;
+    for (int r0 = 0, ci = 0; r0 < T; r0 += h->proj_chunk, ++ci) {
+        const int m = T - r0 < h->proj_chunk ? T - r0 : h->proj_chunk;
+        const char *hc = reinterpret_cast<const char *>(hidden) + (size_t)r0 * ld_hidden * 2;
+
+        rlk::ProjGemmParams gp{};
+        gp.M = m;
+        gp.N = V;
+        gp.K = H;
+        gp.z = h->proj_z;
+        gp.ldz = h->proj_ldz;
+        gp.stats = h->proj_stats;
+        gp.status = h->status;
+        slot = h->prof_begin(kProjGemm, stream);
+        e = rlk::launch_proj_gemm(hc, ld_hidden, w_lm, ld_w, gp, stream);
+        h->prof_end(slot, stream);
+        if (e != cudaSuccess) return cuda_fail(h, e);
+
+        rlk::TokenPrepParams tp{};
+        tp.logits = h->proj_z;
+        tp.ld_logits = h->proj_ldz;
+        tp.row0 = r0;
+        tp.rows = m;
+        tp.logits_dtype = RL_F32;
+        tp.targets = in->targets;
+        tp.logp_old = in->logp_old;
+        tp.logp_infer = in->logp_infer;
+        tp.mask = in->mask;
+        tp.cu_seqlens = in->cu_seqlens;
+        tp.num_seqs = S;
+        tp.num_tokens = T;
+        tp.vocab = V;
+        tp.seq_adv = h->seq_adv;
+        tp.seq_w = h->seq_w;
+        tp.c = h->consts;
+        tp.rec = h->tok_rec;
+        tp.meta = h->tok_meta;
+        tp.status = h->status;
+        slot = h->prof_begin(kTokenPrep, stream);
+        e = rlk::launch_token_prep(tp, stream);
+        h->prof_end(slot, stream);
+        if (e != cudaSuccess) return cuda_fail(h, e);
+
+        rlk::ProjRowParams rp{};
+        rp.z = h->proj_z;
+        rp.ldz = h->proj_ldz;
+        rp.stats = h->proj_stats;
+        rp.n_tiles = h->proj_n_tiles;
+        rp.dz = h->proj_dz;
+        rp.lddz = h->proj_lddz;
+        rp.row0 = r0;
+        rp.rows = m;
+        rp.vocab = V;
+        rp.rec = h->tok_rec;
+        rp.meta = h->tok_meta;
+        rp.c = h->consts;
+        rp.logp_out = out->logp;
+        rp.entropy_out = entropy;
+        rp.flags_out = flags;
+        rp.tok_obj = h->tok_obj;
+        rp.status = h->status;
+        slot = h->prof_begin(kProjRows, stream);
+        e = rlk::launch_proj_rows(rp, stream);
+        h->prof_end(slot, stream);
+        if (e != cudaSuccess) return cuda_fail(h, e);
+        launches += 3;
+
+        // dH_c [m x H] = dZ_c [m x V] W [V x H]; column-major view: dH^T = W^T dZ^T
+        char *dhc = reinterpret_cast<char *>(dhidden) + (size_t)r0 * ld_dhidden * 2;
+        slot = h->prof_begin(kLibGemm, stream);
+        cublasStatus_t cs =
+            cublasGemmEx(cb, CUBLAS_OP_N, CUBLAS_OP_N, H, m, V, &one, w_lm, CUDA_R_16BF, (int)ld_w, h->proj_dz,
+                         CUDA_R_16BF, (int)h->proj_lddz, &zero, dhc, CUDA_R_16BF, (int)ld_dhidden, CUBLAS_COMPUTE_32F,
+                         CUBLAS_GEMM_DEFAULT);
+        // dW [V x H] (+)= dZ_c^T [V x m] H_c [m x H]; column-major view: dW^T = H_c^T dZ_c
+        if (cs == CUBLAS_STATUS_SUCCESS)
+            cs = cublasGemmEx(cb, CUBLAS_OP_N, CUBLAS_OP_T, H, V, m, &one, hc, CUDA_R_16BF, (int)ld_hidden,
+                              h->proj_dz, CUDA_R_16BF, (int)h->proj_lddz, ci == 0 ? &zero : &one, dw_lm, CUDA_R_32F,
+                              (int)ld_dw, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+        h->prof_end(slot, stream);
+        if (cs != CUBLAS_STATUS_SUCCESS) return RL_ERR_CUDA;
+    }
+
+    if (T == 0 && dw_lm) {  // no chunk ran: the weight gradient is zero
+        e = cudaMemset2DAsync(dw_lm, (size_t)ld_dw * 4, 0, (size_t)H * 4, (size_t)V, stream);
+        if (e != cudaSuccess) return cuda_fail(h, e);
+    }
+
+    rlk::ReduceParams rd{};
+    rd.cu_seqlens = in->cu_seqlens;
+    rd.num_seqs = S;
+    rd.num_tokens = T;
+    rd.tok_obj = h->tok_obj;
+    rd.entropy = entropy;
+    rd.flags = flags;
+    rd.seq_w64 = h->seq_w64;
+    rd.seq_n = h->seq_n;
+    rd.seq_obj = h->seq_obj;
+    rd.seq_ent = h->seq_ent;
+    rd.seq_cnt = h->seq_cnt;
+    rd.loss = out->loss;
+    rd.loss_f64 = out->loss_f64;
+    rd.counts = out->counts;
+    rd.mean_entropy = out->mean_entropy;
+    rd.status = h->status;
+    slot = h->prof_begin(kSegReduce, stream);
+    e = rlk::launch_seg_reduce(rd, stream);
+    h->prof_end(slot, stream);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+    slot = h->prof_begin(kFinalReduce, stream);
+    e = rlk::launch_final_reduce(rd, stream);
+    h->prof_end(slot, stream);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+    h->launches += launches + 2;
+    return RL_OK;
+}
+
+}  // extern "C"

@@ -10,38 +10,7 @@
 
 #include "common.cuh"
 
-namespace {
-
-constexpr int kNumKernels = 5;
-const char *const kKernelNames[kNumKernels] = {"seg_prep", "token_prep", "row_loss", "seg_reduce", "final_reduce"};
-
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-}  // namespace
-
-struct rl_loss_handle_s {
-    rl_loss_config cfg;
-    int device;
-    rlk::LossConsts consts;
-    // workspace (one cudaMalloc, carved below)
-    void *ws;
-    size_t ws_bytes;
-    uint32_t *status;
-    float *seq_adv, *seq_w;
-    double *seq_w64, *seq_obj, *seq_ent;
-    int32_t *seq_n, *seq_cnt;
-    float *tok_obj, *tok_ent;
-    uint8_t *tok_flags;
-    float4 *tok_rec;
-    uint32_t *tok_meta;
-    float *loss_scratch;
-    // bookkeeping
-    int64_t launches;
-    cudaError_t last_cuda_error;  // the CUDA error behind the last RL_ERR_CUDA of this handle
-    // profiling
-    int32_t prof_capacity, prof_calls;
-    std::vector<cudaEvent_t> prof_events;  // [capacity][kernels][2]
-};
+#include "handle.cuh"
 
 static size_t workspace_layout(const rl_loss_config &c, rl_loss_handle_s *h, char *base) {
     const size_t S = (size_t)c.max_seqs, T = (size_t)c.max_tokens;
@@ -158,8 +127,6 @@ RL_LOSS_API rl_status rl_loss_create(const rl_loss_config *config, rl_loss_t *ou
     }
     h->launches = 0;
     h->last_cuda_error = cudaSuccess;
-    h->prof_capacity = 0;
-    h->prof_calls = 0;
     *out = h;
     return RL_OK;
 }
@@ -171,6 +138,7 @@ RL_LOSS_API rl_status rl_loss_destroy(rl_loss_t h) {
     if (cur != h->device) cudaSetDevice(h->device);
     cudaDeviceSynchronize();
     for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
+    h->proj_release();
     cudaError_t err = cudaFree(h->ws);
     if (cur != h->device && cur >= 0) cudaSetDevice(cur);
     delete h;
@@ -203,12 +171,6 @@ RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t h, const rl_loss_inputs
     }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
 
-    const bool prof = h->prof_calls < h->prof_capacity;
-    cudaEvent_t *ev = prof ? &h->prof_events[(size_t)h->prof_calls * kNumKernels * 2] : nullptr;
-    auto mark = [&](int k, int which) {
-        if (prof) cudaEventRecord(ev[2 * k + which], stream);
-    };
-
     rlk::SeqPrepParams sp{};
     sp.cu_seqlens = in->cu_seqlens;
     sp.mask = in->mask;
@@ -229,6 +191,8 @@ RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t h, const rl_loss_inputs
     rlk::TokenPrepParams tp{};
     tp.logits = in->logits;
     tp.ld_logits = in->ld_logits;
+    tp.row0 = 0;
+    tp.rows = T;
     tp.logits_dtype = c.logits_dtype;
     tp.targets = in->targets;
     tp.logp_old = in->logp_old;
@@ -284,28 +248,27 @@ RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t h, const rl_loss_inputs
         h->last_cuda_error = e;
         return RL_ERR_CUDA;
     };
-    mark(0, 0);
+    int slot = h->prof_begin(kSegPrep, stream);
     err = rlk::launch_seg_prep(sp, stream);
-    mark(0, 1);
+    h->prof_end(slot, stream);
     if (err != cudaSuccess) return failed(err);
-    mark(1, 0);
+    slot = h->prof_begin(kTokenPrep, stream);
     err = rlk::launch_token_prep(tp, stream);
-    mark(1, 1);
+    h->prof_end(slot, stream);
     if (err != cudaSuccess) return failed(err);
-    mark(2, 0);
+    slot = h->prof_begin(kRowLoss, stream);
     err = rlk::launch_row_loss(rp, c.logits_dtype, stream);
-    mark(2, 1);
+    h->prof_end(slot, stream);
     if (err != cudaSuccess) return failed(err);
-    mark(3, 0);
+    slot = h->prof_begin(kSegReduce, stream);
     err = rlk::launch_seg_reduce(rd, stream);
-    mark(3, 1);
+    h->prof_end(slot, stream);
     if (err != cudaSuccess) return failed(err);
-    mark(4, 0);
+    slot = h->prof_begin(kFinalReduce, stream);
     err = rlk::launch_final_reduce(rd, stream);
-    mark(4, 1);
+    h->prof_end(slot, stream);
     if (err != cudaSuccess) return failed(err);
     h->launches += (T > 0) ? 5 : 3;
-    if (prof) h->prof_calls++;
     return RL_OK;
 }
 
@@ -326,15 +289,7 @@ RL_LOSS_API rl_status rl_loss_get_device_status(rl_loss_t h, void *stream_ptr, u
 
 RL_LOSS_API rl_status rl_loss_profile_start(rl_loss_t h, int32_t max_calls) {
     if (!h || max_calls < 0) return RL_ERR_INVALID_ARG;
-    for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
-    h->prof_events.clear();
-    h->prof_capacity = 0;
-    h->prof_calls = 0;
-    h->prof_events.resize((size_t)max_calls * kNumKernels * 2, nullptr);
-    for (auto &e : h->prof_events)
-        if (cudaEventCreate(&e) != cudaSuccess) return RL_ERR_CUDA;
-    h->prof_capacity = max_calls;
-    return RL_OK;
+    return h->prof_reset((size_t)max_calls * kProfSlotsPerCall) ? RL_OK : RL_ERR_CUDA;
 }
 
 RL_LOSS_API rl_status rl_loss_profile_read(rl_loss_t h, rl_loss_profile *out) {
@@ -342,19 +297,16 @@ RL_LOSS_API rl_status rl_loss_profile_read(rl_loss_t h, rl_loss_profile *out) {
     std::memset(out, 0, sizeof *out);
     out->num_kernels = kNumKernels;
     for (int k = 0; k < kNumKernels; ++k) std::snprintf(out->names[k], sizeof out->names[k], "%s", kKernelNames[k]);
-    for (int call = 0; call < h->prof_calls; ++call) {
-        for (int k = 0; k < kNumKernels; ++k) {
-            cudaEvent_t a = h->prof_events[((size_t)call * kNumKernels + k) * 2];
-            cudaEvent_t b = h->prof_events[((size_t)call * kNumKernels + k) * 2 + 1];
-            if (cudaEventSynchronize(b) != cudaSuccess) return RL_ERR_CUDA;
-            float ms = 0.f;
-            if (cudaEventElapsedTime(&ms, a, b) != cudaSuccess) return RL_ERR_CUDA;
-            out->launches[k] += 1;
-            out->total_ms[k] += ms;
-        }
+    for (int i = 0; i < h->prof_used; ++i) {
+        cudaEvent_t a = h->prof_events[2 * (size_t)i], b = h->prof_events[2 * (size_t)i + 1];
+        if (cudaEventSynchronize(b) != cudaSuccess) return RL_ERR_CUDA;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, a, b) != cudaSuccess) return RL_ERR_CUDA;
+        out->launches[h->prof_cls[i]] += 1;
+        out->total_ms[h->prof_cls[i]] += ms;
     }
     h->prof_capacity = 0;
-    h->prof_calls = 0;
+    h->prof_used = 0;
     return RL_OK;
 }
 

@@ -68,8 +68,9 @@ __global__ void __launch_bounds__(kPrepThreads) seg_prep_kernel(SeqPrepParams p)
 
 // One thread per token.
 __global__ void __launch_bounds__(kTokenThreads) token_prep_kernel(TokenPrepParams p) {
-    const int t = blockIdx.x * kTokenThreads + threadIdx.x;
-    if (t >= p.num_tokens) return;
+    const int i_row = blockIdx.x * kTokenThreads + threadIdx.x;
+    if (i_row >= p.rows) return;
+    const int t = p.row0 + i_row;
     const int i = find_seq(p.cu_seqlens, p.num_seqs, t);
     if (i < 0) raise_status(p.status, RL_ERR_SEQLENS);
     const float A = i >= 0 ? p.seq_adv[i] : 0.f;
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(kTokenThreads) token_prep_kernel(TokenPrepPara
     const bool in_bounds = (-p.c.ln_beta <= d) && (d <= p.c.ln_beta);
     float zy = 0.f;
     if (ok) {
-        const size_t off = (size_t)t * (size_t)p.ld_logits + (size_t)y;
+        const size_t off = (size_t)i_row * (size_t)p.ld_logits + (size_t)y;
         if (p.logits_dtype == RL_F32) {
             zy = __ldg(reinterpret_cast<const float *>(p.logits) + off);
         } else {
@@ -180,8 +181,8 @@ cudaError_t launch_seg_prep(const SeqPrepParams &p, cudaStream_t stream) {
 }
 
 cudaError_t launch_token_prep(const TokenPrepParams &p, cudaStream_t stream) {
-    if (p.num_tokens == 0) return cudaSuccess;
-    token_prep_kernel<<<(p.num_tokens + kTokenThreads - 1) / kTokenThreads, kTokenThreads, 0, stream>>>(p);
+    if (p.rows <= 0) return cudaSuccess;
+    token_prep_kernel<<<(p.rows + kTokenThreads - 1) / kTokenThreads, kTokenThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -229,3 +229,78 @@ def to_numpy(batch: Batch) -> dict:
                 logp_old=batch.logp_old.cpu().numpy(), logp_infer=batch.logp_infer.cpu().numpy(),
                 mask=batch.mask.cpu().numpy(), cu_seqlens=batch.cu_seqlens.cpu().numpy(),
                 rewards_or_adv=batch.rewards_or_adv.cpu().numpy())
+
+
+# ---------------------------------------------------------------------------- fused projection (case 4)
+
+PROJ_CASE = dict(name="fused projection 64x8 L128 H6144 V151552 chunk4096", prompts=64, group=8, length=128,
+                 hidden=6144, vocab=151552, chunk=4096, h_std=1.0, w_std=0.02, old_noise=0.05, infer_noise=0.1,
+                 outlier_frac=0.01, reward_p=0.5, mask_frac=0.25, beta=2.0)
+
+
+@dataclass
+class ProjBatch:
+    """Hidden states, LM head and the per-token inputs of the fused path.
+
+    hidden [T, ldh] bf16 ~ N(0, h_std); w [V, ldw] bf16 ~ N(0, w_std); targets
+    drawn from softmax(hidden @ w^T); the rest as in ``Batch`` (``batch.logits``
+    is an empty placeholder: the logits are never materialised).
+    """
+    hidden: torch.Tensor
+    w: torch.Tensor
+    batch: Batch
+    chunk: int
+
+    @property
+    def hidden_dim(self) -> int:
+        return int(self.hidden.shape[1])
+
+
+def make_projection_batch(device="cpu", seed: int = 0, chunk_rows: int = 1024, **over) -> ProjBatch:
+    """Case 4 (or a smaller variant of it through keyword overrides of PROJ_CASE)."""
+    case = dict(PROJ_CASE)
+    case.update(over)
+    base = 20261202 + 4 + 1000 * seed
+    S = case["prompts"] * case["group"]
+    lengths = [case["length"]] * S
+    T, H, V = S * case["length"], case["hidden"], case["vocab"]
+    if H % 8:
+        raise ValueError("hidden size must be a multiple of 8 (16-byte rows)")
+    ldh, ldw = padded_ld(H, "bf16"), padded_ld(H, "bf16")
+    g_h, g_w = _gen(device, base, 1), _gen(device, base, 8)
+    hidden = torch.zeros((T, ldh), dtype=torch.bfloat16, device=device)
+    w = torch.zeros((V, ldw), dtype=torch.bfloat16, device=device)
+    for r0 in range(0, T, chunk_rows):
+        r1 = min(T, r0 + chunk_rows)
+        hidden[r0:r1, :H] = (torch.randn((r1 - r0, H), generator=g_h, device=device) * case["h_std"]).to(torch.bfloat16)
+    for r0 in range(0, V, 8 * chunk_rows):
+        r1 = min(V, r0 + 8 * chunk_rows)
+        w[r0:r1, :H] = (torch.randn((r1 - r0, H), generator=g_w, device=device) * case["w_std"]).to(torch.bfloat16)
+    targets = torch.empty(T, dtype=torch.int32, device=device)
+    logp_true = torch.empty(T, dtype=torch.float32, device=device)
+    g_tgt = _gen(device, base, 2)
+    for r0 in range(0, T, chunk_rows):
+        r1 = min(T, r0 + chunk_rows)
+        z = (hidden[r0:r1, :H] @ w[:, :H].T).float()  # input shaping only
+        u = torch.rand(z.shape, generator=g_tgt, device=device, dtype=torch.float32)
+        y = torch.argmax(z - torch.log(-torch.log(u.clamp_min(1e-30))), dim=1)
+        targets[r0:r1] = y.to(torch.int32)
+        logp_true[r0:r1] = torch.log_softmax(z, dim=1).gather(1, y[:, None])[:, 0]
+        del z, u
+    g_old, g_inf, g_out = _gen(device, base, 3), _gen(device, base, 4), _gen(device, base, 5)
+    logp_old = logp_true + case["old_noise"] * torch.randn(T, generator=g_old, device=device)
+    logp_infer = logp_old + case["infer_noise"] * torch.randn(T, generator=g_inf, device=device)
+    is_out = torch.rand(T, generator=g_out, device=device) < case["outlier_frac"]
+    sign = torch.where(torch.rand(T, generator=g_out, device=device) < 0.5, -1.0, 1.0)
+    logp_infer = logp_infer + is_out.float() * sign * 2.0
+    rewards = (torch.rand(S, generator=_gen("cpu", base, 6)) < case["reward_p"]).float()
+    rng = np.random.default_rng(base * 100 + 7)
+    mask = np.concatenate([span_mask(L, case["mask_frac"], rng) for L in lengths])
+    cu = torch.zeros(S + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    b = Batch(logits=torch.empty((T, 0), dtype=torch.bfloat16, device=device), targets=targets,
+              logp_old=logp_old.float().contiguous(), logp_infer=logp_infer.float().contiguous(),
+              mask=torch.from_numpy(mask).to(device), cu_seqlens=cu.to(device), rewards_or_adv=rewards.to(device),
+              vocab=V, group=case["group"], dtype="bf16", adv_mode=0, beta=case["beta"],
+              meta=dict(case=4, name=case["name"], seed=seed, lengths=lengths))
+    return ProjBatch(hidden=hidden, w=w, batch=b, chunk=case["chunk"])

@@ -1,0 +1,151 @@
+"""The fused sequence-chunked projection + loss path against the fp64 oracle:
+the tcgen05 projection GEMM alone (ragged tiles, full width), the whole fused
+forward+backward on small cases spanning several chunks and tiles, its
+determinism, and the full-size case on sampled rows plus identities."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_helpers import params_for
+from rl_post_loss_gb300 import build as nvbuild
+from rl_post_loss_gb300 import capi, synthetic
+
+pytestmark = pytest.mark.gpu
+
+TOL_LOGP_STATED = 3e-2   # fused-GEMM configuration, as stated for this workload
+TOL_LOGP_STRICT = 2e-4   # fp32-accumulated logits: what the arithmetic gives
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    nvbuild.build()
+    capi.load()
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("M,K,N", [(128, 64, 256), (300, 320, 1000), (257, 6144, 2048), (64, 6144, 151552)])
+def test_projection_gemm_matches_fp64(M, K, N):
+    g = torch.Generator(device="cuda").manual_seed(M * 7 + K + N)
+    h = (torch.randn((M, K), generator=g, device="cuda")).to(torch.bfloat16)
+    w = (torch.randn((N, K), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    rl = capi.RlLoss(N, 1, M, 1, capi.RL_BF16)
+    rl.projection_setup(K, M)
+    ldz = (N + 3) // 4 * 4
+    z = torch.full((M, ldz), float("nan"), dtype=torch.float32, device="cuda")
+    rl.projection_logits(h, w, M, z)
+    torch.cuda.synchronize()
+    got = z[:, :N].double().cpu().numpy()
+    ref = oracle.projection_logits(_bits(h), _bits(w))
+    scale = oracle.bf16_bits_to_f64(_bits(h)).__abs__() @ oracle.bf16_bits_to_f64(_bits(w)).__abs__().T
+    err = np.abs(got - ref)
+    assert np.all(err <= 1e-5 * scale + 1e-6), f"max err {err.max()} (scaled {(err / (scale + 1e-30)).max()})"
+    assert bool(torch.isnan(z[:, N:]).all()), "padding columns written"
+
+
+def _small(prompts=2, group=4, length=50, hidden=320, vocab=1000, chunk=160, seed=0, **over):
+    return synthetic.make_projection_batch("cuda", seed=seed, prompts=prompts, group=group, length=length,
+                                           hidden=hidden, vocab=vocab, chunk=chunk, **over)
+
+
+def _check_fused(pb, out, report=None):
+    b = pb.batch
+    p = params_for(b)
+    npb = {k: getattr(b, k).cpu().numpy() for k in
+           ("targets", "logp_old", "logp_infer", "mask", "cu_seqlens", "rewards_or_adv")}
+    H = pb.hidden_dim
+    ref = oracle.projection_forward_backward(_bits(pb.hidden[:, :H]), _bits(pb.w[:, :H]), npb, p)
+    L = out["loss_f64"].item()
+    assert abs(L - ref["loss"]) <= 1e-4 * abs(ref["loss"]) + 1e-12, (L, ref["loss"])
+    lp = out["logp"].cpu().numpy().astype(np.float64)
+    assert np.abs(lp - ref["logp"]).max() <= TOL_LOGP_STATED
+    assert np.abs(lp - ref["logp"]).max() <= TOL_LOGP_STRICT
+    assert np.abs(out["entropy"].cpu().numpy() - ref["entropy"]).max() <= TOL_LOGP_STRICT
+    f = out["flags"].cpu().numpy()
+    assert np.array_equal(f & 0xD, ref["flags"] & 0xD)
+    advt = np.repeat(ref["adv"], np.diff(npb["cu_seqlens"]))
+    rule = oracle.clip_active_vec(out["logp"].cpu().numpy(), npb["logp_old"], advt, p.eps_low, p.eps_high)
+    assert np.array_equal((f >> 1) & 1, rule)
+    near = np.abs(np.abs(ref["logp"] - npb["logp_old"]) - 0.2469) < 1e-3  # none expected at these noise levels
+    ok = ~near
+    dh = out["dhidden"][:, :H].double().cpu().numpy()
+    dw = out["dw_lm"][:, :H].double().cpu().numpy()
+    for name, got, want in (("dhidden", dh[ok], ref["dh"][ok]), ("dW", dw, ref["dW"])):
+        rn = np.linalg.norm(got - want, axis=1) / np.maximum(np.linalg.norm(want, axis=1), 1e-30)
+        nz = np.linalg.norm(want, axis=1) > 0
+        assert rn[nz].max() <= 1e-2, f"{name} row relative L2 {rn[nz].max()}"
+        rms = np.sqrt((want ** 2).mean(axis=1, keepdims=True))
+        assert np.all(np.abs(got - want) <= 3e-2 * np.abs(want) + 1e-2 * rms + 1e-30), name
+        zero = ~nz
+        assert np.all(got[zero] == 0.0), f"{name}: rows with zero gradient must be exact zeros"
+        if report is not None:
+            report[name + "_row_rel_l2_max"] = float(rn[nz].max())
+    if report is not None:
+        report.update(loss=L, loss_oracle=ref["loss"], logp_max_err=float(np.abs(lp - ref["logp"]).max()))
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(vocab=4097, hidden=128, chunk=96), dict(prompts=1, length=300, chunk=512)])
+def test_fused_projection_small_parity(kw):
+    pb = _small(**kw)
+    rl = capi.projection_handle(pb)
+    out = capi.alloc_projection_outputs(pb)
+    capi.run_projection(rl, pb, out)
+    torch.cuda.synchronize()
+    assert rl.device_status() & ~(1 << capi.CODES["RL_ERR_EMPTY_SEQ"]) == 0
+    rep = {}
+    _check_fused(pb, out, rep)
+    print(rep)
+
+
+def test_fused_projection_bit_identical_runs():
+    pb = _small(prompts=2, group=8, length=64, hidden=512, vocab=3000, chunk=200)
+    rl = capi.projection_handle(pb)
+    outs = []
+    for _ in range(3):
+        out = capi.alloc_projection_outputs(pb)
+        capi.run_projection(rl, pb, out)
+        torch.cuda.synchronize()
+        outs.append(out)
+    for k in outs[0]:
+        for o in outs[1:]:
+            assert torch.equal(outs[0][k].view(torch.uint8), o[k].view(torch.uint8)), k
+
+
+@pytest.mark.slow
+def test_fused_projection_full_size_sampled():
+    torch.cuda.empty_cache()
+    pb = synthetic.make_projection_batch("cuda")
+    b = pb.batch
+    rl = capi.projection_handle(pb)
+    out = capi.alloc_projection_outputs(pb)
+    capi.run_projection(rl, pb, out)
+    torch.cuda.synchronize()
+    assert rl.device_status() & ~(1 << capi.CODES["RL_ERR_EMPTY_SEQ"]) == 0
+    T, H = b.num_tokens, pb.hidden_dim
+    p = params_for(b)
+    npb = {k: getattr(b, k).cpu().numpy() for k in
+           ("targets", "logp_old", "logp_infer", "mask", "cu_seqlens", "rewards_or_adv")}
+    n, adv, w = oracle.seq_prep(npb["cu_seqlens"], npb["mask"], npb["rewards_or_adv"], p)
+    rng = np.random.default_rng(4)
+    ids = np.unique(np.concatenate([[0, T - 1, 4095, 4096], rng.choice(T, 28, replace=False)]))
+    wb = _bits(pb.w[:, :H])
+    ref = oracle.projection_rows(ids, _bits(pb.hidden[:, :H]), wb, npb["targets"], npb["logp_old"],
+                                 npb["logp_infer"], npb["mask"], npb["cu_seqlens"], adv, w, p, want_dh=True)
+    lp = out["logp"].cpu().numpy()[ids].astype(np.float64)
+    assert np.abs(lp - ref["logp"]).max() <= TOL_LOGP_STATED
+    assert np.abs(lp - ref["logp"]).max() <= TOL_LOGP_STRICT
+    assert np.abs(out["entropy"].cpu().numpy()[ids] - ref["entropy"]).max() <= TOL_LOGP_STRICT
+    assert np.array_equal(out["flags"].cpu().numpy()[ids] & 0xD, ref["flags"] & 0xD)
+    dh = out["dhidden"][torch.as_tensor(ids, device="cuda"), :H].double().cpu().numpy()
+    nz = np.linalg.norm(ref["dh"], axis=1) > 0
+    rn = np.linalg.norm(dh - ref["dh"], axis=1)[nz] / np.linalg.norm(ref["dh"], axis=1)[nz]
+    assert rn.size == 0 or rn.max() <= 1e-2, rn.max()
+    # identity at any size: sum_t <dH_t, h_t> = sum_{t,v} dZ_tv z_tv = sum_v <dW_v, W_v>
+    lhs = (out["dhidden"][:, :H].double() * pb.hidden[:, :H].double()).sum().item()
+    rhs = (out["dw_lm"][:, :H].double() * pb.w[:, :H].double()).sum().item()
+    assert abs(lhs - rhs) <= 1e-2 * max(abs(lhs), abs(rhs)) + 1e-9, (lhs, rhs)
+    print({"logp_max_err": float(np.abs(lp - ref["logp"]).max()), "dh_row_rel_l2_max": float(rn.max()),
+           "trace_dH_h": lhs, "trace_dW_W": rhs, "loss": out["loss_f64"].item()})
