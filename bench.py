@@ -44,6 +44,7 @@ def parse_args():
     ap.add_argument("--prompts", type=int, default=0,
                     help="use only the first P prompts' responses (small profiling runs); 0 = the whole case")
     ap.add_argument("--max-len", type=int, default=0, help="cap every response length (small profiling runs)")
+    ap.add_argument("--vocab", type=int, default=0, help="case 4: vocabulary override (small profiling runs)")
     return ap.parse_args()
 
 
@@ -65,6 +66,13 @@ def measured_peaks(key: str = "hbm_gbs"):
         return fallback[key], "fallback"
 
 
+# the source files each profiled kernel is compiled from
+KERNEL_SOURCES = {
+    "row_loss": ["row_loss.cu", "common.cuh"],
+    "proj_gemm": ["proj_gemm.cu", "proj.cuh", "ptx.cuh", "common.cuh"],
+}
+
+
 def kernel_traffic(kernel: str, case_id: int):
     """Per-launch DRAM bytes of ``kernel`` from the committed ncu summary, or
     None when that summary was taken on another version of the kernel source."""
@@ -74,17 +82,16 @@ def kernel_traffic(kernel: str, case_id: int):
     text = open(path).read()
     m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     m_hash = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    if not (m_bytes and m_hash) or m_hash.group(1) != kernel_source_hash():
+    if not (m_bytes and m_hash) or m_hash.group(1) != kernel_source_hash(kernel):
         return None
     return float(m_bytes.group(1))
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "rl_post_loss_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()
 
 
@@ -426,6 +433,8 @@ def main_projection(args):
     over = {}
     if args.prompts:
         over["prompts"] = args.prompts
+    if args.vocab:
+        over["vocab"] = args.vocab
     pb = synthetic.make_projection_batch("cuda", seed=rank, **over)
     b = pb.batch
     rl = capi.projection_handle(pb)
