@@ -148,6 +148,24 @@ class ClockSampler:
                 "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
 
 
+def max_over_ranks(x: float) -> float:
+    """The maximum of a per-rank value over the process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(tokens_per_step: int, steps: int, world: int, ms: float) -> float:
+    """Whole-job tokens/s of `world` replicas, each running `steps` steps of
+    `tokens_per_step` tokens, timed by the slowest rank (`ms`)."""
+    return world * steps * tokens_per_step / (ms / 1e3)
+
+
 def algorithmic_bytes(batch) -> float:
     es = 2 if batch.dtype == "bf16" else 4
     return float(batch.num_tokens) * (2.0 * batch.vocab * es + SIDE_BYTES_PER_TOKEN)
@@ -312,13 +330,10 @@ def main():
     ms = start.elapsed_time(stop)
     launches = rl.launch_count() - launches0
     prof = rl.profile_read()
-    if world > 1:
-        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms)
 
     T = batch.num_tokens
-    value = world * args.steps * T / (ms / 1e3)
+    value = replica_throughput(T, args.steps, world, ms)
     row_n, row_ms = prof["row_loss"]
     row_avg_ms = row_ms / max(1, row_n)
     bytes_per_launch = algorithmic_bytes(batch)
@@ -345,11 +360,8 @@ def main():
     e_stop.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e_start.elapsed_time(e_stop) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * T / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e2e_ms)
+    e2e_value = replica_throughput(T, 1, world, e2e_ms)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -461,12 +473,9 @@ def main_projection(args):
     ms = start.elapsed_time(stop)
     launches = rl.launch_count() - launches0
     prof = rl.profile_read()
-    if world > 1:
-        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms)
     T, H, V = b.num_tokens, pb.hidden_dim, b.vocab
-    value = world * args.steps * T / (ms / 1e3)
+    value = replica_throughput(T, args.steps, world, ms)
     flops_alg = 6.0 * T * V * H  # projection, dL/dh and dL/dW GEMMs
     g_n, g_ms = prof["proj_gemm"]
     gemm_flops = 2.0 * T * V * H / max(1, g_n // args.steps)  # per launch (one chunk)
@@ -495,10 +504,7 @@ def main_projection(args):
     e_stop.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e_start.elapsed_time(e_stop) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, cores, desc = projection_sample_rate(pb, args.cpu_seconds)
@@ -521,7 +527,7 @@ def main_projection(args):
                                 "executed_flops_per_step": flops_alg, "note": "6 N V H per step"},
                 "kernel_ms": {k: v[1] / args.steps for k, v in prof.items() if v[0]},
                 "clocks": clocks.summary(),
-                "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "e2e": {"value": replica_throughput(T, 1, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": 8, "ms_per_step": e2e_ms},
                 "gpu_launches": launches, "device_status": capi.status_bits_to_names(bits), "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)

@@ -234,17 +234,23 @@ def projection_rows(row_ids, hidden_bits, w_bits, targets, logp_old, logp_infer,
     return out
 
 
-def projection_forward_backward(hidden_bits, w_bits, batch: dict, p: LossParams) -> dict:
-    """Whole-batch oracle of the fused path (small sizes): loss, per-token
-    results, dL/dh = dZ W and dL/dW = dZ^T h, all in float64."""
+def projection_forward_backward_f64(h: np.ndarray, W: np.ndarray, batch: dict, p: LossParams) -> dict:
+    """Whole-batch oracle of the fused path on float64 hidden states h [T, H]
+    and LM head W [V, H]: z = h W^T, the loss of Eq. (1) on z, dL/dz, and by the
+    chain rule dL/dh = dL/dz W and dL/dW = (dL/dz)^T h."""
     cu = batch["cu_seqlens"]
     T = int(cu[-1])
     n, adv, w = seq_prep(cu, batch["mask"], batch["rewards_or_adv"], p)
-    W = bf16_bits_to_f64(w_bits)
-    h = bf16_bits_to_f64(hidden_bits[:T])
-    out = projection_rows(np.arange(T), hidden_bits, w_bits, batch["targets"], batch["logp_old"],
-                          batch["logp_infer"], batch["mask"], cu, adv, w, p, want_dh=True, w64=W)
-    out["dW"] = out["dz"].T @ h
+    z = np.ascontiguousarray(h[:T] @ W.T)
+    out = rows(np.arange(T), z, F64, W.shape[0], batch["targets"], batch["logp_old"], batch["logp_infer"],
+               batch["mask"], cu, adv, w, p, want_dz=True)
+    out["dh"] = out["dz"] @ W
+    out["dW"] = out["dz"].T @ h[:T]
     out["loss"] = loss(cu, w, out["tok_obj"])
     out["n_tokens"], out["adv"], out["w"] = n, adv, w
     return out
+
+
+def projection_forward_backward(hidden_bits, w_bits, batch: dict, p: LossParams) -> dict:
+    """The same on bf16 inputs (bit patterns), widened exactly to float64."""
+    return projection_forward_backward_f64(bf16_bits_to_f64(hidden_bits), bf16_bits_to_f64(w_bits), batch, p)

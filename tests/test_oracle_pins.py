@@ -374,3 +374,46 @@ def test_hyperparameters_match_the_page():
     for cid in (0, 1, 2):
         assert synthetic.CASES[cid]["beta"] == hp["beta"]
     assert (synthetic.EPS_LOW, synthetic.EPS_HIGH) == (hp["eps_low"], hp["eps_high"])
+
+
+# ----------------------------------------------------------------------------- fused projection oracle
+
+def test_projection_logits_exact_on_integer_inputs():
+    """Small integers are exact in bf16 and their products and sums exact in
+    float64: the projection must equal the integer matrix product."""
+    rng = np.random.default_rng(12)
+    hi = rng.integers(-8, 9, (5, 7))
+    wi = rng.integers(-8, 9, (6, 7))
+    to_bits = lambda a: (np.asarray(a, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    z = oracle.projection_logits(to_bits(hi), to_bits(wi))
+    want = [[sum(int(hi[i, k]) * int(wi[j, k]) for k in range(7)) for j in range(6)] for i in range(5)]
+    assert np.array_equal(z, np.array(want, np.float64))
+
+
+def test_projection_gradients_match_finite_differences():
+    """dL/dh and dL/dW of the fused-path oracle against central differences of
+    its loss in every entry of h and W (catches a transposed or swapped operand)."""
+    rng = np.random.default_rng(13)
+    T, H, V = 6, 5, 7
+    h = rng.normal(0, 1, (T, H))
+    W = rng.normal(0, 0.5, (V, H))
+    cu = np.array([0, 2, 4, 6], np.int32)
+    tg = rng.integers(0, V, T).astype(np.int32)
+    b = _batch(np.zeros((T, V)), tg, np.zeros(T), np.zeros(T), np.ones(T), cu, [0.7, -0.4, 1.1])
+    p = LossParams(group_size=1, adv_mode=1)
+    lp = oracle.projection_forward_backward_f64(h, W, b, p)["logp"]
+    b["logp_old"] = (lp - np.array([0.05, -0.1, 0.3, 0.0, -0.02, 0.12])).astype(np.float32)
+    b["logp_infer"] = (b["logp_old"].astype(np.float64) - rng.normal(0, 0.2, T)).astype(np.float32)
+    out = oracle.projection_forward_backward_f64(h, W, b, p)
+    hstep = 1e-6
+    for name, X, grad in (("h", h, out["dh"]), ("W", W, out["dW"])):
+        fd = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += hstep
+            Xm[idx] -= hstep
+            args_p = (Xp, W) if name == "h" else (h, Xp)
+            args_m = (Xm, W) if name == "h" else (h, Xm)
+            fd[idx] = (oracle.projection_forward_backward_f64(*args_p, b, p)["loss"] -
+                       oracle.projection_forward_backward_f64(*args_m, b, p)["loss"]) / (2 * hstep)
+        np.testing.assert_allclose(grad, fd, rtol=1e-5, atol=1e-8 * np.abs(grad).max(), err_msg=name)
