@@ -51,10 +51,10 @@ def _load():
     lib = ctypes.CDLL(build())
     P = ctypes.c_void_p
     i64, i32, f32, f64 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_double
-    lib.oracle_seq_prep.argtypes = [i64, i64, P, P, P, i32, f32, i32, P, P, P]
+    lib.oracle_seq_prep.argtypes = [i64, i64, P, P, P, i32, f32, i32, i32, P, P, P]
     lib.oracle_seq_prep.restype = i32
     lib.oracle_rows.argtypes = [i64, P, i64, i64, i32, P, P, P, P, P, i64, P, P, P, f32, f32, f32, i32,
-                                P, P, P, P, P, P]
+                                i32, i32, P, P, P, P, P, P, P, P]
     lib.oracle_rows.restype = i32
     lib.oracle_loss.argtypes = [i64, P, P, P]
     lib.oracle_loss.restype = f64
@@ -87,9 +87,13 @@ class LossParams:
     eps_high: float = 0.28
     beta: float = 2.0
     adv_eps: float = 1e-6
-    adv_mode: int = 0          # 0: group-normalised rewards, 1: given per-sequence advantage
+    adv_mode: int = 0          # 0: group-normalised rewards, 1: given per-sequence advantage,
+                               # 2: given per-token advantage, 3: teacher log-probs (on-policy distillation)
     std_unbiased: int = 0
     pop_indicator: int = 0     # 0: pop returns rho (printed operator), 1: returns 1
+    objective: int = 0         # 0: GRPO + IcePop (Eq. 1), 1: direct double-sided importance sampling
+    loss_norm: int = 0         # 0: 1/(S |y_i|) per response (Eq. 1), 1: mean over all generated tokens
+    dis_stopgrad: int = 1      # DIS only: 1 = f(r) treated as a constant
 
 
 def seq_prep(cu_seqlens, mask, rewards_or_adv, p: LossParams):
@@ -102,17 +106,20 @@ def seq_prep(cu_seqlens, mask, rewards_or_adv, p: LossParams):
     n = np.zeros(S, np.int64)
     adv = np.zeros(S, np.float64)
     w = np.zeros(S, np.float64)
+    if p.adv_mode >= 2:
+        r = np.zeros(S, np.float32)  # per-token modes: the [T] array is used by rows()
     rc = lib.oracle_seq_prep(S, p.group_size, _ptr(cu), _ptr(m), _ptr(r), p.adv_mode, p.adv_eps,
-                             p.std_unbiased, _ptr(n), _ptr(adv), _ptr(w))
+                             p.std_unbiased, p.loss_norm, _ptr(n), _ptr(adv), _ptr(w))
     if rc != 0:
         raise ValueError("oracle_seq_prep rejected its arguments")
     return n, adv, w
 
 
 def rows(row_ids, logits_rows, dtype: int, V: int, targets, logp_old, logp_infer, mask, cu_seqlens, adv, w,
-         p: LossParams, want_dz: bool = False):
+         p: LossParams, want_dz: bool = False, token_adv=None):
     """Per-token results for ``row_ids``; ``logits_rows`` is [len(row_ids), ld]
-    (float32, float64, or uint16 holding bf16 bits). Returns a dict of arrays."""
+    (float32, float64, or uint16 holding bf16 bits). ``token_adv`` is the [T]
+    array of adv_mode 2 (advantages) or 3 (teacher log-probs). Returns a dict."""
     lib = _load()
     ids = np.ascontiguousarray(row_ids, dtype=np.int64)
     z = np.ascontiguousarray(logits_rows)
@@ -135,10 +142,12 @@ def rows(row_ids, logits_rows, dtype: int, V: int, targets, logp_old, logp_infer
     m = np.ascontiguousarray(mask, dtype=np.uint8)
     a = np.ascontiguousarray(adv, dtype=np.float64)
     ww = np.ascontiguousarray(w, dtype=np.float64)
+    ta = None if p.adv_mode < 2 else np.ascontiguousarray(token_adv, dtype=np.float32)
     rc = lib.oracle_rows(n, _ptr(ids), V, ld, dtype, _ptr(z), _ptr(tg), _ptr(lo), _ptr(li), _ptr(m),
                          cu.shape[0] - 1, _ptr(cu), _ptr(a), _ptr(ww), p.eps_low, p.eps_high, p.beta,
-                         p.pop_indicator, _ptr(out["logp"]), _ptr(out["entropy"]), _ptr(out["flags"]),
-                         _ptr(out["tok_obj"]), _ptr(out["g"]), _ptr(dz))
+                         p.pop_indicator, p.objective, p.dis_stopgrad, _ptr(ta if p.adv_mode == 2 else None),
+                         _ptr(ta if p.adv_mode == 3 else None), _ptr(out["logp"]), _ptr(out["entropy"]),
+                         _ptr(out["flags"]), _ptr(out["tok_obj"]), _ptr(out["g"]), _ptr(dz))
     if rc != 0:
         raise ValueError("oracle_rows rejected its arguments")
     if want_dz:
@@ -170,11 +179,12 @@ def forward_backward(batch: dict, dtype: int, V: int, p: LossParams, want_dz: bo
         ids = np.arange(r0, min(T, r0 + row_block), dtype=np.int64)
         parts.append(rows(ids, batch["logits"][r0:r0 + len(ids)], dtype, V, batch["targets"],
                           batch["logp_old"], batch["logp_infer"], batch["mask"], cu, adv, w, p,
-                          want_dz=want_dz))
+                          want_dz=want_dz, token_adv=batch.get("token_adv")))
     if not parts:  # no tokens at all
         parts.append(rows(np.zeros(0, np.int64), np.zeros((0, V), {F32: np.float32, BF16: np.uint16,
                           F64: np.float64}[dtype]), dtype, V, batch["targets"], batch["logp_old"],
-                          batch["logp_infer"], batch["mask"], cu, adv, w, p, want_dz=want_dz))
+                          batch["logp_infer"], batch["mask"], cu, adv, w, p, want_dz=want_dz,
+                          token_adv=batch.get("token_adv")))
     out = {k: np.concatenate([o[k] for o in parts]) for k in parts[0]}
     out["loss"] = loss(cu, w, out["tok_obj"])
     out["n_tokens"], out["adv"], out["w"] = n, adv, w

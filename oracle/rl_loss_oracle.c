@@ -44,6 +44,26 @@
  *  - A target id outside [0, V) excludes its token from the loss (objective
  *    and gradient 0), sets flag bit 3 and leaves logp as NaN.
  *
+ * Two further objectives / advantages of the same pages (adv_mode, objective):
+ *  - Per-token advantages (adv_mode 2, e.g. from a critic) and the on-policy
+ *    distillation advantage A_t = sg[log pi_teacher(y_t) - log pi_theta(y_t)]
+ *    (adv_mode 3, "GLM-5: from Vibe Coding to Agentic Engineering", section 3.5,
+ *    Eq. (2)), which replaces A in Eq. (1). Its sign, which decides the clip
+ *    side, is taken in fp32: fl32(logp_teacher - fl32(logp)).
+ *  - Direct double-sided importance sampling (objective 1, section 4.1.2,
+ *    Eqs. (3)-(5); "Zhipu AI / GLM: From Blank Infilling to Compaction-Aware
+ *    Agentic Reinforcement Learning", section 11, "Direct Double-Sided
+ *    Importance Sampling"): r = exp(logp - logp_rollout) with the rollout
+ *    engine's log-prob (logp_infer), f(r) = r on the open interval
+ *    (1 - eps_low, 1 + eps_high) and 0 outside (decided in fp32 on
+ *    fl32(fl32(logp) - logp_rollout) against the clip thresholds), token term
+ *    f(r) A logp. Readings: the loss is minus the printed objective (as for
+ *    Eq. (1)); "E_t" is the mean over the generated tokens when loss_norm = 1;
+ *    whether f is stop-gradient is unmarked on the pages, so both readings
+ *    exist: dis_stopgrad = 1 differentiates A logp only (dL/dlogp = -w f A),
+ *    0 differentiates f too (dL/dlogp = -w r A (1 + logp) inside the interval).
+ *    Flag bit0 is then "inside the interval" and bit1 is unused.
+ *
  * Flag bits per token: bit0 pop in bounds, bit1 clip branch active, bit2 mask
  * is 0, bit3 target id out of range.
  *
@@ -119,21 +139,30 @@ void oracle_clip_active_vec(int64_t n, const float *logp, const float *logp_old,
  *   n_i   = |y_i| = number of mask=1 tokens of response i
  *   A_i   = (R_i - mean(R_group)) / (std(R_group) + adv_eps)   (adv_mode 0)
  *         = rewards_or_adv[i]                                 (adv_mode 1)
- *   w_i   = 1 / (S * n_i), or 0 when n_i == 0
+ *   w_i   = 1 / (S * n_i), or 0 when n_i == 0          (loss_norm 0, Eq. (1))
+ *         = 1 / sum_j n_j, or 0 when n_i == 0         (loss_norm 1, mean over tokens)
  * Groups are G consecutive responses. Returns 0, or -1 on bad arguments.
  */
 int32_t oracle_seq_prep(int64_t S, int64_t G, const int32_t *cu_seqlens, const uint8_t *mask,
                         const float *rewards_or_adv, int32_t adv_mode, float adv_eps, int32_t std_unbiased,
-                        int64_t *n_tokens, double *adv, double *w) {
+                        int32_t loss_norm, int64_t *n_tokens, double *adv, double *w) {
     if (S < 1 || G < 1 || S % G != 0) return -1;
-    if (adv_mode != 0 && adv_mode != 1) return -1;
+    if (adv_mode < 0 || adv_mode > 3) return -1;
     if (adv_mode == 0 && std_unbiased && G < 2) return -1;
+    int64_t total = 0;
     for (int64_t i = 0; i < S; ++i) {
         if (cu_seqlens[i + 1] < cu_seqlens[i]) return -1;
         int64_t n = 0;
         for (int64_t t = cu_seqlens[i]; t < cu_seqlens[i + 1]; ++t) n += mask[t] ? 1 : 0;
         n_tokens[i] = n;
+        total += n;
         w[i] = n > 0 ? 1.0 / ((double)S * (double)n) : 0.0;
+    }
+    if (loss_norm == 1) /* the mean over every generated token of the batch */
+        for (int64_t i = 0; i < S; ++i) w[i] = n_tokens[i] > 0 ? 1.0 / (double)total : 0.0;
+    if (adv_mode >= 2) { /* per-token advantages: no per-response value */
+        for (int64_t i = 0; i < S; ++i) adv[i] = 0.0;
+        return 0;
     }
     if (adv_mode == 1) {
         for (int64_t i = 0; i < S; ++i) adv[i] = (double)rewards_or_adv[i];
@@ -174,7 +203,8 @@ int32_t oracle_seq_prep(int64_t S, int64_t G, const int32_t *cu_seqlens, const u
 int32_t oracle_rows(int64_t n_rows, const int64_t *row_ids, int64_t V, int64_t ld, int32_t dtype, const void *logits,
                     const int32_t *targets, const float *logp_old, const float *logp_infer, const uint8_t *mask,
                     int64_t S, const int32_t *cu_seqlens, const double *adv, const double *w, float eps_low,
-                    float eps_high, float beta, int32_t pop_indicator, double *logp, double *entropy,
+                    float eps_high, float beta, int32_t pop_indicator, int32_t objective, int32_t dis_stopgrad,
+                    const float *adv_token, const float *teacher_logp, double *logp, double *entropy,
                     uint8_t *flags, double *tok_obj, double *g, double *dz) {
     if (V < 1 || ld < V || n_rows < 0) return -1;
     if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64) return -1;
@@ -211,13 +241,31 @@ int32_t oracle_rows(int64_t n_rows, const int64_t *row_ids, int64_t V, int64_t l
         const double lp_y = target_ok ? logit_at(row, dtype, y) - logZ : NAN;
         logp[k] = lp_y;
 
-        const double A = adv[i];
+        /* the advantage of this token, and the sign that decides the clip side */
+        double A = adv[i], A_sign = adv[i];
+        if (adv_token) A = A_sign = (double)adv_token[t];
+        if (teacher_logp) {
+            A = target_ok ? (double)teacher_logp[t] - lp_y : 0.0;
+            volatile float a32 = teacher_logp[t] - (float)lp_y; /* fp32, as the kernel decides it */
+            A_sign = target_ok ? (double)a32 : 0.0;
+        }
         const int m = mask[t] ? 1 : 0;
-        const int in_bounds = oracle_pop_in_bounds(logp_old[t], logp_infer[t], beta);
-        const int clip = target_ok ? oracle_clip_active((float)lp_y, logp_old[t], A, eps_low, eps_high) : 0;
-        flags[k] = (uint8_t)(in_bounds | (clip << 1) | ((!m) << 2) | ((!target_ok) << 3));
 
         double obj = 0.0, gt = 0.0;
+        if (objective == 1) {
+            /* direct double-sided importance sampling against the rollout log-prob */
+            volatile float e = (float)lp_y - logp_infer[t];
+            const int gate = target_ok && e > oracle_clip_lo_f32(eps_low) && e < oracle_clip_hi_f32(eps_high);
+            flags[k] = (uint8_t)(gate | ((!m) << 2) | ((!target_ok) << 3));
+            if (target_ok && m && gate) {
+                const double r = exp(lp_y - (double)logp_infer[t]);
+                obj = r * A * lp_y; /* f(r) A log pi, f(r) = r inside the interval */
+                gt = dis_stopgrad ? -w[i] * r * A : -w[i] * r * A * (1.0 + lp_y);
+            }
+        } else {
+        const int in_bounds = oracle_pop_in_bounds(logp_old[t], logp_infer[t], beta);
+        const int clip = target_ok ? oracle_clip_active((float)lp_y, logp_old[t], A_sign, eps_low, eps_high) : 0;
+        flags[k] = (uint8_t)(in_bounds | (clip << 1) | ((!m) << 2) | ((!target_ok) << 3));
         if (target_ok && m) {
             const double rho = exp((double)logp_old[t] - (double)logp_infer[t]);
             const double pop = in_bounds ? (pop_indicator ? 1.0 : rho) : 0.0;
@@ -226,6 +274,7 @@ int32_t oracle_rows(int64_t n_rows, const int64_t *row_ids, int64_t V, int64_t l
             obj = pop * fmin(r * A, r_clipped * A);
             /* d/dlogp of min(r A, clip(r) A): r A on the unclipped branch, 0 on the clipped one */
             gt = clip ? 0.0 : -w[i] * pop * A * r;
+        }
         }
         tok_obj[k] = obj;
         g[k] = gt;

@@ -417,3 +417,154 @@ def test_projection_gradients_match_finite_differences():
             fd[idx] = (oracle.projection_forward_backward_f64(*args_p, b, p)["loss"] -
                        oracle.projection_forward_backward_f64(*args_m, b, p)["loss"]) / (2 * hstep)
         np.testing.assert_allclose(grad, fd, rtol=1e-5, atol=1e-8 * np.abs(grad).max(), err_msg=name)
+
+
+# ----------------------------------------------------------------------------- DIS, OPD, per-token advantages
+
+def _tok_batch(rng, lengths, V, token_adv=None):
+    b = _onpolicy_batch(rng, lengths, V, [0.0] * len(lengths))
+    if token_adv is not None:
+        b["token_adv"] = np.asarray(token_adv, np.float32)
+    return b
+
+
+def test_dis_closed_form_at_r_one_and_token_mean():
+    rng = np.random.default_rng(20)
+    lengths = [3, 5, 2]
+    A = rng.normal(0, 1, 10).astype(np.float32)
+    b = _tok_batch(rng, lengths, 19, A)
+    b["logp_infer"] = b["logp_old"].copy()  # the rollout log-prob: r = 1 up to fp32 rounding
+    p = LossParams(group_size=1, adv_mode=2, objective=1, loss_norm=1)
+    out = oracle.forward_backward(b, F64, 19, p)
+    want = -float(np.mean(A.astype(np.float64) * out["logp"]))
+    assert abs(out["loss"] - want) < 1e-6 * np.abs(A).sum()
+    np.testing.assert_allclose(out["g"], -A / 10.0, rtol=1e-6)  # stop-gradient reading: -f A / N
+    assert np.all(out["flags"] & 1)
+
+
+def test_dis_gate_is_open_interval_and_sign_free():
+    rng = np.random.default_rng(21)
+    b = _tok_batch(rng, [6], 11, [0.5, -0.5, 0.5, -0.5, 0.5, -0.5])
+    r = np.array([1.5, 1.5, 0.7, 0.7, 1.1, 0.9])
+    b["logp_infer"] = (b["logp_old"].astype(np.float64) - np.log(r)).astype(np.float32)
+    p = LossParams(group_size=1, adv_mode=2, objective=1, loss_norm=1)
+    out = oracle.forward_backward(b, F64, 11, p, want_dz=True)
+    assert list(out["flags"] & 1) == [0, 0, 0, 0, 1, 1]  # outside on both sides whatever the sign of A
+    assert np.all(out["dz"][:4] == 0.0) and np.all(out["tok_obj"][:4] == 0.0)
+    # the interval is open: ln r exactly at fl32(ln 1.28) or fl32(ln 0.8) is outside
+    hi, lo = oracle.thresholds_f32(2.0, 0.2, 0.28)[1:]
+    b1 = _tok_batch(rng, [1], 4, [1.0])
+    b1["logits"] = np.array([[5.0, 0.0, 0.0, 0.0]])
+    b1["targets"] = np.array([0], np.int32)
+    lp32 = np.float32(oracle.forward_backward(b1, F64, 4, p)["logp"][0])
+    checked = 0
+    for e, inside in ((hi, False), (lo, False), (np.nextafter(hi, np.float32(0)), True),
+                      (np.nextafter(lo, np.float32(0)), True)):
+        li = np.float32(lp32 - e)
+        if np.float32(lp32 - li) != e:
+            continue  # this e is not reachable from lp32 by one fp32 subtraction
+        b1["logp_infer"] = np.array([li], np.float32)
+        assert bool(oracle.forward_backward(b1, F64, 4, p)["flags"][0] & 1) == inside, (e, inside)
+        checked += 1
+    assert checked >= 2
+
+
+def test_dis_full_autodiff_gradient_matches_finite_differences():
+    rng = np.random.default_rng(22)
+    V, lengths = 6, [3, 2]
+    T = sum(lengths)
+    z = rng.normal(0, 1.5, (T, V))
+    tg = rng.integers(0, V, T).astype(np.int32)
+    cu = np.array([0, 3, 5], np.int32)
+    A = np.array([0.7, -1.2, 0.4, 1.5, -0.3], np.float32)
+    b = _batch(z, tg, np.zeros(T), np.zeros(T), np.ones(T), cu, [0.0, 0.0])
+    b["token_adv"] = A
+    p = LossParams(group_size=1, adv_mode=2, objective=1, loss_norm=1, dis_stopgrad=0)
+    lp = oracle.forward_backward(b, F64, V, p)["logp"]
+    b["logp_infer"] = (lp - np.array([0.05, -0.1, 0.15, 0.6, -0.02])).astype(np.float32)  # token 3 outside
+    out = oracle.forward_backward(b, F64, V, p, want_dz=True)
+    assert not (out["flags"][3] & 1) and (out["flags"][[0, 1, 2, 4]] & 1).all()
+    h = 1e-6
+    fd = np.zeros((T, V))
+    for t in range(T):
+        for v in range(V):
+            zp, zm = z.copy(), z.copy()
+            zp[t, v] += h
+            zm[t, v] -= h
+            bp, bm = dict(b, logits=zp), dict(b, logits=zm)
+            fd[t, v] = (oracle.forward_backward(bp, F64, V, p)["loss"] -
+                        oracle.forward_backward(bm, F64, V, p)["loss"]) / (2 * h)
+    np.testing.assert_allclose(out["dz"], fd, rtol=1e-5, atol=1e-8 * np.abs(out["dz"]).max())
+
+
+def test_stop_gradient_readings_equal_frozen_surrogates():
+    """DIS with f frozen, and OPD with A frozen: dL/dz is the gradient of
+    sum_t c_t logp_t(z) with the per-token coefficients held at their value."""
+    rng = np.random.default_rng(23)
+    V, T = 7, 4
+    z = rng.normal(0, 1.0, (T, V))
+    tg = rng.integers(0, V, T).astype(np.int32)
+    cu = np.array([0, 4], np.int32)
+    base = _batch(z, tg, np.zeros(T), np.zeros(T), np.ones(T), cu, [0.0])
+    p0 = LossParams(group_size=1, adv_mode=1)
+    lp = oracle.forward_backward(base, F64, V, p0)["logp"]
+    cases = []
+    bd = dict(base, token_adv=np.array([0.9, -0.6, 1.3, -1.1], np.float32),
+              logp_infer=(lp - np.array([0.05, -0.1, 0.12, 0.0])).astype(np.float32))
+    cases.append((bd, LossParams(group_size=1, adv_mode=2, objective=1, loss_norm=1, dis_stopgrad=1)))
+    bo = dict(base, token_adv=(lp + np.array([0.3, -0.4, 0.2, -0.1])).astype(np.float32),
+              logp_old=(lp - np.array([0.05, 0.0, -0.06, 0.02])).astype(np.float32))
+    bo["logp_infer"] = bo["logp_old"].copy()
+    cases.append((bo, LossParams(group_size=1, adv_mode=3)))
+    for b, p in cases:
+        out = oracle.forward_backward(b, F64, V, p, want_dz=True)
+        c = out["g"]  # dL/dlogp with the stop-gradient factors frozen
+        h = 1e-6
+        fd = np.zeros((T, V))
+        for t in range(T):
+            for v in range(V):
+                zp, zm = z.copy(), z.copy()
+                zp[t, v] += h
+                zm[t, v] -= h
+                lp_p = oracle.forward_backward(dict(base, logits=zp), F64, V, p0)["logp"]
+                lp_m = oracle.forward_backward(dict(base, logits=zm), F64, V, p0)["logp"]
+                fd[t, v] = float(np.dot(c, lp_p - lp_m)) / (2 * h)
+        np.testing.assert_allclose(out["dz"], fd, rtol=1e-5, atol=1e-9 * np.abs(out["dz"]).max())
+
+
+def test_opd_teacher_advantage_closed_form_and_clip_side():
+    rng = np.random.default_rng(24)
+    lengths = [4, 3]
+    b = _onpolicy_batch(rng, lengths, 13, [0.0, 0.0])
+    lp = oracle.forward_backward(b, F64, 13, LossParams(group_size=1, adv_mode=1))["logp"]
+    delta = np.array([0.3, -0.2, 0.5, 0.1, -0.4, 0.25, -0.05])
+    b["token_adv"] = (lp + delta).astype(np.float32)  # teacher log-probs
+    p = LossParams(group_size=1, adv_mode=3)
+    out = oracle.forward_backward(b, F64, 13, p)
+    want = -(np.mean(delta[:4]) + np.mean(delta[4:])) / 2  # r = 1, rho = 1: L = -(1/S) sum_i mean_t A_t
+    assert abs(out["loss"] - want) < 2e-6
+    # the sign of the distillation advantage picks the clipped side
+    b2 = dict(b)
+    b2["logp_old"] = (b["logp_old"].astype(np.float64) - np.log(1.5)).astype(np.float32)  # r = 1.5
+    b2["logp_infer"] = b2["logp_old"].copy()
+    out2 = oracle.forward_backward(b2, F64, 13, p)
+    assert list((out2["flags"] >> 1) & 1) == [int(d > 0) for d in delta]
+
+
+def test_per_token_advantages_reduce_to_per_response_and_token_norm_invariance():
+    rng = np.random.default_rng(25)
+    lengths = [3, 4, 2]
+    A = [0.8, -0.3, 1.2]
+    b = _onpolicy_batch(rng, lengths, 9, A)
+    b["logp_infer"] = (b["logp_old"] + rng.normal(0, 0.2, 9)).astype(np.float32)
+    per_seq = oracle.forward_backward(b, F64, 9, LossParams(group_size=1, adv_mode=1), want_dz=True)
+    bt = dict(b, token_adv=np.repeat(np.array(A, np.float32), lengths))
+    per_tok = oracle.forward_backward(bt, F64, 9, LossParams(group_size=1, adv_mode=2), want_dz=True)
+    assert per_tok["loss"] == per_seq["loss"] and np.array_equal(per_tok["dz"], per_seq["dz"])
+    # with the token mean, splitting response 1 into two responses changes nothing
+    pt = LossParams(group_size=1, adv_mode=2, loss_norm=1)
+    L = oracle.forward_backward(bt, F64, 9, pt)["loss"]
+    split = dict(bt, cu_seqlens=np.array([0, 3, 5, 7, 9], np.int32))
+    assert abs(oracle.forward_backward(split, F64, 9, pt)["loss"] - L) < 1e-15
+    ps = LossParams(group_size=1, adv_mode=2, loss_norm=0)
+    assert abs(oracle.forward_backward(split, F64, 9, ps)["loss"] - oracle.forward_backward(bt, F64, 9, ps)["loss"]) > 1e-6
