@@ -79,14 +79,34 @@ typedef enum rl_dtype { RL_F32 = 0, RL_BF16 = 1 } rl_dtype;
 
 typedef enum rl_adv_mode {
     RL_ADV_GROUP_REWARDS = 0, /* rewards_or_adv = R [S]; A_i normalised per group of G */
-    RL_ADV_PER_SEQ = 1        /* rewards_or_adv = A [S] given, e.g. teacher_score - student_score
+    RL_ADV_PER_SEQ = 1,       /* rewards_or_adv = A [S] given, e.g. teacher_score - student_score
                                  with G = 1 ("2.5 GLM-5 -- 异步 Agentic RL 工程", Cross-Stage Distillation) */
+    RL_ADV_PER_TOKEN = 2,     /* rewards_or_adv = A [T] given per token (e.g. from a critic) */
+    RL_ADV_TEACHER_LOGP = 3   /* rewards_or_adv = log pi_teacher(y_t) [T]: A_t = sg[log pi_teacher(y_t) - logp_t],
+                                 on-policy distillation ("GLM-5: from Vibe Coding to Agentic Engineering",
+                                 section 3.5, Eq. (2)); its sign is taken in fp32 from the kernel's logp */
 } rl_adv_mode;
 
+typedef enum rl_objective {
+    RL_OBJ_GRPO_ICEPOP = 0,   /* Eq. (1): pop(rho) min(r A, clip(r) A), r = exp(logp - logp_old) */
+    RL_OBJ_DIS = 1            /* direct double-sided importance sampling (section 4.1.2, Eqs. (3)-(5)):
+                                 f(r) A logp with r = exp(logp - logp_infer) (the rollout log-prob) and
+                                 f(r) = r on the open interval (1 - eps_low, 1 + eps_high), else 0;
+                                 logp_old and beta are not used; not with RL_ADV_TEACHER_LOGP */
+} rl_objective;
+
+typedef enum rl_loss_norm {
+    RL_NORM_PER_RESPONSE = 0, /* weight 1/(S |y_i|): the 1/G, 1/|y_i| of Eq. (1) with E_x the mean over prompts */
+    RL_NORM_PER_TOKEN = 1     /* weight 1/sum_i |y_i|: the mean over every generated token of the batch */
+} rl_loss_norm;
+
 /* Per-token flag bits written to rl_loss_outputs.flags. */
-#define RL_FLAG_POP_IN_BOUNDS 0x1u /* 1/beta <= rho <= beta (decided in fp32: -fl32(ln beta) <= fl32(lo - li) <= fl32(ln beta)) */
+#define RL_FLAG_POP_IN_BOUNDS 0x1u /* 1/beta <= rho <= beta (decided in fp32: -fl32(ln beta) <= fl32(lo - li) <= fl32(ln beta));
+                                      with RL_OBJ_DIS: 1 - eps_low < r < 1 + eps_high (fl32(logp - li) strictly
+                                      between fl32(ln(1 - eps_low)) and fl32(ln(1 + eps_high))) */
 #define RL_FLAG_CLIP_ACTIVE 0x2u   /* clipped branch of min() taken: A>0 and fl32(logp - lo) > fl32(ln(1+eps_high)),
-                                      or A<0 and fl32(logp - lo) < fl32(ln(1-eps_low)); its gradient is 0 */
+                                      or A<0 and fl32(logp - lo) < fl32(ln(1-eps_low)); its gradient is 0
+                                      (RL_OBJ_GRPO_ICEPOP only) */
 #define RL_FLAG_MASKED 0x4u        /* loss mask m_t == 0 */
 #define RL_FLAG_BAD_TARGET 0x8u    /* target id outside [0, V): token excluded, logp = NaN */
 
@@ -106,6 +126,11 @@ typedef struct rl_loss_config {
     int32_t std_unbiased;  /* 0: population std (ddof 0), 1: ddof 1 (needs G >= 2) */
     int32_t pop_indicator; /* 0: pop returns rho (the printed operator), 1: returns 1 */
     int32_t logits_dtype;  /* rl_dtype of logits and of dlogits */
+    int32_t objective;     /* rl_objective (0 = Eq. (1)) */
+    int32_t loss_norm;     /* rl_loss_norm (0 = per response) */
+    int32_t dis_stopgrad;  /* RL_OBJ_DIS only. The pages leave open whether f(r) is stop-gradient:
+                              1 = f(r) is a constant (dL/dlogp = -w f(r) A),
+                              0 = differentiated too (dL/dlogp = -w r A (1 + logp) inside the interval) */
 } rl_loss_config;
 
 /* One batch of T packed response tokens in S responses. */
@@ -120,7 +145,8 @@ typedef struct rl_loss_inputs {
     const float *logp_infer;      /* [T] log pi_old^infer(y_t), from the rollout engine */
     const uint8_t *mask;          /* [T] loss mask, nonzero = 1 */
     const int32_t *cu_seqlens;    /* [S+1] offsets: response i is tokens [cu[i], cu[i+1]); cu[0]=0, cu[S]=T */
-    const float *rewards_or_adv;  /* [S] rewards (RL_ADV_GROUP_REWARDS) or advantages (RL_ADV_PER_SEQ) */
+    const float *rewards_or_adv;  /* [S] rewards (RL_ADV_GROUP_REWARDS) or advantages (RL_ADV_PER_SEQ);
+                                     [T] advantages (RL_ADV_PER_TOKEN) or teacher log-probs (RL_ADV_TEACHER_LOGP) */
 } rl_loss_inputs;
 
 /* Where results go. Only `loss` and `dlogits` are required; NULL skips an output. */
@@ -134,7 +160,7 @@ typedef struct rl_loss_outputs {
     float *entropy;       /* [T] per-token entropy of softmax(z_t) in nats, or NULL */
     uint8_t *flags;       /* [T] RL_FLAG_* bits, or NULL */
     float *seq_adv;       /* [S] A_i as used, or NULL */
-    int32_t *counts;      /* [4] mask=1 tokens popped, mask=1 tokens clipped, mask=0 tokens,
+    int32_t *counts;      /* [4] mask=1 tokens popped (DIS: outside the interval), mask=1 tokens clipped, mask=0 tokens,
                              responses with no mask=1 token; or NULL */
     float *mean_entropy;  /* [1] mean entropy over mask=1 tokens, or NULL */
 } rl_loss_outputs;

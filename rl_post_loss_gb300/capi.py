@@ -17,7 +17,9 @@ LIB_PATH = os.path.join(HERE, "librl_loss.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "rl_loss.h")
 
 RL_F32, RL_BF16 = 0, 1
-RL_ADV_GROUP_REWARDS, RL_ADV_PER_SEQ = 0, 1
+RL_ADV_GROUP_REWARDS, RL_ADV_PER_SEQ, RL_ADV_PER_TOKEN, RL_ADV_TEACHER_LOGP = 0, 1, 2, 3
+RL_OBJ_GRPO_ICEPOP, RL_OBJ_DIS = 0, 1
+RL_NORM_PER_RESPONSE, RL_NORM_PER_TOKEN = 0, 1
 RL_FLAG_POP_IN_BOUNDS, RL_FLAG_CLIP_ACTIVE, RL_FLAG_MASKED, RL_FLAG_BAD_TARGET = 1, 2, 4, 8
 
 STATUS_NAMES = {0: "RL_OK", 1: "RL_ERR_INVALID_ARG", 2: "RL_ERR_SHAPE", 3: "RL_ERR_DTYPE",
@@ -38,7 +40,8 @@ class rl_loss_config(ctypes.Structure):
                 ("max_tokens", ctypes.c_int32), ("max_seqs", ctypes.c_int32),
                 ("eps_low", ctypes.c_float), ("eps_high", ctypes.c_float), ("beta", ctypes.c_float),
                 ("adv_eps", ctypes.c_float), ("adv_mode", ctypes.c_int32), ("std_unbiased", ctypes.c_int32),
-                ("pop_indicator", ctypes.c_int32), ("logits_dtype", ctypes.c_int32)]
+                ("pop_indicator", ctypes.c_int32), ("logits_dtype", ctypes.c_int32), ("objective", ctypes.c_int32),
+                ("loss_norm", ctypes.c_int32), ("dis_stopgrad", ctypes.c_int32)]
 
 
 class rl_loss_inputs(ctypes.Structure):
@@ -200,9 +203,11 @@ class RlLoss:
 
     def __init__(self, vocab_size: int, group_size: int, max_tokens: int, max_seqs: int, logits_dtype: int,
                  eps_low: float = 0.2, eps_high: float = 0.28, beta: float = 2.0, adv_eps: float = 1e-6,
-                 adv_mode: int = RL_ADV_GROUP_REWARDS, std_unbiased: bool = False, pop_indicator: bool = False):
+                 adv_mode: int = RL_ADV_GROUP_REWARDS, std_unbiased: bool = False, pop_indicator: bool = False,
+                 objective: int = RL_OBJ_GRPO_ICEPOP, loss_norm: int = RL_NORM_PER_RESPONSE, dis_stopgrad: bool = True):
         self.config = rl_loss_config(vocab_size, group_size, max_tokens, max_seqs, eps_low, eps_high, beta,
-                                     adv_eps, adv_mode, int(std_unbiased), int(pop_indicator), logits_dtype)
+                                     adv_eps, adv_mode, int(std_unbiased), int(pop_indicator), logits_dtype,
+                                     objective, loss_norm, int(dis_stopgrad))
         self.handle = rl_loss_create(self.config)
 
     def close(self):
@@ -295,7 +300,7 @@ def status_bits_to_names(bits: int) -> list[str]:
 def handle_for_batch(batch, max_tokens: int | None = None, max_seqs: int | None = None, **overrides) -> RlLoss:
     """A handle configured for a ``synthetic.Batch`` (capacity = the batch's size)."""
     kw = dict(eps_low=batch.eps_low, eps_high=batch.eps_high, beta=batch.beta, adv_eps=batch.adv_eps,
-              adv_mode=batch.adv_mode)
+              adv_mode=batch.adv_mode, objective=batch.objective, loss_norm=batch.loss_norm)
     kw.update(overrides)
     return RlLoss(batch.vocab, batch.group, max(1, max_tokens or batch.num_tokens), max_seqs or batch.num_seqs,
                   RL_BF16 if batch.dtype == "bf16" else RL_F32, **kw)
@@ -323,8 +328,9 @@ def alloc_outputs(batch, in_place: bool = False, ld: int | None = None) -> dict:
 
 def run_batch(rl: RlLoss, batch, outputs: dict, stream=None) -> dict:
     """One forward+backward of ``batch`` into ``outputs`` (asynchronous)."""
+    adv = batch.token_adv if (batch.adv_mode >= RL_ADV_PER_TOKEN) else batch.rewards_or_adv
     rl.forward_backward(batch.logits, batch.targets, batch.logp_old, batch.logp_infer, batch.mask,
-                        batch.cu_seqlens, batch.rewards_or_adv, stream=stream, **outputs)
+                        batch.cu_seqlens, adv, stream=stream, **outputs)
     return outputs
 
 
@@ -348,6 +354,7 @@ def alloc_projection_outputs(pb) -> dict:
 
 def run_projection(rl: RlLoss, pb, outputs: dict, stream=None) -> dict:
     b = pb.batch
+    adv = b.token_adv if (b.adv_mode >= RL_ADV_PER_TOKEN) else b.rewards_or_adv
     rl.fused_projection_forward_backward(pb.hidden, pb.w, b.targets, b.logp_old, b.logp_infer, b.mask, b.cu_seqlens,
-                                         b.rewards_or_adv, stream=stream, **outputs)
+                                         adv, stream=stream, **outputs)
     return outputs

@@ -36,15 +36,21 @@ struct LossConsts {
     float one_plus_eps_high;
     float one_minus_eps_low;
     int32_t pop_indicator;
+    int32_t objective;     // rl_objective
+    int32_t dis_stopgrad;  // RL_OBJ_DIS: f(r) held constant in the gradient
+    int32_t adv_teacher;   // A_t = fl32(logp_teacher - logp) (RL_ADV_TEACHER_LOGP)
 };
 
 // ---------------------------------------------------------------- per-token record
 //
 // Everything a row kernel needs about token t besides its logits row, prepared
-// once per call by token_prep (the parts of Eq. (1) of the GLM-5 report page,
-// section 3.2, that do not depend on the row's softmax):
-//   rec[t]  = {z_y, logp_old, pop*A*m, w*pop*A*m}   (the last two 0 when the token is masked,
-//                                                    popped or has a bad target)
+// once per call by token_prep (the parts of the objective that do not depend
+// on the row's softmax):
+//   rec[t]  = {z_y, l_ref, c, w * c}   with l_ref = logp_old (Eq. (1)) or the
+//             rollout log-prob logp_infer (DIS), and c = m * pop(rho) * A
+//             (Eq. (1)), m * pop(rho) (Eq. (1) with the distillation advantage,
+//             whose A needs logp), or m * A (DIS); c = 0 for masked, popped or
+//             bad-target tokens
 //   meta[t] = y (low 24 bits) | pre-flags << 24
 // pre-flags: RL_FLAG_POP_IN_BOUNDS, RL_FLAG_MASKED, RL_FLAG_BAD_TARGET, and the
 // sign of A in the two internal bits below (stripped from the output flags).
@@ -103,26 +109,44 @@ struct RowOut {
     uint32_t flags;
 };
 
-__device__ __forceinline__ RowOut finish_row(RowStats2 st, float4 rec, uint32_t meta, const LossConsts &c) {
+// `teacher` is log pi_teacher(y_t) when c.adv_teacher (ignored otherwise).
+__device__ __forceinline__ RowOut finish_row(RowStats2 st, float4 rec, uint32_t meta, const LossConsts &c,
+                                             float teacher = 0.f) {
     RowOut o;
     const float log2S = log2f(st.s);
     o.logZ2 = st.m2 + log2S;
     const float logZ = o.logZ2 * kLn2;
     o.H = (log2S - st.u2 / st.s) * kLn2;
-    const uint32_t pre = meta >> 24;
+    uint32_t pre = meta >> 24;
     o.y = meta & kMetaYMask;
     const bool ok = !(pre & RL_FLAG_BAD_TARGET);
     o.logp = ok ? __fsub_rn(rec.x, logZ) : __int_as_float(0x7fc00000);
     const float e = __fsub_rn(o.logp, rec.y);  // ln r, one fp32 subtraction
-    const bool clip = ok && (((pre & kPreAPos) && e > c.clip_hi) || ((pre & kPreANeg) && e < c.clip_lo));
-    o.flags = (pre & kPreOut) | (clip ? RL_FLAG_CLIP_ACTIVE : 0u);
     o.obj = 0.f;
     o.g = 0.f;
-    if (rec.z != 0.f) {  // m * pop * A != 0
+    if (c.objective == RL_OBJ_DIS) {
+        // direct double-sided importance sampling: f(r) = r on the open interval
+        const bool gate = ok && e > c.clip_lo && e < c.clip_hi;
+        o.flags = (pre & (RL_FLAG_MASKED | RL_FLAG_BAD_TARGET)) | (gate ? RL_FLAG_POP_IN_BOUNDS : 0u);
+        if (gate && rec.z != 0.f) {  // m * A != 0
+            const float ratio = expf(e);
+            o.obj = rec.z * ratio * o.logp;
+            o.g = c.dis_stopgrad ? -rec.w * ratio : -rec.w * ratio * (1.f + o.logp);
+        }
+        return o;
+    }
+    float A = 1.f;  // rec.z / rec.w already carry A unless it comes from the teacher
+    if (c.adv_teacher) {
+        A = ok ? __fsub_rn(teacher, o.logp) : 0.f;  // sg[log pi_teacher - log pi_theta], in fp32
+        pre = (pre & ~(kPreAPos | kPreANeg)) | (A > 0.f ? kPreAPos : 0u) | (A < 0.f ? kPreANeg : 0u);
+    }
+    const bool clip = ok && (((pre & kPreAPos) && e > c.clip_hi) || ((pre & kPreANeg) && e < c.clip_lo));
+    o.flags = (pre & kPreOut) | (clip ? RL_FLAG_CLIP_ACTIVE : 0u);
+    if (rec.z != 0.f && A != 0.f) {  // m * pop * A != 0
         const float ratio = expf(e);
         const float branch = clip ? ((pre & kPreAPos) ? c.one_plus_eps_high : c.one_minus_eps_low) : ratio;
-        o.obj = rec.z * branch;
-        o.g = clip ? 0.f : -rec.w * ratio;
+        o.obj = rec.z * A * branch;
+        o.g = clip ? 0.f : -rec.w * A * ratio;
     }
     return o;
 }
@@ -182,7 +206,7 @@ struct SeqPrepParams {
     const int32_t *cu_seqlens;
     const uint8_t *mask;
     const float *rewards_or_adv;
-    int32_t num_seqs, num_tokens, group_size, adv_mode, std_unbiased;
+    int32_t num_seqs, num_tokens, group_size, adv_mode, std_unbiased, loss_norm;
     float adv_eps;
     float *seq_adv;      // workspace [S]
     float *seq_w;        // workspace [S] fp32 1/(S n_i)
@@ -205,6 +229,7 @@ struct TokenPrepParams {
     int32_t num_seqs, num_tokens, vocab;
     const float *seq_adv;
     const float *seq_w;
+    const float *token_adv;  // [T] per-token advantages (RL_ADV_PER_TOKEN), else null
     LossConsts c;
     float4 *rec;     // workspace [T]
     uint32_t *meta;  // workspace [T]
@@ -218,6 +243,7 @@ struct RowParams {
     int64_t ld_dlogits;
     const float4 *rec;
     const uint32_t *meta;
+    const float *teacher;  // [T] log pi_teacher (RL_ADV_TEACHER_LOGP), else null
     int32_t num_tokens, vocab;
     LossConsts c;
     float *logp_out;     // optional
@@ -246,6 +272,8 @@ struct ReduceParams {
 };
 
 cudaError_t launch_seg_prep(const SeqPrepParams &p, cudaStream_t stream);
+// RL_NORM_PER_TOKEN: w_i = 1 / sum_j |y_j| (one block, fixed order); after seg_prep.
+cudaError_t launch_seg_token_norm(const SeqPrepParams &p, cudaStream_t stream);
 cudaError_t launch_token_prep(const TokenPrepParams &p, cudaStream_t stream);
 cudaError_t launch_seg_reduce(const ReduceParams &p, cudaStream_t stream);
 cudaError_t launch_final_reduce(const ReduceParams &p, cudaStream_t stream);

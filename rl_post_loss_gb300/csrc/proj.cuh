@@ -36,6 +36,7 @@ struct ProjRowParams {
     int32_t rows, vocab;
     const float4 *rec;   // per-token records (indexed by token)
     const uint32_t *meta;
+    const float *teacher; // [T] log pi_teacher (RL_ADV_TEACHER_LOGP), else null
     LossConsts c;
     float *logp_out;     // optional, indexed by token
     float *entropy_out;

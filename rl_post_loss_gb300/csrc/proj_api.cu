@@ -155,6 +155,7 @@ RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(
     sp.group_size = c.group_size;
     sp.adv_mode = c.adv_mode;
     sp.std_unbiased = c.std_unbiased;
+    sp.loss_norm = c.loss_norm;
     sp.adv_eps = c.adv_eps;
     sp.seq_adv = h->seq_adv;
     sp.seq_w = h->seq_w;
@@ -164,6 +165,7 @@ RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(
     sp.status = h->status;
     int slot = h->prof_begin(kSegPrep, stream);
     cudaError_t e = rlk::launch_seg_prep(sp, stream);
+    if (e == cudaSuccess && c.loss_norm == RL_NORM_PER_TOKEN) e = rlk::launch_seg_token_norm(sp, stream);
     h->prof_end(slot, stream);
     if (e != cudaSuccess) return cuda_fail(h, e);
     int64_t launches = 1;
@@ -204,6 +206,7 @@ RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(
         tp.vocab = V;
         tp.seq_adv = h->seq_adv;
         tp.seq_w = h->seq_w;
+        tp.token_adv = c.adv_mode == RL_ADV_PER_TOKEN ? in->rewards_or_adv : nullptr;
         tp.c = h->consts;
         tp.rec = h->tok_rec;
         tp.meta = h->tok_meta;
@@ -225,6 +228,7 @@ RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(
         rp.vocab = V;
         rp.rec = h->tok_rec;
         rp.meta = h->tok_meta;
+        rp.teacher = c.adv_mode == RL_ADV_TEACHER_LOGP ? in->rewards_or_adv : nullptr;
         rp.c = h->consts;
         rp.logp_out = out->logp;
         rp.entropy_out = entropy;

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kThreads) proj_rows_kernel(ProjRowParams p) {
         RowStats2 w = lane < kThreads / 32 ? warp_stats[lane] : empty_stats();
         w = warp_merge_stats2(w);
         if (lane == 0) {
-            const RowOut o = finish_row(w, __ldg(p.rec + t), __ldg(p.meta + t), p.c);
+            const RowOut o = finish_row(w, __ldg(p.rec + t), __ldg(p.meta + t), p.c, p.teacher ? __ldg(p.teacher + t) : 0.f);
             if (!isfinite(o.logZ2)) raise_status(p.status, RL_ERR_NONFINITE);
             if (p.logp_out) p.logp_out[t] = o.logp;
             p.entropy_out[t] = o.H;

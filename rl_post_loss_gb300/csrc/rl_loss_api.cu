@@ -56,6 +56,32 @@ static size_t workspace_layout(const rl_loss_config &c, rl_loss_handle_s *h, cha
 
 static int elem_size(int32_t dtype) { return dtype == RL_F32 ? 4 : 2; }
 
+// Objective / advantage / normalisation codes of a configuration are known and compatible.
+static bool config_modes_valid(const rl_loss_config &c) {
+    if (c.adv_mode < RL_ADV_GROUP_REWARDS || c.adv_mode > RL_ADV_TEACHER_LOGP) return false;
+    if (c.std_unbiased && c.adv_mode == RL_ADV_GROUP_REWARDS && c.group_size < 2) return false;
+    if (c.objective != RL_OBJ_GRPO_ICEPOP && c.objective != RL_OBJ_DIS) return false;
+    if (c.objective == RL_OBJ_DIS && c.adv_mode == RL_ADV_TEACHER_LOGP) return false;
+    if (c.loss_norm != RL_NORM_PER_RESPONSE && c.loss_norm != RL_NORM_PER_TOKEN) return false;
+    if (c.dis_stopgrad != 0 && c.dis_stopgrad != 1) return false;
+    return true;
+}
+
+// fp32 decision thresholds, each rounded once from a double, and the modes.
+static rlk::LossConsts loss_consts(const rl_loss_config &c) {
+    rlk::LossConsts k{};
+    k.ln_beta = (float)std::log((double)c.beta);
+    k.clip_hi = (float)std::log1p((double)c.eps_high);
+    k.clip_lo = (float)std::log1p(-(double)c.eps_low);
+    k.one_plus_eps_high = 1.f + c.eps_high;
+    k.one_minus_eps_low = 1.f - c.eps_low;
+    k.pop_indicator = c.pop_indicator ? 1 : 0;
+    k.objective = c.objective;
+    k.dis_stopgrad = c.dis_stopgrad;
+    k.adv_teacher = c.adv_mode == RL_ADV_TEACHER_LOGP ? 1 : 0;
+    return k;
+}
+
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 extern "C" {
@@ -95,8 +121,7 @@ RL_LOSS_API rl_status rl_loss_create(const rl_loss_config *config, rl_loss_t *ou
     if (!(c.eps_low >= 0.f && c.eps_low < 1.f) || !(c.eps_high >= 0.f) || !std::isfinite(c.eps_high))
         return RL_ERR_INVALID_ARG;
     if (!(c.adv_eps >= 0.f) || !std::isfinite(c.adv_eps)) return RL_ERR_INVALID_ARG;
-    if (c.adv_mode != RL_ADV_GROUP_REWARDS && c.adv_mode != RL_ADV_PER_SEQ) return RL_ERR_INVALID_ARG;
-    if (c.std_unbiased && c.adv_mode == RL_ADV_GROUP_REWARDS && c.group_size < 2) return RL_ERR_INVALID_ARG;
+    if (!config_modes_valid(c)) return RL_ERR_INVALID_ARG;
 
     rl_loss_handle_s *h = new (std::nothrow) rl_loss_handle_s();
     if (!h) return RL_ERR_INVALID_ARG;
@@ -105,13 +130,7 @@ RL_LOSS_API rl_status rl_loss_create(const rl_loss_config *config, rl_loss_t *ou
         delete h;
         return RL_ERR_CUDA;
     }
-    // fp32 decision thresholds, each rounded once from a double
-    h->consts.ln_beta = (float)std::log((double)c.beta);
-    h->consts.clip_hi = (float)std::log1p((double)c.eps_high);
-    h->consts.clip_lo = (float)std::log1p(-(double)c.eps_low);
-    h->consts.one_plus_eps_high = 1.f + c.eps_high;
-    h->consts.one_minus_eps_low = 1.f - c.eps_low;
-    h->consts.pop_indicator = c.pop_indicator ? 1 : 0;
+    h->consts = loss_consts(c);
 
     h->ws_bytes = workspace_layout(c, nullptr, nullptr);
     if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
@@ -180,6 +199,7 @@ RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t h, const rl_loss_inputs
     sp.group_size = c.group_size;
     sp.adv_mode = c.adv_mode;
     sp.std_unbiased = c.std_unbiased;
+    sp.loss_norm = c.loss_norm;
     sp.adv_eps = c.adv_eps;
     sp.seq_adv = h->seq_adv;
     sp.seq_w = h->seq_w;
@@ -204,6 +224,7 @@ RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t h, const rl_loss_inputs
     tp.vocab = V;
     tp.seq_adv = h->seq_adv;
     tp.seq_w = h->seq_w;
+    tp.token_adv = c.adv_mode == RL_ADV_PER_TOKEN ? in->rewards_or_adv : nullptr;
     tp.c = h->consts;
     tp.rec = h->tok_rec;
     tp.meta = h->tok_meta;
@@ -216,6 +237,7 @@ RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t h, const rl_loss_inputs
     rp.ld_dlogits = out->ld_dlogits;
     rp.rec = h->tok_rec;
     rp.meta = h->tok_meta;
+    rp.teacher = c.adv_mode == RL_ADV_TEACHER_LOGP ? in->rewards_or_adv : nullptr;
     rp.num_tokens = T;
     rp.vocab = V;
     rp.c = h->consts;
@@ -250,6 +272,7 @@ RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t h, const rl_loss_inputs
     };
     int slot = h->prof_begin(kSegPrep, stream);
     err = rlk::launch_seg_prep(sp, stream);
+    if (err == cudaSuccess && c.loss_norm == RL_NORM_PER_TOKEN) err = rlk::launch_seg_token_norm(sp, stream);
     h->prof_end(slot, stream);
     if (err != cudaSuccess) return failed(err);
     slot = h->prof_begin(kTokenPrep, stream);
@@ -268,7 +291,7 @@ RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t h, const rl_loss_inputs
     err = rlk::launch_final_reduce(rd, stream);
     h->prof_end(slot, stream);
     if (err != cudaSuccess) return failed(err);
-    h->launches += (T > 0) ? 5 : 3;
+    h->launches += ((T > 0) ? 5 : 3) + (c.loss_norm == RL_NORM_PER_TOKEN ? 1 : 0);
     return RL_OK;
 }
 
@@ -375,8 +398,7 @@ extern "C" RL_LOSS_API rl_status rl_loss_forward_backward_noalloc(const rl_loss_
     if (!(c.eps_low >= 0.f && c.eps_low < 1.f) || !(c.eps_high >= 0.f) || !std::isfinite(c.eps_high))
         return RL_ERR_INVALID_ARG;
     if (!(c.adv_eps >= 0.f) || !std::isfinite(c.adv_eps)) return RL_ERR_INVALID_ARG;
-    if (c.adv_mode != RL_ADV_GROUP_REWARDS && c.adv_mode != RL_ADV_PER_SEQ) return RL_ERR_INVALID_ARG;
-    if (c.std_unbiased && c.adv_mode == RL_ADV_GROUP_REWARDS && c.group_size < 2) return RL_ERR_INVALID_ARG;
+    if (!config_modes_valid(c)) return RL_ERR_INVALID_ARG;
     if (inputs->num_tokens > kNoAllocMaxTokens || inputs->num_seqs > kNoAllocMaxSeqs) return RL_ERR_CAPACITY;
 
     int device = -1;
@@ -391,12 +413,7 @@ extern "C" RL_LOSS_API rl_status rl_loss_forward_backward_noalloc(const rl_loss_
     h.cfg.max_tokens = kNoAllocMaxTokens;
     h.cfg.max_seqs = kNoAllocMaxSeqs;
     h.device = device;
-    h.consts.ln_beta = (float)std::log((double)c.beta);
-    h.consts.clip_hi = (float)std::log1p((double)c.eps_high);
-    h.consts.clip_lo = (float)std::log1p(-(double)c.eps_low);
-    h.consts.one_plus_eps_high = 1.f + c.eps_high;
-    h.consts.one_minus_eps_low = 1.f - c.eps_low;
-    h.consts.pop_indicator = c.pop_indicator ? 1 : 0;
+    h.consts = loss_consts(c);
     h.ws_bytes = workspace_layout(h.cfg, nullptr, nullptr);
     if (h.ws_bytes > kNoAllocScratchBytes) return RL_ERR_CAPACITY;
     h.ws = scratch;

@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kRowThreads) row_loss_twopass_kernel(RowParams
         RowStats2 w = lane < kRowThreads / 32 ? warp_stats[lane] : empty_stats();
         w = warp_merge_stats2(w);
         if (lane == 0) {
-            const RowOut o = finish_row(w, rec, meta, p.c);
+            const RowOut o = finish_row(w, rec, meta, p.c, p.teacher ? __ldg(p.teacher + row) : 0.f);
             if (!isfinite(o.logZ2)) raise_status(p.status, RL_ERR_NONFINITE);  // NaN or +inf logit in the row
             if (p.logp_out) p.logp_out[row] = o.logp;
             p.entropy_out[row] = o.H;

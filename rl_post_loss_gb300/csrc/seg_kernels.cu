@@ -44,7 +44,9 @@ __global__ void __launch_bounds__(kPrepThreads) seg_prep_kernel(SeqPrepParams p)
     p.seq_w[i] = (float)w;
     if (n == 0) raise_status(p.status, RL_ERR_EMPTY_SEQ);
     float a;
-    if (p.adv_mode == RL_ADV_PER_SEQ) {
+    if (p.adv_mode == RL_ADV_PER_TOKEN || p.adv_mode == RL_ADV_TEACHER_LOGP) {
+        a = 0.f;  // per-token advantages: nothing per response
+    } else if (p.adv_mode == RL_ADV_PER_SEQ) {
         a = p.rewards_or_adv[i];
     } else {
         // group statistics in double, fixed order over the group's G rewards;
@@ -66,6 +68,21 @@ __global__ void __launch_bounds__(kPrepThreads) seg_prep_kernel(SeqPrepParams p)
     if (p.seq_adv_out) p.seq_adv_out[i] = a;
 }
 
+// One block: the number of generated tokens of the batch (fixed-order sum of
+// |y_i|) and w_i = 1 / that number for the mean over tokens.
+__global__ void __launch_bounds__(kReduceThreads) seg_token_norm_kernel(SeqPrepParams p) {
+    __shared__ int iscratch[32];
+    int n = 0;
+    for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) n += p.seq_n[i];
+    n = block_sum_i32(n, iscratch);
+    const double w = n > 0 ? 1.0 / (double)n : 0.0;
+    for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) {
+        const double wi = p.seq_n[i] > 0 ? w : 0.0;
+        p.seq_w64[i] = wi;
+        p.seq_w[i] = (float)wi;
+    }
+}
+
 // One thread per token.
 __global__ void __launch_bounds__(kTokenThreads) token_prep_kernel(TokenPrepParams p) {
     const int i_row = blockIdx.x * kTokenThreads + threadIdx.x;
@@ -73,7 +90,7 @@ __global__ void __launch_bounds__(kTokenThreads) token_prep_kernel(TokenPrepPara
     const int t = p.row0 + i_row;
     const int i = find_seq(p.cu_seqlens, p.num_seqs, t);
     if (i < 0) raise_status(p.status, RL_ERR_SEQLENS);
-    const float A = i >= 0 ? p.seq_adv[i] : 0.f;
+    const float A = p.token_adv ? __ldg(p.token_adv + t) : (i >= 0 ? p.seq_adv[i] : 0.f);
     const float w = i >= 0 ? p.seq_w[i] : 0.f;
     const int y = __ldg(p.targets + t);
     const bool ok = (y >= 0) && (y < p.vocab);
@@ -92,11 +109,19 @@ __global__ void __launch_bounds__(kTokenThreads) token_prep_kernel(TokenPrepPara
             zy = __uint_as_float(static_cast<uint32_t>(b) << 16);
         }
     }
-    float popA = 0.f;
-    if (m && ok && in_bounds) popA = (p.c.pop_indicator ? 1.f : expf(d)) * A;
-    const uint32_t pre = (in_bounds ? RL_FLAG_POP_IN_BOUNDS : 0u) | (m ? 0u : RL_FLAG_MASKED) |
-                         (ok ? 0u : RL_FLAG_BAD_TARGET) | (A > 0.f ? kPreAPos : 0u) | (A < 0.f ? kPreANeg : 0u);
-    p.rec[t] = make_float4(zy, lo, popA, w * popA);
+    uint32_t pre = (m ? 0u : RL_FLAG_MASKED) | (ok ? 0u : RL_FLAG_BAD_TARGET) | (A > 0.f ? kPreAPos : 0u) |
+                   (A < 0.f ? kPreANeg : 0u);
+    float cf = 0.f, lref = lo;
+    if (p.c.objective == RL_OBJ_DIS) {
+        // the gate needs logp: the token carries m * A and the rollout log-prob
+        lref = __ldg(p.logp_infer + t);
+        if (m && ok) cf = A;
+    } else {
+        pre |= in_bounds ? RL_FLAG_POP_IN_BOUNDS : 0u;
+        const float pop = (m && ok && in_bounds) ? (p.c.pop_indicator ? 1.f : expf(d)) : 0.f;
+        cf = p.c.adv_teacher ? pop : pop * A;  // the distillation advantage is applied once logp is known
+    }
+    p.rec[t] = make_float4(zy, lref, cf, w * cf);
     p.meta[t] = (ok ? (uint32_t)y : 0u) | (pre << 24);
 }
 
@@ -177,6 +202,11 @@ __global__ void __launch_bounds__(kReduceThreads) final_reduce_kernel(ReducePara
 
 cudaError_t launch_seg_prep(const SeqPrepParams &p, cudaStream_t stream) {
     seg_prep_kernel<<<p.num_seqs, kPrepThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_seg_token_norm(const SeqPrepParams &p, cudaStream_t stream) {
+    seg_token_norm_kernel<<<1, kReduceThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -77,6 +77,9 @@ class Batch:
     eps_high: float = EPS_HIGH
     adv_eps: float = ADV_EPS
     meta: dict = field(default_factory=dict)
+    token_adv: torch.Tensor | None = None  # [T] advantages (adv_mode 2) or teacher log-probs (adv_mode 3)
+    objective: int = 0                     # 0: GRPO + IcePop, 1: direct double-sided importance sampling
+    loss_norm: int = 0                     # 0: per response, 1: mean over generated tokens
 
     @property
     def num_tokens(self) -> int:
@@ -91,7 +94,8 @@ class Batch:
               ("logits", "targets", "logp_old", "logp_infer", "mask", "cu_seqlens", "rewards_or_adv")}
         return Batch(**kw, vocab=self.vocab, group=self.group, dtype=self.dtype, adv_mode=self.adv_mode,
                      beta=self.beta, eps_low=self.eps_low, eps_high=self.eps_high, adv_eps=self.adv_eps,
-                     meta=dict(self.meta))
+                     meta=dict(self.meta), objective=self.objective, loss_norm=self.loss_norm,
+                     token_adv=None if self.token_adv is None else self.token_adv.to(device))
 
 
 def _gen(device, base: int, stream: int) -> torch.Generator:
@@ -211,11 +215,26 @@ def make_batch(case_id: int, device="cpu", seed: int = 0, lengths: list[int] | N
     rng = np.random.default_rng(base * 100 + 7)
     mask = np.concatenate([span_mask(L, case["mask_frac"], rng) for L in lengths]) if T else np.zeros(0, np.uint8)
 
+    # optional variants of the objective (overrides): per-token advantages ~ N(0, 1)
+    # ("token_adv": "normal", adv_mode 2), teacher log-probs logp_old + N(0, teacher_noise)
+    # ("token_adv": "teacher", adv_mode 3), the DIS objective ("objective": 1), the
+    # mean over tokens ("loss_norm": 1)
+    token_adv, adv_mode = None, case["adv_mode"]
+    if case.get("token_adv"):
+        g_ta = _gen(device, base, 9)
+        if case["token_adv"] == "teacher":
+            token_adv = (logp_old + case.get("teacher_noise", 0.3) * torch.randn(T, generator=g_ta, device=device))
+            adv_mode = 3
+        else:
+            token_adv = torch.randn(T, generator=g_ta, device=device)
+            adv_mode = 2
+        token_adv = token_adv.float().contiguous()
     return Batch(logits=logits, targets=targets, logp_old=logp_old.float().contiguous(),
                  logp_infer=logp_infer.float().contiguous(), mask=torch.from_numpy(mask).to(device),
                  cu_seqlens=cu.to(device), rewards_or_adv=rw.float().to(device), vocab=V, group=G,
-                 dtype=case["dtype"], adv_mode=case["adv_mode"], beta=case["beta"],
-                 meta=dict(case=case_id, name=case["name"], seed=seed, lengths=list(lengths)))
+                 dtype=case["dtype"], adv_mode=adv_mode, beta=case["beta"],
+                 meta=dict(case=case_id, name=case["name"], seed=seed, lengths=list(lengths)),
+                 token_adv=token_adv, objective=case.get("objective", 0), loss_norm=case.get("loss_norm", 0))
 
 
 def to_numpy(batch: Batch) -> dict:

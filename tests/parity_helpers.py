@@ -8,7 +8,9 @@ oracle's own decision wherever the oracle's log-prob is not within the
 log-prob tolerance of a clip threshold. On top of the stated dL/dlogits bound a
 tighter one is checked that follows from the arithmetic: one rounding to the
 output dtype (2^-9 relative for bf16) plus about 1e-6 relative from the fp32
-softmax, i.e. rel 4e-3 (bf16) / 1e-5 (fp32) + 2e-6 |dL/dlogp| + 1e-30.
+softmax, i.e. rel 4e-3 (bf16) / 1e-5 (fp32) + 2e-6 |dL/dlogp| + 1e-30; for the
+DIS objective without stop-gradient the factor (1 + logp) of dL/dlogp adds
+1e-5 / |1 + logp| relative.
 """
 from __future__ import annotations
 
@@ -27,7 +29,8 @@ DZ_STRICT_REL = {"f32": 1e-5, "bf16": 4e-3}
 
 def params_for(batch, **over) -> LossParams:
     kw = dict(group_size=batch.group, eps_low=batch.eps_low, eps_high=batch.eps_high, beta=batch.beta,
-              adv_eps=batch.adv_eps, adv_mode=batch.adv_mode)
+              adv_eps=batch.adv_eps, adv_mode=batch.adv_mode, objective=batch.objective,
+              loss_norm=batch.loss_norm)
     kw.update(over)
     return LossParams(**kw)
 
@@ -60,6 +63,7 @@ class OracleRun:
                                                        cu_seqlens=batch.cu_seqlens,
                                                        rewards_or_adv=batch.rewards_or_adv).items()}
         a = self.np
+        self.token_adv = None if batch.token_adv is None else batch.token_adv.cpu().numpy()
         self.n, self.adv, self.w = oracle.seq_prep(a["cu_seqlens"], a["mask"], a["rewards_or_adv"], p)
         T = batch.num_tokens
         parts = []
@@ -74,9 +78,15 @@ class OracleRun:
         a = self.np
         return oracle.rows(ids, logits_rows_np(self.batch, ids), odtype(self.batch), self.batch.vocab,
                            a["targets"], a["logp_old"], a["logp_infer"], a["mask"], a["cu_seqlens"], self.adv,
-                           self.w, self.p, want_dz=want_dz)
+                           self.w, self.p, want_dz=want_dz, token_adv=self.token_adv)
 
-    def adv_per_token(self) -> np.ndarray:
+    def adv_per_token(self, logp32=None) -> np.ndarray:
+        """Each token's advantage; for the distillation advantage, its fp32
+        value from the given fp32 log-probs (the sign decides the clip side)."""
+        if self.p.adv_mode == 2:
+            return self.token_adv.astype(np.float64)
+        if self.p.adv_mode == 3:
+            return (self.token_adv.astype(np.float32) - np.asarray(logp32, np.float32)).astype(np.float64)
         cu = self.np["cu_seqlens"]
         return np.repeat(self.adv, np.diff(cu))
 
@@ -91,25 +101,40 @@ def check_tokens(batch, run: OracleRun, out: dict, report: dict | None = None):
     ok_t = (o["flags"] & 8) == 0
     assert np.array_equal(flags & 8, o["flags"] & 8), "bad-target bits differ"
     assert np.array_equal(flags & 4, o["flags"] & 4), "mask bits differ"
-    assert np.array_equal(flags & 1, o["flags"] & 1), "pop bits differ"
     err = np.abs(logp[ok_t] - o["logp"][ok_t])
     assert err.size == 0 or err.max() <= tol, f"logp max err {err.max()}"
     assert np.all(np.isnan(logp[~ok_t]))
     eerr = np.abs(ent - o["entropy"])
     assert eerr.size == 0 or eerr.max() <= tol, f"entropy max err {eerr.max()}"
-    # clip bits: exact against the rule applied to the kernel's own fp32 log-prob
-    advt = run.adv_per_token()
-    lo = run.np["logp_old"]
     lp32 = out["logp"].cpu().numpy()
-    rule = oracle.clip_active_vec(np.where(ok_t, lp32, 0), lo, np.where(ok_t, advt, 0.0), run.p.eps_low,
-                                  run.p.eps_high)
-    assert np.array_equal((flags >> 1) & 1, rule), "clip bits differ from the rule on the kernel's logp"
-    # and equal to the oracle's own decision away from the thresholds
     hi, lo_thr = oracle.thresholds_f32(run.p.beta, run.p.eps_low, run.p.eps_high)[1:]
-    e64 = o["logp"] - lo.astype(np.float64)
-    near = ok_t & ((np.abs(e64 - hi) <= tol) | (np.abs(e64 - lo_thr) <= tol))
-    diff = ((flags >> 1) & 1) != ((o["flags"] >> 1) & 1)
-    assert not np.any(diff & ~near), "clip bits differ away from a threshold"
+    if run.p.objective == 1:
+        # the DIS gate: exact against the rule on the kernel's own fp32 log-prob
+        li = run.np["logp_infer"]
+        e32 = (np.where(ok_t, lp32, 0).astype(np.float32) - li.astype(np.float32)).astype(np.float32)
+        rule = (ok_t & (e32 > lo_thr) & (e32 < hi)).astype(np.uint8)
+        assert np.array_equal(flags & 1, rule), "DIS gate bits differ from the rule on the kernel's logp"
+        assert not np.any(flags & 2)
+        e64 = o["logp"] - li.astype(np.float64)
+        near = ok_t & ((np.abs(e64 - hi) <= tol) | (np.abs(e64 - lo_thr) <= tol))
+        diff = (flags & 1) != (o["flags"] & 1)
+        assert not np.any(diff & ~near), "DIS gate bits differ away from a threshold"
+    else:
+        assert np.array_equal(flags & 1, o["flags"] & 1), "pop bits differ"
+        # clip bits: exact against the rule applied to the kernel's own fp32 log-prob
+        advt = run.adv_per_token(lp32)
+        lo = run.np["logp_old"]
+        rule = oracle.clip_active_vec(np.where(ok_t, lp32, 0), lo, np.where(ok_t, advt, 0.0), run.p.eps_low,
+                                      run.p.eps_high)
+        assert np.array_equal((flags >> 1) & 1, rule), "clip bits differ from the rule on the kernel's logp"
+        # and equal to the oracle's own decision away from the thresholds (and, for
+        # the distillation advantage, away from a zero advantage)
+        e64 = o["logp"] - lo.astype(np.float64)
+        near = ok_t & ((np.abs(e64 - hi) <= tol) | (np.abs(e64 - lo_thr) <= tol))
+        if run.p.adv_mode == 3:
+            near |= ok_t & (np.abs(run.token_adv.astype(np.float64) - o["logp"]) <= tol)
+        diff = ((flags >> 1) & 1) != ((o["flags"] >> 1) & 1)
+        assert not np.any(diff & ~near), "clip bits differ away from a threshold"
     if report is not None:
         report.update(logp_max_err=float(err.max()) if err.size else 0.0,
                       entropy_max_err=float(eerr.max()) if eerr.size else 0.0,
@@ -132,8 +157,8 @@ def check_seq_outputs(batch, run: OracleRun, out: dict):
     cnt = out["counts"].cpu().numpy()
     o = run.tok["flags"]
     m = run.np["mask"] != 0
-    assert cnt[0] == int((m & ((o & 1) == 0)).sum()), "popped count"
     gflags = out["flags"].cpu().numpy()
+    assert cnt[0] == int((m & ((gflags & 1) == 0)).sum()), "popped count"
     assert cnt[1] == int((m & ((gflags & 2) != 0)).sum()), "clipped count"
     assert cnt[2] == int((~m).sum()), "masked count"
     assert cnt[3] == int((run.n == 0).sum()), "empty responses"
@@ -156,7 +181,12 @@ def check_dz_rows(batch, run: OracleRun, out: dict, row_ids, skip_rows=None, rep
     bound = DZ_ABS + DZ_REL * np.abs(dz)
     assert np.all(err <= bound), f"dlogits stated bound: worst excess {(err - bound).max()}"
     g = np.abs(ref["g"])[:, None]
-    strict = DZ_STRICT_REL[batch.dtype] * np.abs(dz) + 2e-6 * g + 1e-30
+    rel = np.full((row_ids.size, 1), DZ_STRICT_REL[batch.dtype])
+    if run.p.objective == 1 and not run.p.dis_stopgrad:
+        # dL/dlogp = -w r A (1 + logp): an fp32 logp (abs error ~1e-6) makes the
+        # factor (1 + logp) lose relative accuracy as logp approaches -1
+        rel = rel + 1e-5 / np.maximum(np.abs(1.0 + ref["logp"]), 1e-12)[:, None]
+    strict = rel * np.abs(dz) + 2e-6 * g + 1e-30
     bad = err > strict
     assert not bad.any(), f"dlogits strict bound violated at {np.argwhere(bad)[:5]} ({err[bad][:5]}, {dz[bad][:5]})"
     zero_rows = ref["g"] == 0.0
