@@ -264,3 +264,29 @@ def projection_forward_backward_f64(h: np.ndarray, W: np.ndarray, batch: dict, p
 def projection_forward_backward(hidden_bits, w_bits, batch: dict, p: LossParams) -> dict:
     """The same on bf16 inputs (bit patterns), widened exactly to float64."""
     return projection_forward_backward_f64(bf16_bits_to_f64(hidden_bits), bf16_bits_to_f64(w_bits), batch, p)
+
+
+# ---------------------------------------------------------------------------- GAE
+
+def gae(cu_seqlens, rewards, values, mask, gamma: float, lam: float, skip_observations: bool = True,
+        rollout_ids=None) -> np.ndarray:
+    """Skip-observation GAE per response, optionally with the cross-trajectory
+    discount over consecutive responses of one rollout (see oracle_gae)."""
+    lib = _load()
+    if not hasattr(lib, "_gae_typed"):
+        P = ctypes.c_void_p
+        lib.oracle_gae.argtypes = [ctypes.c_int64, P, P, P, P, ctypes.c_double, ctypes.c_double, ctypes.c_int32,
+                                   P, P]
+        lib.oracle_gae.restype = ctypes.c_int32
+        lib._gae_typed = True
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    r = np.ascontiguousarray(rewards, dtype=np.float32)
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    m = np.ascontiguousarray(mask, dtype=np.uint8)
+    ro = None if rollout_ids is None else np.ascontiguousarray(rollout_ids, dtype=np.int32)
+    out = np.zeros(int(cu[-1]) if cu.size else 0, np.float64)
+    rc = lib.oracle_gae(cu.shape[0] - 1, _ptr(cu), _ptr(r), _ptr(v), _ptr(m), gamma, lam, int(skip_observations),
+                        _ptr(ro), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_gae rejected its arguments")
+    return out

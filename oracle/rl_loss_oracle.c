@@ -300,3 +300,58 @@ double oracle_loss(int64_t S, const int32_t *cu_seqlens, const double *w, const 
     }
     return L;
 }
+
+/*
+ * Generalized advantage estimation over packed responses, with observation
+ * tokens skipped ("Zhipu AI / GLM: From Blank Infilling to Compaction-Aware
+ * Agentic Reinforcement Learning", section 11, "Restoring a critic at group
+ * size one": skip-observation GAE, and "Token loss and cross-trajectory GAE").
+ *
+ * Within response i the action tokens are the mask=1 tokens; observation
+ * (mask=0) tokens are skipped: the recursion links an action token directly to
+ * the next action token of the same response. Walking backwards over the
+ * action tokens t with next action token t' (none after the last one):
+ *   delta_t = r_t + gamma * V_{t'} - V_t           (V_{t'} = 0 after the last action token)
+ *   A_t     = delta_t + gamma * lambda * A_{t'}    (A_{t'} = 0 after the last action token)
+ * Observation tokens get A = 0. With skip_observations = 0 every token is an
+ * action token (plain token-level GAE).
+ *
+ * Cross-trajectory discount (rollout_ids != NULL): consecutive responses with
+ * the same rollout id are the segments of one rollout; segment s's advantages
+ * are multiplied by (gamma * lambda)^{N_{>s}}, N_{>s} being the number of
+ * trainable (mask=1) tokens in the later segments of the same rollout.
+ * Readings: gamma and lambda are inputs (the pages leave them undisclosed);
+ * rewards are per token (zero except where the environment pays out).
+ * Everything in double. Returns 0, or -1 on bad arguments.
+ */
+int32_t oracle_gae(int64_t S, const int32_t *cu_seqlens, const float *rewards, const float *values,
+                   const uint8_t *mask, double gamma, double lambda, int32_t skip_observations,
+                   const int32_t *rollout_ids, double *adv) {
+    if (S < 0) return -1;
+    for (int64_t i = 0; i < S; ++i) {
+        if (cu_seqlens[i + 1] < cu_seqlens[i]) return -1;
+        double A_next = 0.0, V_next = 0.0;
+        for (int64_t t = cu_seqlens[i + 1] - 1; t >= cu_seqlens[i]; --t) {
+            const int action = skip_observations ? (mask[t] != 0) : 1;
+            if (!action) {
+                adv[t] = 0.0;
+                continue;
+            }
+            const double delta = (double)rewards[t] + gamma * V_next - (double)values[t];
+            const double A = delta + gamma * lambda * A_next;
+            adv[t] = A;
+            A_next = A;
+            V_next = (double)values[t];
+        }
+    }
+    if (rollout_ids) {
+        for (int64_t s = 0; s < S; ++s) {
+            int64_t later = 0;
+            for (int64_t u = s + 1; u < S && rollout_ids[u] == rollout_ids[s]; ++u)
+                for (int64_t t = cu_seqlens[u]; t < cu_seqlens[u + 1]; ++t) later += mask[t] ? 1 : 0;
+            const double f = pow(gamma * lambda, (double)later);
+            for (int64_t t = cu_seqlens[s]; t < cu_seqlens[s + 1]; ++t) adv[t] *= f;
+        }
+    }
+    return 0;
+}

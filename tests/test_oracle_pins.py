@@ -568,3 +568,60 @@ def test_per_token_advantages_reduce_to_per_response_and_token_norm_invariance()
     assert abs(oracle.forward_backward(split, F64, 9, pt)["loss"] - L) < 1e-15
     ps = LossParams(group_size=1, adv_mode=2, loss_norm=0)
     assert abs(oracle.forward_backward(split, F64, 9, ps)["loss"] - oracle.forward_backward(bt, F64, 9, ps)["loss"]) > 1e-6
+
+
+# ----------------------------------------------------------------------------- GAE
+
+def _gae_case(rng, lengths, obs_frac=0.3):
+    T = sum(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    r = np.where(rng.random(T) < 0.1, rng.normal(0, 1, T), 0.0).astype(np.float32)
+    v = rng.normal(0, 1, T).astype(np.float32)
+    m = (rng.random(T) >= obs_frac).astype(np.uint8)
+    return cu, r, v, m
+
+
+def test_gae_special_cases():
+    rng = np.random.default_rng(30)
+    cu, r, v, m = _gae_case(rng, [7, 1, 12], obs_frac=0.0)
+    # lambda = 1, gamma = 1: Monte-Carlo return minus value
+    a = oracle.gae(cu, r, v, m, 1.0, 1.0)
+    for i in range(3):
+        for t in range(cu[i], cu[i + 1]):
+            assert abs(a[t] - (float(np.sum(r[t:cu[i + 1]], dtype=np.float64)) - float(v[t]))) < 1e-12
+    # lambda = 0: the one-step TD error
+    a0 = oracle.gae(cu, r, v, m, 0.9, 0.0)
+    for i in range(3):
+        for t in range(cu[i], cu[i + 1]):
+            v_next = float(v[t + 1]) if t + 1 < cu[i + 1] else 0.0
+            assert abs(a0[t] - (float(r[t]) + 0.9 * v_next - float(v[t]))) < 1e-12
+
+
+def test_gae_skip_observations_equals_gae_on_the_action_tokens_alone():
+    rng = np.random.default_rng(31)
+    cu, r, v, m = _gae_case(rng, [15, 9, 20])
+    a = oracle.gae(cu, r, v, m, 0.97, 0.9)
+    assert np.all(a[m == 0] == 0.0)
+    keep = m.astype(bool)
+    lens = [int(m[cu[i]:cu[i + 1]].sum()) for i in range(3)]
+    cu2 = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    a2 = oracle.gae(cu2, r[keep], v[keep], np.ones(int(keep.sum()), np.uint8), 0.97, 0.9, skip_observations=False)
+    np.testing.assert_allclose(a[keep], a2, rtol=0, atol=1e-13)
+    # responses are independent: changing one response leaves the others unchanged
+    r3 = r.copy()
+    r3[cu[1]:cu[2]] += 5.0
+    a3 = oracle.gae(cu, r3, v, m, 0.97, 0.9)
+    assert np.array_equal(a3[:cu[1]], a[:cu[1]]) and np.array_equal(a3[cu[2]:], a[cu[2]:])
+
+
+def test_gae_cross_trajectory_discount():
+    rng = np.random.default_rng(32)
+    cu, r, v, m = _gae_case(rng, [6, 5, 8, 4])
+    ro = np.array([7, 7, 7, 9], np.int32)  # responses 0-2 are segments of one rollout
+    gl = 0.95 * 0.9
+    loc = oracle.gae(cu, r, v, m, 0.95, 0.9)
+    a = oracle.gae(cu, r, v, m, 0.95, 0.9, rollout_ids=ro)
+    n = [int(m[cu[i]:cu[i + 1]].sum()) for i in range(4)]
+    later = [n[1] + n[2], n[2], 0, 0]
+    for i in range(4):
+        np.testing.assert_allclose(a[cu[i]:cu[i + 1]], loc[cu[i]:cu[i + 1]] * gl ** later[i], rtol=1e-14)
