@@ -36,7 +36,9 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--case", type=int, default=1, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--case", default="1", choices=["0", "1", "2", "3", "4", "gae", "topk"],
+                    help="0-3: the fused loss over logits; 4: the fused projection + loss; gae: skip-observation "
+                         "GAE; topk: deterministic top-k")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -276,6 +278,11 @@ def workload_config(batch, case_id):
 
 def main():
     args = parse_args()
+    if args.case == "gae":
+        return main_gae(args)
+    if args.case == "topk":
+        return main_topk(args)
+    args.case = int(args.case)
     if args.impl == "reference":
         return run_reference(args)
     if args.case == 4:
@@ -534,6 +541,123 @@ def main_projection(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def _device_setup():
+    import torch
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    from rl_post_loss_gb300 import build as nvbuild
+    if not os.path.exists(nvbuild.LIB_PATH):
+        if rank == 0:
+            nvbuild.build()
+        else:
+            for _ in range(600):
+                if os.path.exists(nvbuild.LIB_PATH):
+                    break
+                time.sleep(1)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def _timed(fn, steps: int, warmup: int, local: int, flush=None):
+    """Device time (ms) of `steps` calls of fn on the current stream, max over ranks."""
+    import torch
+    import torch.distributed as dist
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        if dist.is_initialized():
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(steps):
+            if flush is not None:
+                flush.zero_()
+            fn()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if dist.is_initialized():
+            dist.barrier()
+    return max_over_ranks(start.elapsed_time(stop)), clocks.summary()
+
+
+def main_gae(args):
+    """Skip-observation GAE with the cross-trajectory discount over a CompactionRL-sized batch."""
+    import numpy as np
+    import torch
+    rank, world, local = _device_setup()
+    from rl_post_loss_gb300 import capi, synthetic
+    capi.load()
+    gb = synthetic.make_gae_batch("cuda", seed=rank)
+    T, S = gb.num_tokens, int(gb.cu_seqlens.shape[0]) - 1
+    adv = torch.empty(T, dtype=torch.float32, device="cuda")
+    run = lambda: capi.gae(gb.rewards, gb.values, gb.mask, gb.cu_seqlens, gb.gamma, gb.lam, True,
+                           rollout_ids=gb.rollout_ids, advantages=adv)
+    ms, clocks = _timed(run, args.steps, args.warmup, local)
+    value = replica_throughput(T, args.steps, world, ms)
+    bytes_per_token = 4 + 4 + 1 + 4  # rewards, values, mask in; advantages out
+    peak, kind = measured_peaks()
+    achieved = T * bytes_per_token / (ms / args.steps / 1e3) / 1e9
+    # e2e: host inputs -> device, GAE, advantages -> host
+    host = {k: getattr(gb, k).cpu().pin_memory() for k in ("rewards", "values", "mask", "cu_seqlens", "rollout_ids")}
+    out_host = torch.empty(T, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for k in range(args.e2e_steps + 1):
+        if k == 1:
+            torch.cuda.synchronize()
+            e0.record(stream)
+        for name, t in host.items():
+            getattr(gb, name).copy_(t, non_blocking=True)
+        run()
+        out_host.copy_(adv, non_blocking=True)
+        stream.synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        npb = {k: getattr(gb, k).cpu().numpy() for k in ("rewards", "values", "mask", "cu_seqlens", "rollout_ids")}
+        done, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < args.cpu_seconds:
+            oracle.gae(npb["cu_seqlens"], npb["rewards"], npb["values"], npb["mask"], gb.gamma, gb.lam, True,
+                       npb["rollout_ids"])
+            done += T
+        dt = time.perf_counter() - t0
+        cpu = {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"the whole batch x {done // T}, fp64 sequential recursion, {dt:.1f} s"}
+    if rank == 0:
+        line = {"metric": "response tokens/s, skip-observation GAE with cross-trajectory discount",
+                "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic",
+                "config": {"workload": "gae: " + synthetic.GAE_CASE["name"], "tokens": T, "segments": S,
+                           "gamma": gb.gamma, "lambda": gb.lam, "parallelism": "replicas",
+                           "l2": "no flush: each step reads %.0f MB and writes %.0f MB, more than the 129 MB L2"
+                                 % (T * 9 / 1e6, T * 4 / 1e6)},
+                "roofline": {"bound": "hbm", "kernel": "gae", "achieved": achieved, "peak": peak,
+                             "peak_kind": f"{kind} copy bandwidth", "unit": "GB/s", "frac": achieved / peak,
+                             "traffic": None, "algorithmic_bytes_per_launch": T * bytes_per_token,
+                             "avg_launch_ms": ms / args.steps},
+                "clocks": clocks,
+                "e2e": {"value": replica_throughput(T, 1, world, e2e_ms), "unit": "tokens/s",
+                        "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
+                        "d2h_bytes_per_step": T * 4, "ms_per_step": e2e_ms},
+                "gpu_launches": args.steps, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main_topk(args):
+    raise SystemExit("the top-k workload is not built yet")
 
 
 if __name__ == "__main__":

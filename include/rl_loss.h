@@ -230,6 +230,38 @@ RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(rl_loss_t handle
                                                                 int64_t ld_dhidden, float *dw_lm, int64_t ld_dw,
                                                                 const rl_loss_outputs *outputs, void *stream);
 
+/* ---- Generalized advantage estimation (the step before a critic-based loss) --
+ * "Zhipu AI / GLM: From Blank Infilling to Compaction-Aware Agentic
+ * Reinforcement Learning", section 11: skip-observation GAE of the
+ * single-rollout critic, and CompactionRL's cross-trajectory discount. Per
+ * response, walking backwards over its action (mask=1) tokens t with next
+ * action token t' of the same response:
+ *   A_t = r_t + gamma V_{t'} - V_t + gamma lambda A_{t'}   (V_{t'} = A_{t'} = 0 after the last)
+ * observation (mask=0) tokens are skipped and get A = 0 (with
+ * skip_observations = 0 every token is an action token). With
+ * cross_trajectory, consecutive responses sharing a rollout id are segments
+ * of one rollout and segment s is scaled by (gamma lambda)^{N_{>s}}, N_{>s}
+ * the mask=1 tokens of its later segments. Computed in double as a parallel
+ * scan of affine maps in a fixed tree: bit-identical run to run. The result
+ * feeds RL_ADV_PER_TOKEN. */
+typedef struct rl_gae_config {
+    double gamma;              /* discount, 0 <= gamma <= 1 (not disclosed on the pages: an input); double so
+                                  that (gamma lambda)^N over a long rollout keeps its accuracy */
+    double lambda;             /* GAE lambda, 0 <= lambda <= 1 */
+    int32_t skip_observations; /* 1: mask=0 tokens are skipped; 0: every token is an action token */
+    int32_t cross_trajectory;  /* 1: apply (gamma lambda)^{N_{>s}} over segments (needs rollout_ids) */
+} rl_gae_config;
+
+/* Device pointers: rewards [T], values [T] fp32, mask [T] u8, cu_seqlens
+ * [S+1] i32, rollout_ids [S] i32 (read when cross_trajectory, else may be
+ * NULL); writes advantages [T] fp32 and, if non-NULL, returns [T] = A + V.
+ * `device_status` (optional, device uint32) receives RL_ERR_SEQLENS bits.
+ * Needs no handle and allocates nothing; one launch on `stream`. */
+RL_LOSS_API rl_status rl_gae_advantages(const rl_gae_config *config, int32_t num_tokens, int32_t num_seqs,
+                                        const float *rewards, const float *values, const uint8_t *mask,
+                                        const int32_t *cu_seqlens, const int32_t *rollout_ids, float *advantages,
+                                        float *returns, uint32_t *device_status, void *stream);
+
 /* Synchronises `stream`, returns the accumulated device status bits
  * (1u << code for each rl_status code raised) in *bits and clears them. */
 RL_LOSS_API rl_status rl_loss_get_device_status(rl_loss_t handle, void *stream, uint32_t *bits);

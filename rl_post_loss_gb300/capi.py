@@ -58,6 +58,11 @@ class rl_loss_outputs(ctypes.Structure):
                 ("mean_entropy", ctypes.c_void_p)]
 
 
+class rl_gae_config(ctypes.Structure):
+    _fields_ = [("gamma", ctypes.c_double), ("lambda_", ctypes.c_double), ("skip_observations", ctypes.c_int32),
+                ("cross_trajectory", ctypes.c_int32)]
+
+
 class rl_loss_profile(ctypes.Structure):
     _fields_ = [("num_kernels", ctypes.c_int32), ("names", (ctypes.c_char * 32) * 8),
                 ("launches", ctypes.c_int64 * 8), ("total_ms", ctypes.c_double * 8)]
@@ -90,6 +95,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "rl_loss_forward_backward_noalloc": ([ctypes.POINTER(rl_loss_config), ctypes.POINTER(rl_loss_inputs),
                                               ctypes.POINTER(rl_loss_outputs), P, P], st),
         "rl_loss_projection_setup": ([P, ctypes.c_int32, ctypes.c_int32], st),
+        "rl_gae_advantages": ([ctypes.POINTER(rl_gae_config), ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P, P, P,
+                               P], st),
         "rl_loss_projection_logits": ([P, P, ctypes.c_int64, P, ctypes.c_int64, ctypes.c_int32, P, ctypes.c_int64,
                                        P], st),
         "rl_loss_fused_projection_forward_backward": ([P, P, ctypes.c_int64, P, ctypes.c_int64,
@@ -107,7 +114,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
 def header_functions(path: str = HEADER) -> list[str]:
     """Names of every function the C header declares."""
     text = open(path).read()
-    return sorted(set(re.findall(r"RL_LOSS_API\s+[\w\s\*]+?\b(rl_loss_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"RL_LOSS_API\s+[\w\s\*]+?\b(rl_(?:loss|gae)_\w+)\s*\(", text)))
 
 
 def _check(code: int, what: str):
@@ -186,6 +193,27 @@ def rl_loss_fused_projection_forward_backward(handle, hidden, ld_hidden, w_lm, l
     return load().rl_loss_fused_projection_forward_backward(handle, hidden, ld_hidden, w_lm, ld_w,
                                                             ctypes.byref(inputs), dhidden, ld_dhidden, dw_lm, ld_dw,
                                                             ctypes.byref(outputs), ctypes.c_void_p(stream))
+
+
+def rl_gae_advantages(config: rl_gae_config, num_tokens, num_seqs, rewards, values, mask, cu_seqlens, rollout_ids,
+                      advantages, returns, device_status, stream) -> int:
+    return load().rl_gae_advantages(ctypes.byref(config), num_tokens, num_seqs, rewards, values, mask, cu_seqlens,
+                                    rollout_ids, advantages, returns, device_status, ctypes.c_void_p(stream))
+
+
+def gae(rewards, values, mask, cu_seqlens, gamma: float, lam: float, skip_observations: bool = True,
+        rollout_ids=None, returns=None, advantages=None, device_status=None, stream=None):
+    """Advantages (and optionally returns) on the GPU; torch CUDA tensors in and out."""
+    import torch
+    T, S = int(rewards.shape[0]), int(cu_seqlens.shape[0]) - 1
+    if advantages is None:
+        advantages = torch.empty(T, dtype=torch.float32, device=rewards.device)
+    cfg = rl_gae_config(gamma, lam, int(skip_observations), int(rollout_ids is not None))
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    _check(rl_gae_advantages(cfg, T, S, _ptr(rewards), _ptr(values), _ptr(mask), _ptr(cu_seqlens), _ptr(rollout_ids),
+                             _ptr(advantages), _ptr(returns), _ptr(device_status), stream), "rl_gae_advantages")
+    return advantages
 
 
 def rl_loss_version() -> int:

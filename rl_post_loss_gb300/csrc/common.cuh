@@ -271,6 +271,22 @@ struct ReduceParams {
     uint32_t *status;
 };
 
+struct GaeParams {
+    const int32_t *cu_seqlens;
+    int32_t num_seqs, num_tokens;
+    const float *rewards;      // [T]
+    const float *values;       // [T]
+    const uint8_t *mask;       // [T] 1 = action token
+    double gamma, lambda;
+    int32_t skip_observations;
+    const int32_t *rollout_ids;  // [S] or null (no cross-trajectory discount)
+    float *adv;                // [T]
+    float *returns;            // [T] adv + V, or null
+    uint32_t *status;
+};
+
+cudaError_t launch_gae(const GaeParams &p, cudaStream_t stream);
+
 cudaError_t launch_seg_prep(const SeqPrepParams &p, cudaStream_t stream);
 // RL_NORM_PER_TOKEN: w_i = 1 / sum_j |y_j| (one block, fixed order); after seg_prep.
 cudaError_t launch_seg_token_norm(const SeqPrepParams &p, cudaStream_t stream);

@@ -429,3 +429,32 @@ extern "C" RL_LOSS_API rl_status rl_loss_forward_backward_noalloc(const rl_loss_
         return RL_ERR_CUDA;
     return RL_OK;
 }
+
+extern "C" RL_LOSS_API rl_status rl_gae_advantages(const rl_gae_config *config, int32_t num_tokens, int32_t num_seqs,
+                                                   const float *rewards, const float *values, const uint8_t *mask,
+                                                   const int32_t *cu_seqlens, const int32_t *rollout_ids,
+                                                   float *advantages, float *returns, uint32_t *device_status,
+                                                   void *stream_ptr) {
+    if (!config) return RL_ERR_INVALID_ARG;
+    const rl_gae_config &c = *config;
+    if (!(c.gamma >= 0.0 && c.gamma <= 1.0) || !(c.lambda >= 0.0 && c.lambda <= 1.0)) return RL_ERR_INVALID_ARG;
+    if (num_tokens < 0 || num_seqs < 1) return RL_ERR_SHAPE;
+    if (!cu_seqlens || (num_tokens > 0 && (!rewards || !values || !mask || !advantages))) return RL_ERR_INVALID_ARG;
+    if (c.cross_trajectory && !rollout_ids) return RL_ERR_INVALID_ARG;
+    rlk::GaeParams p{};
+    p.cu_seqlens = cu_seqlens;
+    p.num_seqs = num_seqs;
+    p.num_tokens = num_tokens;
+    p.rewards = rewards;
+    p.values = values;
+    p.mask = mask;
+    p.gamma = c.gamma;
+    p.lambda = c.lambda;
+    p.skip_observations = c.skip_observations ? 1 : 0;
+    p.rollout_ids = c.cross_trajectory ? rollout_ids : nullptr;
+    p.adv = advantages;
+    p.returns = returns;
+    p.status = device_status;  // may be NULL: the bits are then not reported
+    if (rlk::launch_gae(p, reinterpret_cast<cudaStream_t>(stream_ptr)) != cudaSuccess) return RL_ERR_CUDA;
+    return RL_OK;
+}

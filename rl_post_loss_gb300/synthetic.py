@@ -323,3 +323,56 @@ def make_projection_batch(device="cpu", seed: int = 0, chunk_rows: int = 1024, *
               vocab=V, group=case["group"], dtype="bf16", adv_mode=0, beta=case["beta"],
               meta=dict(case=4, name=case["name"], seed=seed, lengths=lengths))
     return ProjBatch(hidden=hidden, w=w, batch=b, chunk=case["chunk"])
+
+
+# ---------------------------------------------------------------------------- GAE inputs
+
+GAE_CASE = dict(name="GAE 128 rollouts x 2 segments x 65536 tokens, 30% observation", rollouts=128, segments=2,
+                length=65536, obs_frac=0.30, gamma=1.0, lam=0.95)
+
+
+@dataclass
+class GaeBatch:
+    """Per-token rewards (a Bernoulli(0.5) outcome on each rollout's last action
+    token, 1% of action tokens with N(0, 0.1) process rewards), critic values
+    N(0, 0.5), observation spans (mask 0) covering obs_frac of every segment,
+    and rollout ids (consecutive segments of one rollout share an id)."""
+    rewards: torch.Tensor
+    values: torch.Tensor
+    mask: torch.Tensor
+    cu_seqlens: torch.Tensor
+    rollout_ids: torch.Tensor
+    gamma: float
+    lam: float
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.rewards.shape[0])
+
+
+def make_gae_batch(device="cpu", seed: int = 0, lengths: list[int] | None = None, **over) -> GaeBatch:
+    case = dict(GAE_CASE)
+    case.update(over)
+    base = 20261202 + 5 + 1000 * seed
+    if lengths is None:
+        lengths = [case["length"]] * (case["rollouts"] * case["segments"])
+    S, T = len(lengths), int(sum(lengths))
+    rng = np.random.default_rng(base * 100 + 7)
+    mask = np.concatenate([span_mask(L, case["obs_frac"], rng) for L in lengths]) if T else np.zeros(0, np.uint8)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    g = _gen("cpu", base, 6)
+    rewards = torch.zeros(T)
+    proc = torch.rand(T, generator=g) < 0.01
+    rewards[proc] = 0.1 * torch.randn(int(proc.sum()), generator=g)
+    seg = case["segments"]
+    rollout_ids = np.arange(S, dtype=np.int32) // max(1, seg)
+    for i in range(S):  # the outcome reward on the last action token of each rollout's last segment
+        if (i + 1) % seg == 0 or i == S - 1:
+            act = np.nonzero(mask[cu[i]:cu[i + 1]])[0]
+            if act.size:
+                rewards[cu[i] + act[-1]] += float(torch.rand(1, generator=g) < 0.5)
+    rewards = rewards * torch.from_numpy(mask).float()
+    values = 0.5 * torch.randn(T, generator=_gen("cpu", base, 1))
+    return GaeBatch(rewards=rewards.to(device), values=values.to(device), mask=torch.from_numpy(mask).to(device),
+                    cu_seqlens=torch.from_numpy(cu).to(device), rollout_ids=torch.from_numpy(rollout_ids).to(device),
+                    gamma=case["gamma"], lam=case["lam"])

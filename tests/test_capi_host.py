@@ -27,7 +27,7 @@ def test_library_exports_every_declared_function(lib):
         assert hasattr(lib, n), n
     out = subprocess.check_output(["nm", "-D", "--defined-only", capi.LIB_PATH]).decode()
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
-    api = {n for n in exported if n.startswith("rl_loss_")}
+    api = {n for n in exported if n.startswith(("rl_loss_", "rl_gae_"))}
     assert api == set(names), (api ^ set(names))
 
 
@@ -42,10 +42,12 @@ int main(void) {
   printf("rl_loss_inputs %zu\n", sizeof(rl_loss_inputs));
   printf("rl_loss_outputs %zu\n", sizeof(rl_loss_outputs));
   printf("rl_loss_profile %zu\n", sizeof(rl_loss_profile));
+  printf("rl_gae_config %zu\n", sizeof(rl_gae_config));
   F(rl_loss_config, logits_dtype) F(rl_loss_config, adv_eps)
   F(rl_loss_inputs, ld_logits) F(rl_loss_inputs, logits) F(rl_loss_inputs, rewards_or_adv)
   F(rl_loss_outputs, ld_dlogits) F(rl_loss_outputs, mean_entropy) F(rl_loss_outputs, counts)
   F(rl_loss_profile, launches) F(rl_loss_profile, total_ms)
+  F(rl_gae_config, skip_observations) F(rl_gae_config, cross_trajectory)
   return 0;
 }
 '''
@@ -56,7 +58,8 @@ int main(void) {
         subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), c, "-o", exe])
         got = dict(line.split() for line in subprocess.check_output([exe]).decode().splitlines())
     sizes = {"rl_loss_config": capi.rl_loss_config, "rl_loss_inputs": capi.rl_loss_inputs,
-             "rl_loss_outputs": capi.rl_loss_outputs, "rl_loss_profile": capi.rl_loss_profile}
+             "rl_loss_outputs": capi.rl_loss_outputs, "rl_loss_profile": capi.rl_loss_profile,
+             "rl_gae_config": capi.rl_gae_config}
     for name, cls in sizes.items():
         assert int(got[name]) == ctypes.sizeof(cls), name
     for key, val in got.items():
