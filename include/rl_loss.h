@@ -241,9 +241,10 @@ RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(rl_loss_t handle
  * skip_observations = 0 every token is an action token). With
  * cross_trajectory, consecutive responses sharing a rollout id are segments
  * of one rollout and segment s is scaled by (gamma lambda)^{N_{>s}}, N_{>s}
- * the mask=1 tokens of its later segments. Computed in double as a parallel
- * scan of affine maps in a fixed tree: bit-identical run to run. The result
- * feeds RL_ADV_PER_TOKEN. */
+ * the mask=1 tokens of its later segments. Computed in fp32 in one pass over
+ * the token arrays: 4096-token chunks, each folded into an affine map, a fixed
+ * tree inside a chunk and a look-back over the chunks to the right in a fixed
+ * order; bit-identical run to run. The result feeds RL_ADV_PER_TOKEN. */
 typedef struct rl_gae_config {
     double gamma;              /* discount, 0 <= gamma <= 1 (not disclosed on the pages: an input); double so
                                   that (gamma lambda)^N over a long rollout keeps its accuracy */
@@ -252,15 +253,32 @@ typedef struct rl_gae_config {
     int32_t cross_trajectory;  /* 1: apply (gamma lambda)^{N_{>s}} over segments (needs rollout_ids) */
 } rl_gae_config;
 
-/* Device pointers: rewards [T], values [T] fp32, mask [T] u8, cu_seqlens
- * [S+1] i32, rollout_ids [S] i32 (read when cross_trajectory, else may be
- * NULL); writes advantages [T] fp32 and, if non-NULL, returns [T] = A + V.
- * `device_status` (optional, device uint32) receives RL_ERR_SEQLENS bits.
- * Needs no handle and allocates nothing; one launch on `stream`. */
+/* Bytes of device workspace rl_gae_advantages needs for num_tokens tokens
+ * (a 256-byte header and a 48-byte slot per 4096-token chunk). */
+RL_LOSS_API size_t rl_gae_workspace_bytes(int32_t num_tokens);
+
+/* Device pointers: rewards [T], values [T] fp32, mask [T] u8 (nonzero =
+ * action token), cu_seqlens [S+1] i32 non-decreasing within [0, T] (tokens
+ * outside [cu_seqlens[0], cu_seqlens[S]) are not written), rollout_ids [S] i32
+ * (read when cross_trajectory, else may be NULL); writes advantages [T] fp32
+ * and, if non-NULL, returns [T] = A + V on action tokens, 0 elsewhere.
+ * rewards, values, advantages and returns must be 4-byte aligned; with every
+ * array 16-byte aligned the kernel uses 16-byte accesses.
+ * `workspace` (device, 256-byte aligned, at least rl_gae_workspace_bytes(T))
+ * is owned by the caller and must be zero-filled before its first use; every
+ * call that completes clears its counters and flags again, so the same
+ * workspace serves the next call of any size; one workspace per stream.
+ * `device_status` (optional, device uint32) receives RL_ERR_SEQLENS and
+ * RL_ERR_TIMEOUT bits (after a timeout, zero the workspace again).
+ * Host-side errors: RL_ERR_INVALID_ARG (NULL pointer, gamma or lambda outside
+ * [0, 1]), RL_ERR_SHAPE (T < 0 or S < 1), RL_ERR_CAPACITY (workspace too
+ * small), RL_ERR_ALIGNMENT. Needs no handle and allocates nothing; one
+ * launch on `stream`. */
 RL_LOSS_API rl_status rl_gae_advantages(const rl_gae_config *config, int32_t num_tokens, int32_t num_seqs,
                                         const float *rewards, const float *values, const uint8_t *mask,
                                         const int32_t *cu_seqlens, const int32_t *rollout_ids, float *advantages,
-                                        float *returns, uint32_t *device_status, void *stream);
+                                        float *returns, void *workspace, size_t workspace_bytes,
+                                        uint32_t *device_status, void *stream);
 
 /* Synchronises `stream`, returns the accumulated device status bits
  * (1u << code for each rl_status code raised) in *bits and clears them. */

@@ -96,7 +96,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                               ctypes.POINTER(rl_loss_outputs), P, P], st),
         "rl_loss_projection_setup": ([P, ctypes.c_int32, ctypes.c_int32], st),
         "rl_gae_advantages": ([ctypes.POINTER(rl_gae_config), ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P, P, P,
-                               P], st),
+                               ctypes.c_size_t, P, P], st),
+        "rl_gae_workspace_bytes": ([ctypes.c_int32], ctypes.c_size_t),
         "rl_loss_projection_logits": ([P, P, ctypes.c_int64, P, ctypes.c_int64, ctypes.c_int32, P, ctypes.c_int64,
                                        P], st),
         "rl_loss_fused_projection_forward_backward": ([P, P, ctypes.c_int64, P, ctypes.c_int64,
@@ -196,23 +197,50 @@ def rl_loss_fused_projection_forward_backward(handle, hidden, ld_hidden, w_lm, l
 
 
 def rl_gae_advantages(config: rl_gae_config, num_tokens, num_seqs, rewards, values, mask, cu_seqlens, rollout_ids,
-                      advantages, returns, device_status, stream) -> int:
+                      advantages, returns, workspace, workspace_bytes, device_status, stream) -> int:
     return load().rl_gae_advantages(ctypes.byref(config), num_tokens, num_seqs, rewards, values, mask, cu_seqlens,
-                                    rollout_ids, advantages, returns, device_status, ctypes.c_void_p(stream))
+                                    rollout_ids, advantages, returns, workspace, workspace_bytes, device_status,
+                                    ctypes.c_void_p(stream))
+
+
+def rl_gae_workspace_bytes(num_tokens: int) -> int:
+    return int(load().rl_gae_workspace_bytes(int(num_tokens)))
+
+
+_GAE_WORKSPACE: dict = {}
+
+
+def gae_workspace(num_tokens: int, device):
+    """A GAE workspace for this device of at least this size, zero-filled when
+    allocated and kept between calls (every completed call clears its counters
+    and flags again)."""
+    import torch
+    dev = torch.device(device)
+    if dev.index is None:
+        dev = torch.device(dev.type, torch.cuda.current_device())
+    need = rl_gae_workspace_bytes(num_tokens)
+    ws = _GAE_WORKSPACE.get(dev)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+        _GAE_WORKSPACE[dev] = ws
+    return ws
 
 
 def gae(rewards, values, mask, cu_seqlens, gamma: float, lam: float, skip_observations: bool = True,
-        rollout_ids=None, returns=None, advantages=None, device_status=None, stream=None):
+        rollout_ids=None, returns=None, advantages=None, device_status=None, stream=None, workspace=None):
     """Advantages (and optionally returns) on the GPU; torch CUDA tensors in and out."""
     import torch
     T, S = int(rewards.shape[0]), int(cu_seqlens.shape[0]) - 1
     if advantages is None:
         advantages = torch.empty(T, dtype=torch.float32, device=rewards.device)
+    if workspace is None:
+        workspace = gae_workspace(T, rewards.device)
     cfg = rl_gae_config(gamma, lam, int(skip_observations), int(rollout_ids is not None))
     if stream is None:
         stream = torch.cuda.current_stream().cuda_stream
     _check(rl_gae_advantages(cfg, T, S, _ptr(rewards), _ptr(values), _ptr(mask), _ptr(cu_seqlens), _ptr(rollout_ids),
-                             _ptr(advantages), _ptr(returns), _ptr(device_status), stream), "rl_gae_advantages")
+                             _ptr(advantages), _ptr(returns), _ptr(workspace), workspace.numel(),
+                             _ptr(device_status), stream), "rl_gae_advantages")
     return advantages
 
 

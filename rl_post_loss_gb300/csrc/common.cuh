@@ -276,16 +276,22 @@ struct GaeParams {
     int32_t num_seqs, num_tokens;
     const float *rewards;      // [T]
     const float *values;       // [T]
-    const uint8_t *mask;       // [T] 1 = action token
-    double gamma, lambda;
+    const uint8_t *mask;       // [T] nonzero = action token
+    float gamma, gl;           // gamma and gamma * lambda, rounded to fp32 once
+    float log2_gl_hi, log2_gl_lo;  // log2(gamma lambda) as an unevaluated fp32 sum
+    double log2_gl;
+    int32_t gl_kind;           // 0: 0 < gamma lambda < 1; 1: gamma lambda == 0; 2: gamma lambda == 1
     int32_t skip_observations;
     const int32_t *rollout_ids;  // [S] or null (no cross-trajectory discount)
     float *adv;                // [T]
     float *returns;            // [T] adv + V, or null
+    void *workspace;           // gae_workspace_bytes(T), zeroed before the first launch
+    int32_t vec;               // set by launch_gae: every array 16-byte aligned
     uint32_t *status;
 };
 
-cudaError_t launch_gae(const GaeParams &p, cudaStream_t stream);
+size_t gae_workspace_bytes(int64_t num_tokens);
+cudaError_t launch_gae(GaeParams p, cudaStream_t stream);
 
 cudaError_t launch_seg_prep(const SeqPrepParams &p, cudaStream_t stream);
 // RL_NORM_PER_TOKEN: w_i = 1 / sum_j |y_j| (one block, fixed order); after seg_prep.

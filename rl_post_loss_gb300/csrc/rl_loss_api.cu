@@ -430,17 +430,28 @@ extern "C" RL_LOSS_API rl_status rl_loss_forward_backward_noalloc(const rl_loss_
     return RL_OK;
 }
 
+extern "C" RL_LOSS_API size_t rl_gae_workspace_bytes(int32_t num_tokens) {
+    return rlk::gae_workspace_bytes(num_tokens < 0 ? 0 : num_tokens);
+}
+
 extern "C" RL_LOSS_API rl_status rl_gae_advantages(const rl_gae_config *config, int32_t num_tokens, int32_t num_seqs,
                                                    const float *rewards, const float *values, const uint8_t *mask,
                                                    const int32_t *cu_seqlens, const int32_t *rollout_ids,
-                                                   float *advantages, float *returns, uint32_t *device_status,
+                                                   float *advantages, float *returns, void *workspace,
+                                                   size_t workspace_bytes, uint32_t *device_status,
                                                    void *stream_ptr) {
     if (!config) return RL_ERR_INVALID_ARG;
     const rl_gae_config &c = *config;
     if (!(c.gamma >= 0.0 && c.gamma <= 1.0) || !(c.lambda >= 0.0 && c.lambda <= 1.0)) return RL_ERR_INVALID_ARG;
     if (num_tokens < 0 || num_seqs < 1) return RL_ERR_SHAPE;
-    if (!cu_seqlens || (num_tokens > 0 && (!rewards || !values || !mask || !advantages))) return RL_ERR_INVALID_ARG;
+    if (!cu_seqlens || (num_tokens > 0 && (!rewards || !values || !mask || !advantages || !workspace)))
+        return RL_ERR_INVALID_ARG;
     if (c.cross_trajectory && !rollout_ids) return RL_ERR_INVALID_ARG;
+    if (num_tokens > 0 && workspace_bytes < rlk::gae_workspace_bytes(num_tokens)) return RL_ERR_CAPACITY;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return RL_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(rewards) | reinterpret_cast<uintptr_t>(values) |
+         reinterpret_cast<uintptr_t>(advantages) | reinterpret_cast<uintptr_t>(returns)) & 3u)
+        return RL_ERR_ALIGNMENT;
     rlk::GaeParams p{};
     p.cu_seqlens = cu_seqlens;
     p.num_seqs = num_seqs;
@@ -448,12 +459,18 @@ extern "C" RL_LOSS_API rl_status rl_gae_advantages(const rl_gae_config *config, 
     p.rewards = rewards;
     p.values = values;
     p.mask = mask;
-    p.gamma = c.gamma;
-    p.lambda = c.lambda;
+    const double gl = c.gamma * c.lambda;
+    p.gamma = (float)c.gamma;
+    p.gl = (float)gl;
+    p.gl_kind = gl == 0.0 ? 1 : (gl == 1.0 ? 2 : 0);
+    p.log2_gl = p.gl_kind == 0 ? std::log2(gl) : 0.0;
+    p.log2_gl_hi = (float)p.log2_gl;
+    p.log2_gl_lo = (float)(p.log2_gl - (double)p.log2_gl_hi);
     p.skip_observations = c.skip_observations ? 1 : 0;
     p.rollout_ids = c.cross_trajectory ? rollout_ids : nullptr;
     p.adv = advantages;
     p.returns = returns;
+    p.workspace = workspace;
     p.status = device_status;  // may be NULL: the bits are then not reported
     if (rlk::launch_gae(p, reinterpret_cast<cudaStream_t>(stream_ptr)) != cudaSuccess) return RL_ERR_CUDA;
     return RL_OK;

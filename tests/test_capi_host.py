@@ -99,3 +99,23 @@ def test_binding_fails_loudly_without_library(tmp_path):
             capi.load(str(tmp_path / "nope.so"))
     finally:
         capi._lib = saved
+
+
+def test_gae_host_side_argument_checks(lib):
+    # every check below returns before any CUDA call; the pointers are never dereferenced
+    cfg = capi.rl_gae_config(1.0, 0.95, 1, 0)
+    fake = ctypes.c_void_p(0x10000)
+    T = 10000
+    need = capi.rl_gae_workspace_bytes(T)
+    assert need >= 256 + 3 * 32
+    args = lambda ws, nbytes: (ctypes.byref(cfg), T, 4, fake, fake, fake, fake, None, fake, None, ws, nbytes, None,
+                               None)
+    assert lib.rl_gae_advantages(*args(fake, need - 1)) == capi.CODES["RL_ERR_CAPACITY"]
+    assert lib.rl_gae_advantages(*args(ctypes.c_void_p(0x10010), need)) == capi.CODES["RL_ERR_ALIGNMENT"]
+    assert lib.rl_gae_advantages(*args(None, need)) == capi.CODES["RL_ERR_INVALID_ARG"]
+    bad = capi.rl_gae_config(1.5, 0.95, 1, 0)
+    assert lib.rl_gae_advantages(ctypes.byref(bad), T, 4, fake, fake, fake, fake, None, fake, None, fake, need, None,
+                                 None) == capi.CODES["RL_ERR_INVALID_ARG"]
+    cross = capi.rl_gae_config(1.0, 0.95, 1, 1)
+    assert lib.rl_gae_advantages(ctypes.byref(cross), T, 4, fake, fake, fake, fake, None, fake, None, fake, need, None,
+                                 None) == capi.CODES["RL_ERR_INVALID_ARG"]

@@ -4,16 +4,21 @@ determinism.
 
 Tolerance, derived from the kernel's fp32 arithmetic. Every action token's
 advantage is a weighted sum A_t = sum_k x^k delta_{t+k} (x = gamma lambda, k
-counting action tokens), evaluated by the kernel through per-thread folds, a
-fixed-tree scan and a per-thread re-walk, with the carry between tiles held in
-double. Each term passes through at most about 64 fp32 roundings in any one
-tile (fewer than 41 more per tile boundary crossed), and the weight x^k is a
-product of k rounded factors, so
-  |err_t| <= u (128 S0_t + 2 S1_t) + 2 u |A_t|,
+counting action tokens), evaluated by the kernel through per-thread folds of 16
+tokens, a fixed tree over the 256 threads of a 4096-token chunk, a look-back
+tree over the chunks to the right, and a per-thread re-walk. A composition adds
+at most 3 roundings to a term, so a term passes through at most about 120 fp32
+roundings (fold 17, the chunk's tree 24, the look-back tree 15 plus 3 for every
+further 32 chunks, the exclusive tree 27, the re-walk 32), and the weight x^k
+is a product of k rounded factors, so
+  |err_t| <= u (256 S0_t + 2 S1_t) + 2 u |A_t|,
   S0_t = sum_k x^k M_{t+k},  S1_t = sum_k k x^k M_{t+k},
   M_j = |r_j| + |V_j| + gamma |V_next(j)|,  u = 2^-24,
-with S1 dropped when fl32(x) is 0 or 1 (the products are then exact); the
-cross-trajectory factor scales the bound and adds one rounding.
+with S1 dropped when fl32(x) is 0 or 1 (the products are then exact). The
+cross-trajectory factor (gamma lambda)^N, evaluated as 2^(N log2 x) with a
+degree-7 Taylor series for the fractional power, is within 3u of exact: it
+scales the bound, adds 4 u |A_t| and one rounding of the product, and 2^-147
+absolute for products below the normal range.
 """
 import numpy as np
 import pytest
@@ -93,12 +98,15 @@ def gae_error_bound(gb, ref, act, gamma, lam, cross):
         vn = np.append(v[idx[1:]], 0.0)
         M = r[idx] + v[idx] + gamma * vn
         s0 = _reverse_geometric(x, M)
-        b = 128.0 * s0
+        b = 256.0 * s0
         if not exact_powers:
             z = np.append(x * s0[1:], 0.0)
             b = b + 2.0 * _reverse_geometric(x, z)
         a_unscaled = np.abs(ref[idx]) / np.where(scale[idx] > 0, scale[idx], 1.0)
-        bound[idx] = U32 * (b + 2.0 * a_unscaled) * scale[idx] + U32 * np.abs(ref[idx])
+        extra = 4.0 if cross else 0.0
+        bound[idx] = U32 * (b + (2.0 + extra) * a_unscaled) * scale[idx] + U32 * np.abs(ref[idx])
+        if cross:
+            bound[idx] += 2.0 ** -147
     return bound * 1.0001 + 1e-30
 
 
@@ -107,6 +115,15 @@ def gae_error_bound(gb, ref, act, gamma, lam, cross):
 def test_gae_layouts(lengths, skip, cross):
     gb = synthetic.make_gae_batch("cuda", lengths=lengths, segments=2)
     _check(gb, skip=skip, cross=cross)
+
+
+@pytest.mark.parametrize("lengths,segments", [([9000, 8000, 20000, 12000], 2), ([5000, 7000, 300, 9000, 4100, 1], 3),
+                                               ([70000, 3000, 40000, 1, 5000], 5)])
+def test_gae_cross_trajectory_discount_without_underflow(lengths, segments):
+    # gamma lambda close to 1: (gamma lambda)^N stays well inside the fp32 range over whole segments
+    gb = synthetic.make_gae_batch("cuda", lengths=lengths, segments=segments)
+    adv = _check(gb, cross=True, gamma=1.0, lam=0.9999)
+    assert float(adv.abs().min()) >= 0.0 and int((adv != 0).sum()) > 0.5 * int(gb.mask.sum())
 
 
 @pytest.mark.parametrize("gamma,lam", [(1.0, 1.0), (1.0, 0.0), (0.99, 0.95), (0.0, 0.5)])
@@ -135,3 +152,88 @@ def test_gae_full_size_and_bit_identical():
     a2 = capi.gae(gb.rewards, gb.values, gb.mask, gb.cu_seqlens, gb.gamma, gb.lam, True, rollout_ids=gb.rollout_ids)
     torch.cuda.synchronize()
     assert torch.equal(a1.view(torch.int32), a2.view(torch.int32))
+
+
+def _workspace_is_clear(T):
+    """The ticket and done counters and every chunk's flag are zero again."""
+    ws = capi.gae_workspace(T, torch.device("cuda", torch.cuda.current_device()))
+    torch.cuda.synchronize()
+    assert ws.data_ptr() == capi.gae_workspace(T, "cuda").data_ptr()
+    words = ws.view(torch.int32).cpu().numpy()
+    slots = (words.size * 4 - 256) // 48
+    flags = words[(256 + 32) // 4::12][:slots]
+    return bool(np.all(words[:2] == 0)) and bool(np.all(flags == 0))
+
+
+def test_gae_long_responses_span_many_chunks():
+    # 150000 tokens = 37 chunks: the look-back composes more than one window of 32 chunks
+    gb = synthetic.make_gae_batch("cuda", lengths=[150000, 3, 140000, 70000], segments=2)
+    _check(gb, cross=True)
+    _check(gb, skip=False)
+    assert _workspace_is_clear(gb.num_tokens)
+
+
+def test_gae_empty_responses_and_rollout_breaks():
+    lengths = [0, 500, 0, 0, 4100, 0, 7, 0, 9000, 1]
+    gb = synthetic.make_gae_batch("cuda", lengths=lengths, segments=3)
+    # an empty response with another rollout id between two segments of rollout 0 ends that rollout
+    gb.rollout_ids.copy_(torch.tensor([0, 0, 1, 0, 0, 0, 2, 2, 2, 3], dtype=torch.int32))
+    _check(gb, cross=True)
+    _check(gb, cross=False)
+
+
+def test_gae_unaligned_arrays_take_the_scalar_path():
+    base = synthetic.make_gae_batch("cuda", lengths=[3000, 5000, 1234, 4096], segments=2)
+    T = base.num_tokens
+
+    def shifted(t):
+        buf = torch.zeros(T + 1, dtype=t.dtype, device=t.device)
+        buf[1:] = t
+        return buf[1:]
+
+    gb = synthetic.GaeBatch(rewards=shifted(base.rewards), values=shifted(base.values), mask=shifted(base.mask),
+                            cu_seqlens=base.cu_seqlens, rollout_ids=base.rollout_ids, gamma=base.gamma, lam=base.lam)
+    assert gb.rewards.data_ptr() % 16 != 0 and gb.mask.data_ptr() % 16 != 0
+    a_scalar = _check(gb, cross=True)
+    a_vec = _check(base, cross=True)
+    assert torch.equal(a_scalar.view(torch.int32), a_vec.view(torch.int32))
+
+
+def test_gae_tokens_outside_the_responses_are_not_written():
+    lengths = [5000, 0, 3100]
+    gb = synthetic.make_gae_batch("cuda", lengths=lengths, segments=1)
+    pad_l, pad_r = 100, 4200
+    T = gb.num_tokens + pad_l + pad_r
+
+    def padded(t):
+        buf = torch.zeros(T, dtype=t.dtype, device=t.device)
+        buf[pad_l:pad_l + t.numel()] = t
+        return buf
+
+    r, v, m = padded(gb.rewards), padded(gb.values), padded(gb.mask)
+    m[:pad_l] = 1
+    m[pad_l + gb.num_tokens:] = 1
+    cu = gb.cu_seqlens + pad_l
+    adv = torch.full((T,), 7.0, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    capi.gae(r, v, m, cu, gb.gamma, gb.lam, True, advantages=adv, device_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    got = adv.cpu().numpy()
+    assert np.all(got[:pad_l] == 7.0) and np.all(got[pad_l + gb.num_tokens:] == 7.0)
+    ref = oracle.gae(cu.cpu().numpy(), r.cpu().numpy(), v.cpu().numpy(), m.cpu().numpy(), gb.gamma, gb.lam, True)
+    inner = slice(pad_l, pad_l + gb.num_tokens)
+    bound = gae_error_bound(gb, ref[inner], gb.mask.cpu().numpy().astype(bool), gb.gamma, gb.lam, False)
+    assert np.all(np.abs(got[inner] - ref[inner]) <= bound)
+
+
+def test_gae_repeated_calls_are_bit_identical_and_leave_the_workspace_clear():
+    gb = synthetic.make_gae_batch("cuda", lengths=[20000, 7, 65536, 300, 12000] * 4, segments=2)
+    outs = []
+    for _ in range(4):
+        outs.append(capi.gae(gb.rewards, gb.values, gb.mask, gb.cu_seqlens, gb.gamma, gb.lam, True,
+                             rollout_ids=gb.rollout_ids))
+        torch.cuda.synchronize()
+        assert _workspace_is_clear(gb.num_tokens)
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
