@@ -376,3 +376,55 @@ def make_gae_batch(device="cpu", seed: int = 0, lengths: list[int] | None = None
     return GaeBatch(rewards=rewards.to(device), values=values.to(device), mask=torch.from_numpy(mask).to(device),
                     cu_seqlens=torch.from_numpy(cu).to(device), rollout_ids=torch.from_numpy(rollout_ids).to(device),
                     gamma=case["gamma"], lam=case["lam"])
+
+
+# ------------------------------------------------------------------ DSA indexer scores for top-k
+
+TOPK_CASE = dict(name="DSA indexer top-k: last 4096 query positions of a 202,752-token context, k=2048",
+                 rows=4096, context=202752, k=2048)
+TOPK_SMALL = dict(name="DSA indexer top-k, small: 48 query positions of a 20,000-token context", rows=48,
+                  context=20000, k=2048)
+_INDEXER_HEAD_WEIGHTS = (1.0, 0.8, 0.6, 0.4)
+
+
+@dataclass
+class TopkBatch:
+    """Indexer-like scores: sum over 4 heads of w_h * relu(N(0,1)), rounded to
+    bf16 precision (the indexer runs in low precision, so scores tie often) and
+    stored as fp32 [rows, ld]; row q is causal and holds lengths[q] = context -
+    rows + 1 + q valid keys (the rest of the row is filled but not part of it)."""
+    scores: torch.Tensor
+    lengths: torch.Tensor
+    k: int
+
+    @property
+    def rows(self) -> int:
+        return int(self.scores.shape[0])
+
+    @property
+    def ld(self) -> int:
+        return int(self.scores.shape[1])
+
+
+def topk_ld(context: int) -> int:
+    """Row stride: the context rounded up to a multiple of 32 keys."""
+    return (context + 31) // 32 * 32
+
+
+def make_topk_batch(device="cpu", seed: int = 0, **over) -> TopkBatch:
+    case = dict(TOPK_CASE)
+    case.update(over)
+    rows, context = int(case["rows"]), int(case["context"])
+    base = 20261202 + 7 + 1000 * seed
+    ld = topk_ld(context)
+    g = _gen(device, base, 1)
+    scores = torch.empty((rows, ld), dtype=torch.float32, device=device)
+    block = max(1, (1 << 26) // max(ld, 1))
+    for r0 in range(0, rows, block):
+        r1 = min(rows, r0 + block)
+        acc = torch.zeros((r1 - r0, ld), dtype=torch.float32, device=device)
+        for w in _INDEXER_HEAD_WEIGHTS:
+            acc += w * torch.relu(torch.randn((r1 - r0, ld), generator=g, device=device))
+        scores[r0:r1] = acc.to(torch.bfloat16).to(torch.float32)
+    lengths = torch.arange(rows, dtype=torch.int32, device=device) + (context - rows + 1)
+    return TopkBatch(scores=scores, lengths=lengths, k=int(case["k"]))
