@@ -592,6 +592,25 @@ def main_gae(args):
     """Skip-observation GAE with the cross-trajectory discount over a CompactionRL-sized batch."""
     import numpy as np
     import torch
+    if args.impl == "reference":
+        from rl_post_loss_gb300 import synthetic
+        rank, world, local = dist_env()
+        if rank != 0:
+            return 0
+        gb = synthetic.make_gae_batch("cpu")
+        per_step = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+        rates = []
+        desc, cores = "", 1
+        for i in range(args.warmup + args.steps):
+            rate, cores, desc = _gae_oracle_rate(gb, per_step)
+            if i >= args.warmup:
+                rates.append(rate)
+        config = {"workload": "gae: " + synthetic.GAE_CASE["name"], "tokens": gb.num_tokens,
+                  "segments": int(gb.cu_seqlens.shape[0]) - 1, "gamma": gb.gamma, "lambda": gb.lam,
+                  "parallelism": "replicas"}
+        print(json.dumps(_reference_line(GAE_METRIC, "tokens/s", statistics.mean(rates), desc, cores, config, args,
+                                         world, gb.num_tokens)), flush=True)
+        return 0
     rank, world, local = _device_setup()
     from rl_post_loss_gb300 import capi, synthetic
     capi.load()
@@ -624,18 +643,10 @@ def main_gae(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import oracle
-        npb = {k: getattr(gb, k).cpu().numpy() for k in ("rewards", "values", "mask", "cu_seqlens", "rollout_ids")}
-        done, t0 = 0, time.perf_counter()
-        while time.perf_counter() - t0 < args.cpu_seconds:
-            oracle.gae(npb["cu_seqlens"], npb["rewards"], npb["values"], npb["mask"], gb.gamma, gb.lam, True,
-                       npb["rollout_ids"])
-            done += T
-        dt = time.perf_counter() - t0
-        cpu = {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"the whole batch x {done // T}, fp64 sequential recursion, {dt:.1f} s"}
+        rate, cores, desc = _gae_oracle_rate(gb, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
     if rank == 0:
-        line = {"metric": "response tokens/s, skip-observation GAE with cross-trajectory discount",
+        line = {"metric": GAE_METRIC,
                 "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f32", "data": "synthetic",
@@ -656,8 +667,124 @@ def main_gae(args):
     return 0
 
 
+def _gae_oracle_rate(gb, seconds: float):
+    """The oracle's GAE (sequential fp64 recursion, one core) on the whole batch, repeated."""
+    import oracle
+    npb = {k: getattr(gb, k).cpu().numpy() for k in ("rewards", "values", "mask", "cu_seqlens", "rollout_ids")}
+    done, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds or done == 0:
+        oracle.gae(npb["cu_seqlens"], npb["rewards"], npb["values"], npb["mask"], gb.gamma, gb.lam, True,
+                   npb["rollout_ids"])
+        done += gb.num_tokens
+    dt = time.perf_counter() - t0
+    return done / dt, 1, f"the whole batch x {done // gb.num_tokens}, fp64 sequential recursion, {dt:.1f} s"
+
+
+def _topk_oracle_rate(b, seconds: float):
+    """The oracle's top-k (a stable sort per row, one core) on evenly spaced rows, repeated."""
+    import numpy as np
+    from oracle import topk as otopk
+    s = b.scores.cpu().numpy() if b.scores.device.type == "cpu" else None
+    lengths = b.lengths.cpu().numpy()
+    rows = np.linspace(0, b.rows - 1, 16).astype(int)
+    host_rows = {int(q): (s[q] if s is not None else b.scores[q].cpu().numpy())[:int(lengths[q])] for q in rows}
+    done, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds or done == 0:
+        for q in rows:
+            otopk.topk_row(host_rows[int(q)], b.k)
+            done += 1
+    dt = time.perf_counter() - t0
+    return done / dt, 1, f"{done} rows ({len(rows)} evenly spaced rows, repeated), stable sort per row, {dt:.1f} s"
+
+
+def _reference_line(metric, unit, value, desc, cores, config, args, world, per_step_units):
+    return {"metric": metric, "value": value, "unit": unit, "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per_step_units / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config,
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+TOPK_METRIC = "query rows/s, deterministic DSA-indexer top-k (k=2048)"
+GAE_METRIC = "response tokens/s, skip-observation GAE with cross-trajectory discount"
+
+
 def main_topk(args):
-    raise SystemExit("the top-k workload is not built yet")
+    """Deterministic top-k (k = 2048) over DSA indexer scores of a 202,752-token context."""
+    import torch
+    from rl_post_loss_gb300 import synthetic
+    rank, world, local = dist_env() if args.impl == "reference" else _device_setup()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        b = synthetic.make_topk_batch("cuda" if torch.cuda.is_available() else "cpu")
+        per_step = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+        rates = []
+        desc, cores = "", 1
+        for i in range(args.warmup + args.steps):
+            rate, cores, desc = _topk_oracle_rate(b, per_step)
+            if i >= args.warmup:
+                rates.append(rate)
+        print(json.dumps(_reference_line(TOPK_METRIC, "rows/s", statistics.mean(rates), desc, cores,
+                                         _topk_config(b), args, world, b.rows)), flush=True)
+        return 0
+    from rl_post_loss_gb300 import capi
+    capi.load()
+    b = synthetic.make_topk_batch("cuda", seed=rank)
+    out_idx = torch.empty((b.rows, b.k), dtype=torch.int32, device="cuda")
+    out_val = torch.empty((b.rows, b.k), dtype=torch.float32, device="cuda")
+    run = lambda: capi.topk(b.scores, b.k, lengths=b.lengths, out_idx=out_idx, out_val=out_val)
+    ms, clocks = _timed(run, args.steps, args.warmup, local)
+    value = replica_throughput(b.rows, args.steps, world, ms)
+    n_sum = int(b.lengths.sum().item())
+    bytes_per_launch = 4 * n_sum + 4 * b.rows + 8 * b.rows * b.k  # scores read, lengths, positions + scores written
+    peak, kind = measured_peaks()
+    achieved = bytes_per_launch / (ms / args.steps / 1e3) / 1e9
+    # e2e: pinned host scores -> device, top-k, positions -> host
+    host = b.scores.cpu().pin_memory()
+    idx_host = torch.empty((b.rows, b.k), dtype=torch.int32).pin_memory()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.e2e_steps + 1):
+        if i == 1:
+            torch.cuda.synchronize()
+            e0.record(stream)
+        b.scores.copy_(host, non_blocking=True)
+        run()
+        idx_host.copy_(out_idx, non_blocking=True)
+        stream.synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, cores, desc = _topk_oracle_rate(b, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "rows/s", "cores": cores, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        line = {"metric": TOPK_METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": _topk_config(b),
+                "roofline": {"bound": "hbm", "kernel": "topk", "achieved": achieved, "peak": peak,
+                             "peak_kind": f"{kind} copy bandwidth", "unit": "GB/s", "frac": achieved / peak,
+                             "traffic": None, "algorithmic_bytes_per_launch": bytes_per_launch,
+                             "avg_launch_ms": ms / args.steps},
+                "clocks": clocks,
+                "e2e": {"value": replica_throughput(b.rows, 1, world, e2e_ms), "unit": "rows/s",
+                        "h2d_bytes_per_step": host.numel() * 4, "d2h_bytes_per_step": b.rows * b.k * 4,
+                        "ms_per_step": e2e_ms},
+                "gpu_launches": args.steps, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def _topk_config(b):
+    from rl_post_loss_gb300 import synthetic
+    return {"workload": "topk: " + synthetic.TOPK_CASE["name"], "rows": b.rows, "ld": b.ld, "k": b.k,
+            "keys_per_launch": int(b.lengths.sum().item()), "order": "score desc, position asc",
+            "parallelism": "replicas",
+            "l2": "no flush: each step reads %.2f GB of scores, more than the 129 MB L2" % (
+                4 * int(b.lengths.sum().item()) / 1e9)}
 
 
 if __name__ == "__main__":

@@ -280,6 +280,43 @@ RL_LOSS_API rl_status rl_gae_advantages(const rl_gae_config *config, int32_t num
                                         float *returns, void *workspace, size_t workspace_bytes,
                                         uint32_t *device_status, void *stream);
 
+/* ---- Deterministic top-k over DSA indexer scores ----------------------
+ * "GLM-5: from Vibe Coding to Agentic Engineering", section 3.2 ("DSA RL
+ * insights"): the DSA indexer keeps the k = 2048 best-scoring key positions of
+ * every query, and the top-k used in RL must be deterministic (a
+ * non-deterministic CUDA top-k collapsed RL; torch.topk was used instead).
+ * Selection: the first k positions of a row under one total order: NaN above
+ * every number, then larger score, then lower position; -0 and +0 tie. The
+ * result (set and order) is unique and bit-identical from run to run. One
+ * read of each row from HBM (a CTA per row streams it through a shared-memory
+ * candidate buffer with a rising lower bound). */
+typedef enum rl_topk_order {
+    RL_TOPK_BY_SCORE = 0,    /* (score desc, position asc): what a sorted torch.topk returns, ties fixed */
+    RL_TOPK_BY_POSITION = 1  /* the same set by increasing position */
+} rl_topk_order;
+
+typedef struct rl_topk_config {
+    int32_t k;      /* 1 <= k <= rl_topk_max_k() */
+    int32_t order;  /* rl_topk_order */
+} rl_topk_config;
+
+/* Largest k this build supports (4096). */
+RL_LOSS_API int32_t rl_topk_max_k(void);
+
+/* Device pointers: scores [rows x ld] fp32, row-major, 16-byte aligned with
+ * ld % 4 == 0; lengths [rows] i32 (row q's valid scores are its first
+ * lengths[q], 0 <= lengths[q] <= ld; NULL: all ld); writes out_idx [rows x ldo]
+ * i32 positions and, if non-NULL, out_val [rows x ldo] fp32 (the scores
+ * themselves, bit for bit). When lengths[q] < k the missing entries are -1 and
+ * -inf. `device_status` (optional, device uint32) receives RL_ERR_SEQLENS for
+ * a length outside [0, ld] (clamped). Host-side errors: RL_ERR_INVALID_ARG
+ * (NULL pointer, bad order), RL_ERR_SHAPE (rows < 0, ld < 1, ldo < k),
+ * RL_ERR_UNSUPPORTED (k outside [1, rl_topk_max_k()]), RL_ERR_ALIGNMENT.
+ * Needs no handle and allocates nothing; one launch on `stream`. */
+RL_LOSS_API rl_status rl_topk(const rl_topk_config *config, int32_t rows, const float *scores, int64_t ld,
+                              const int32_t *lengths, int32_t *out_idx, float *out_val, int64_t ldo,
+                              uint32_t *device_status, void *stream);
+
 /* Synchronises `stream`, returns the accumulated device status bits
  * (1u << code for each rl_status code raised) in *bits and clears them. */
 RL_LOSS_API rl_status rl_loss_get_device_status(rl_loss_t handle, void *stream, uint32_t *bits);

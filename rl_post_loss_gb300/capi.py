@@ -63,6 +63,13 @@ class rl_gae_config(ctypes.Structure):
                 ("cross_trajectory", ctypes.c_int32)]
 
 
+class rl_topk_config(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_int32), ("order", ctypes.c_int32)]
+
+
+RL_TOPK_BY_SCORE, RL_TOPK_BY_POSITION = 0, 1
+
+
 class rl_loss_profile(ctypes.Structure):
     _fields_ = [("num_kernels", ctypes.c_int32), ("names", (ctypes.c_char * 32) * 8),
                 ("launches", ctypes.c_int64 * 8), ("total_ms", ctypes.c_double * 8)]
@@ -98,6 +105,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "rl_gae_advantages": ([ctypes.POINTER(rl_gae_config), ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P, P, P,
                                ctypes.c_size_t, P, P], st),
         "rl_gae_workspace_bytes": ([ctypes.c_int32], ctypes.c_size_t),
+        "rl_topk_max_k": ([], ctypes.c_int32),
+        "rl_topk": ([ctypes.POINTER(rl_topk_config), ctypes.c_int32, P, ctypes.c_int64, P, P, P, ctypes.c_int64, P, P],
+                    st),
         "rl_loss_projection_logits": ([P, P, ctypes.c_int64, P, ctypes.c_int64, ctypes.c_int32, P, ctypes.c_int64,
                                        P], st),
         "rl_loss_fused_projection_forward_backward": ([P, P, ctypes.c_int64, P, ctypes.c_int64,
@@ -115,7 +125,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
 def header_functions(path: str = HEADER) -> list[str]:
     """Names of every function the C header declares."""
     text = open(path).read()
-    return sorted(set(re.findall(r"RL_LOSS_API\s+[\w\s\*]+?\b(rl_(?:loss|gae)_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"RL_LOSS_API\s+[\w\s\*]+?\b(rl_(?:loss_|gae_|topk)\w*)\s*\(", text)))
 
 
 def _check(code: int, what: str):
@@ -242,6 +252,32 @@ def gae(rewards, values, mask, cu_seqlens, gamma: float, lam: float, skip_observ
                              _ptr(advantages), _ptr(returns), _ptr(workspace), workspace.numel(),
                              _ptr(device_status), stream), "rl_gae_advantages")
     return advantages
+
+
+def rl_topk_max_k() -> int:
+    return int(load().rl_topk_max_k())
+
+
+def topk(scores, k: int, lengths=None, order: str = "score", out_idx=None, out_val=None, want_values=True,
+         device_status=None, stream=None):
+    """Row-wise deterministic top-k on the GPU; torch CUDA tensors in and out. Returns (positions, scores)."""
+    import torch
+    if order not in ("score", "index"):
+        raise ValueError("order is 'score' or 'index'")
+    rows, ld = int(scores.shape[0]), int(scores.shape[1])
+    if scores.stride(1) != 1:
+        raise ValueError("scores rows must be contiguous")
+    if out_idx is None:
+        out_idx = torch.empty((rows, k), dtype=torch.int32, device=scores.device)
+    if out_val is None and want_values:
+        out_val = torch.empty((rows, k), dtype=torch.float32, device=scores.device)
+    cfg = rl_topk_config(k, RL_TOPK_BY_SCORE if order == "score" else RL_TOPK_BY_POSITION)
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    _check(load().rl_topk(ctypes.byref(cfg), rows, _ptr(scores), int(scores.stride(0)), _ptr(lengths), _ptr(out_idx),
+                          _ptr(out_val), int(out_idx.stride(0)), _ptr(device_status), ctypes.c_void_p(stream)),
+           "rl_topk")
+    return out_idx, out_val
 
 
 def rl_loss_version() -> int:

@@ -290,6 +290,22 @@ struct GaeParams {
     uint32_t *status;
 };
 
+// Row-wise deterministic top-k (see topk.cu).
+struct TopkParams {
+    const float *scores;     // [rows x ld], 16-byte aligned, ld % 4 == 0
+    int64_t ld;
+    const int32_t *lengths;  // [rows] valid scores per row, or null (all ld)
+    int32_t rows, k;
+    int32_t order_by_score;  // 1: (score desc, position asc); 0: position asc
+    int32_t *out_idx;        // [rows x ldo]
+    float *out_val;          // [rows x ldo] or null
+    int64_t ldo;
+    uint32_t *status;        // optional
+};
+
+int topk_max_k();
+cudaError_t launch_topk(const TopkParams &p, cudaStream_t stream);
+
 size_t gae_workspace_bytes(int64_t num_tokens);
 cudaError_t launch_gae(GaeParams p, cudaStream_t stream);
 

@@ -12,28 +12,29 @@
 // multiplied by (gamma lambda)^{N_{>s}}, N_{>s} the mask=1 tokens of the later
 // segments of the same rollout.
 //
-// Design. The token range is cut into fixed chunks of 4096 tokens; one block
+// Design. The token range is cut into fixed chunks of 8192 tokens; one block
 // per chunk, chunks handed out right to left by an atomic ticket. What a run
 // of tokens does to the state (A, V) arriving from its right is affine,
 //   A <- p A + q V + c,   V <- V (no action token, no response end) or vf,
-// and a response end resets the state to zero; two integer counts ride along
-// (mask=1 tokens to the right within the response and within the rollout),
-// from which N_{>s} is their difference. Such maps compose associatively.
-// A block folds its 16 tokens per thread into a map (fp32), scans the 256
-// maps of the block with a fixed tree, publishes the chunk's map, and then
-// looks back: it composes the published maps of the chunks to its right, in
-// a fixed order and tree, up to and including the first one that holds a
-// response end (the state further right cannot reach it). The rollout count
-// (an integer, so any order gives the same sum) uses the classic decoupled
-// look-back with inclusive values. Every floating-point result depends only on
-// the inputs, never on timing: bit-identical from run to run.
-// Waits on another chunk's record are bounded (1 s of %globaltimer); a wait
-// that runs out raises RL_ERR_TIMEOUT and treats that chunk as a response end.
-// The last block to finish its look-back clears the flags and the ticket (the
-// records themselves are only read under a flag set by the same launch), so
-// the workspace is ready for the next launch. The chunk is staged in
-// shared memory by coalesced 16-byte asynchronous copies, so that no token
-// value occupies a register across the scan and the look-back.
+// and a response end resets the state to zero; with the cross-trajectory
+// discount two integer counts ride along (mask=1 tokens to the right within
+// the response and within the rollout), whose difference is N_{>s}. Such maps
+// compose associatively. A block stages its chunk in shared memory with
+// coalesced 16-byte asynchronous copies, folds 32 tokens per thread into a map
+// (fp32), scans the 256 maps with a fixed tree and publishes the chunk's map.
+// Warp 0 then looks back: it composes the published maps of the chunks to its
+// right, in a fixed order and tree, up to and including the first one that
+// holds a response end (the state further right cannot reach it); the rollout
+// count (an integer, so any order gives the same sum) uses the classic
+// decoupled look-back with inclusive values. It waits only for the chunks up
+// to those stopping points. Every floating-point result depends only on the
+// inputs, never on timing: bit-identical from run to run. Waits are bounded
+// (1 s of %globaltimer); one that runs out raises RL_ERR_TIMEOUT and treats
+// the chunk as a response end. The last block past its look-back clears the
+// flags and the ticket (records are only read under a flag set by the same
+// launch), so the workspace is ready for the next launch.
+#include <atomic>
+
 #include "common.cuh"
 
 namespace rlk {
@@ -41,11 +42,18 @@ namespace rlk {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTok = 16;                 // consecutive tokens per thread
+constexpr int kTok = 32;                 // consecutive tokens per thread
 constexpr int kChunk = kThreads * kTok;  // tokens per chunk
-constexpr int kWords = kChunk / 32;
+constexpr int kVec = kTok / 4;           // float4 groups per thread
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kWaitNs = 1000000000ull;
+// Dynamic shared memory: rewards and values (one 128-byte row per thread,
+// its eight 16-byte groups XOR-swizzled by the row index so that the 16-byte
+// reads of a quarter warp hit distinct banks), then the mask bytes.
+constexpr int kSmemR = 0;
+constexpr int kSmemV = kChunk * 4;
+constexpr int kSmemM = 2 * kChunk * 4;
+constexpr int kSmemBytes = 2 * kChunk * 4 + kChunk;
 
 // GaeMap::bits
 constexpr uint32_t kPassV = 1;     // no action token and no response end: V passes
@@ -86,7 +94,8 @@ __device__ __forceinline__ GaeMap map_identity() { return GaeMap{1.f, 0.f, 0.f, 
 // the zero state beyond the last chunk
 __device__ __forceinline__ GaeMap map_zero() { return GaeMap{0.f, 0.f, 0.f, 0.f, kClosed, 0, 0}; }
 
-// F o G: G (the tokens to the right) acts first.
+// F o G: G (the tokens to the right) acts first. kC: carry the two counts.
+template <bool kC>
 __device__ __forceinline__ GaeMap compose(const GaeMap &F, const GaeMap &G) {
     GaeMap r;
     r.p = F.p * G.p;
@@ -94,11 +103,12 @@ __device__ __forceinline__ GaeMap compose(const GaeMap &F, const GaeMap &G) {
     r.c = fmaf(F.q, G.vf, fmaf(F.p, G.c, F.c));
     r.vf = (F.bits & kPassV) ? G.vf : F.vf;
     r.bits = (F.bits & G.bits & (kPassV | kPassRoll)) | ((F.bits | G.bits) & kClosed);
-    r.n_resp = F.n_resp + ((F.bits & kClosed) ? 0 : G.n_resp);
-    r.n_roll = F.n_roll + ((F.bits & kPassRoll) ? G.n_roll : 0);
+    r.n_resp = kC ? F.n_resp + ((F.bits & kClosed) ? 0 : G.n_resp) : 0;
+    r.n_roll = kC ? F.n_roll + ((F.bits & kPassRoll) ? G.n_roll : 0) : 0;
     return r;
 }
 
+template <bool kC>
 __device__ __forceinline__ GaeMap shfl_down_map(const GaeMap &a, int off) {
     GaeMap r;
     r.p = __shfl_down_sync(kFull, a.p, off);
@@ -106,11 +116,12 @@ __device__ __forceinline__ GaeMap shfl_down_map(const GaeMap &a, int off) {
     r.c = __shfl_down_sync(kFull, a.c, off);
     r.vf = __shfl_down_sync(kFull, a.vf, off);
     r.bits = __shfl_down_sync(kFull, a.bits, off);
-    r.n_resp = __shfl_down_sync(kFull, a.n_resp, off);
-    r.n_roll = __shfl_down_sync(kFull, a.n_roll, off);
+    r.n_resp = kC ? __shfl_down_sync(kFull, a.n_resp, off) : 0;
+    r.n_roll = kC ? __shfl_down_sync(kFull, a.n_roll, off) : 0;
     return r;
 }
 
+template <bool kC>
 __device__ __forceinline__ GaeMap shfl_map(const GaeMap &a, int src) {
     GaeMap r;
     r.p = __shfl_sync(kFull, a.p, src);
@@ -118,18 +129,19 @@ __device__ __forceinline__ GaeMap shfl_map(const GaeMap &a, int src) {
     r.c = __shfl_sync(kFull, a.c, src);
     r.vf = __shfl_sync(kFull, a.vf, src);
     r.bits = __shfl_sync(kFull, a.bits, src);
-    r.n_resp = __shfl_sync(kFull, a.n_resp, src);
-    r.n_roll = __shfl_sync(kFull, a.n_roll, src);
+    r.n_resp = kC ? __shfl_sync(kFull, a.n_resp, src) : 0;
+    r.n_roll = kC ? __shfl_sync(kFull, a.n_roll, src) : 0;
     return r;
 }
 
 // Inclusive suffix scan within a warp: lane l gets M_l o M_{l+1} o ... o M_31.
+template <bool kC>
 __device__ __forceinline__ GaeMap warp_suffix(GaeMap x) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        const GaeMap o = shfl_down_map(x, off);
-        if (lane + off < 32) x = compose(x, o);
+        const GaeMap o = shfl_down_map<kC>(x, off);
+        if (lane + off < 32) x = compose<kC>(x, o);
     }
     return x;
 }
@@ -150,26 +162,26 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
-// Waits (bounded) until *flag >= want; returns the flag, 0 on timeout.
-__device__ __forceinline__ uint32_t wait_flag(const uint32_t *flag, uint32_t want, uint32_t *status) {
-    uint32_t f = ld_acquire(flag);
-    if (f >= want) return f;
-    const unsigned long long t0 = global_ns();
-    while (true) {
-        __nanosleep(64);
-        f = ld_acquire(flag);
-        if (f >= want) return f;
-        if (global_ns() - t0 > kWaitNs) {
-            gae_raise(status, RL_ERR_TIMEOUT);
-            return 0;
-        }
-    }
-}
-
 __device__ __forceinline__ GaeMap load_record(const ChunkRecord *rec) {
     const float4 a = __ldcg(reinterpret_cast<const float4 *>(rec));
     const int4 b = __ldcg(reinterpret_cast<const int4 *>(rec) + 1);
     return GaeMap{a.x, a.y, a.z, a.w, (uint32_t)b.x, b.y, b.z};
+}
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// Float offset, within a values or rewards tile, of token e of the chunk.
+__device__ __forceinline__ int tile_off(int e) {
+    const int row = e / kTok, col = e % kTok;
+    return row * kTok + 4 * ((col >> 2) ^ (row & 7)) + (col & 3);
 }
 
 // First s in [0, S) with cu[s + 1] > x (S if none); one warp, 32-ary search.
@@ -204,7 +216,13 @@ struct Scale {
     float m, s1, s2, s3;
 };
 
-__device__ Scale cross_scale(int n, const GaeParams &p) {
+struct ScaleArgs {
+    int32_t gl_kind;
+    float log2_gl_hi, log2_gl_lo;
+    double log2_gl;
+};
+
+__device__ __noinline__ Scale cross_scale(int n, ScaleArgs p) {
     if (n <= 0 || p.gl_kind == 2) return Scale{1.f, 1.f, 1.f, 1.f};
     if (p.gl_kind == 1) return Scale{0.f, 1.f, 1.f, 1.f};
     // x = n log2(gamma lambda) = e + f with e an integer and |f| <= 1/2
@@ -243,32 +261,20 @@ __device__ Scale cross_scale(int n, const GaeParams &p) {
 
 __device__ __forceinline__ float apply_scale(float a, const Scale &s) { return ((a * s.m) * s.s1) * s.s2 * s.s3; }
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-
-// Shared-memory rows of one thread's 16 tokens: 64 bytes of data at a stride of
-// 80 bytes, so that the 16-byte reads of a quarter warp hit distinct banks.
-constexpr int kRowFloats = kTok + 4;
-
 template <bool kCross>
-__global__ void __launch_bounds__(kThreads, 4) gae_chunk_kernel(GaeParams p) {
-    __shared__ __align__(16) float s_r[kThreads * kRowFloats];
-    __shared__ __align__(16) float s_v[kThreads * kRowFloats];
-    __shared__ __align__(16) uint32_t s_m[kThreads * kTok / 4];
-    __shared__ uint32_t s_last[kWords];  // bit: the token is the last of its response
-    __shared__ uint32_t s_cont[kWords];  // bit: ... and its rollout continues into the next response
+__global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    float *s_r = reinterpret_cast<float *>(smem + kSmemR);
+    float *s_v = reinterpret_cast<float *>(smem + kSmemV);
+    uint8_t *s_m = smem + kSmemM;
+    __shared__ uint32_t s_last[kThreads];  // bit i of word w: token 32 w + i is the last of its response
+    __shared__ uint32_t s_cont[kThreads];  // ... and its rollout continues into the next response
     __shared__ GaeMap s_wtot[kThreads / 32];
     __shared__ GaeMap s_after[kThreads / 32];
     __shared__ int s_k, s_sa, s_sb, s_lo, s_hi;
     __shared__ float s_EA, s_EV;
     __shared__ int s_EP, s_ER;
+    __shared__ float s_pow[kTok + 1], s_qpow[kTok + 1];  // gl^k and gamma gl^(k-1), by repeated products
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = p.num_tokens, S = p.num_seqs;
@@ -280,9 +286,18 @@ __global__ void __launch_bounds__(kThreads, 4) gae_chunk_kernel(GaeParams p) {
         const uint32_t ticket = atomicAdd(&hdr->ticket, 1u);
         s_k = nchunks - 1 - (int)ticket;
     }
-    if (tid < kWords) {
-        s_last[tid] = 0u;
-        s_cont[tid] = 0u;
+    s_last[tid] = 0u;
+    s_cont[tid] = 0u;
+    if (tid == 32) {
+        float pw = 1.f, qw = 0.f;
+        s_pow[0] = 1.f;
+        s_qpow[0] = 0.f;
+        for (int i = 1; i <= kTok; ++i) {
+            pw = p.gl * pw;
+            qw = fmaf(p.gl, qw, i == 1 ? p.gamma : 0.f);
+            s_pow[i] = pw;
+            s_qpow[i] = qw;
+        }
     }
     __syncthreads();
     const int k = s_k;
@@ -296,22 +311,26 @@ __global__ void __launch_bounds__(kThreads, 4) gae_chunk_kernel(GaeParams p) {
     // stage the chunk: coalesced 16-byte copies straight into shared memory
     if (p.vec && ce - cs == kChunk) {
 #pragma unroll
-        for (int j = 0; j < kTok / 4; ++j) {
+        for (int j = 0; j < kVec; ++j) {
             const int f = j * kThreads + tid;  // float4 index within the chunk
-            const int off = (f >> 2) * kRowFloats + (f & 3) * 4;
+            const int off = tile_off(4 * f);
             cp_async16(s_r + off, p.rewards + cs + 4 * f);
             cp_async16(s_v + off, p.values + cs + 4 * f);
         }
-        cp_async16(s_m + 4 * tid, p.mask + cs + kTok * tid);
+#pragma unroll
+        for (int j = 0; j < kChunk / 16 / kThreads; ++j) {
+            const int f = j * kThreads + tid;
+            cp_async16(s_m + 16 * f, p.mask + cs + 16 * f);
+        }
     } else {
 #pragma unroll 4
         for (int j = 0; j < kTok; ++j) {
             const int e = j * kThreads + tid, t = cs + e;
             const bool in = t < ce;
-            const int off = (e / kTok) * kRowFloats + e % kTok;
+            const int off = tile_off(e);
             s_r[off] = in ? __ldg(p.rewards + t) : 0.f;
             s_v[off] = in ? __ldg(p.values + t) : 0.f;
-            reinterpret_cast<uint8_t *>(s_m)[e] = in ? __ldg(p.mask + t) : (uint8_t)0;
+            s_m[e] = in ? __ldg(p.mask + t) : (uint8_t)0;
         }
     }
 
@@ -362,37 +381,58 @@ __global__ void __launch_bounds__(kThreads, 4) gae_chunk_kernel(GaeParams p) {
     cp_async_wait_all();
     __syncthreads();
 
-    const uint32_t last = (s_last[tid >> 1] >> (16 * (tid & 1))) & 0xffffu;
-    const uint32_t cont = kCross ? (s_cont[tid >> 1] >> (16 * (tid & 1))) & 0xffffu : 0u;
-    uint32_t inr = 0u, act = 0u, msk = 0u;
+    const uint32_t last = s_last[tid];
+    const uint32_t cont = kCross ? s_cont[tid] : 0u;
+    uint32_t inr, act, msk;
     {
-        const uint4 m4 = *reinterpret_cast<const uint4 *>(s_m + 4 * tid);
-        const uint32_t mw[4] = {m4.x, m4.y, m4.z, m4.w};
-        const int lo = s_lo, hi = s_hi;
+        // bit i: token t0 + i lies in [lo, hi) / has a nonzero mask byte / is an action token
+        const uint4 ma = *reinterpret_cast<const uint4 *>(s_m + kTok * tid);
+        const uint4 mb4 = *reinterpret_cast<const uint4 *>(s_m + kTok * tid + 16);
+        const uint32_t mw[8] = {ma.x, ma.y, ma.z, ma.w, mb4.x, mb4.y, mb4.z, mb4.w};
+        uint32_t mb = 0u;
 #pragma unroll
-        for (int i = 0; i < kTok; ++i) {
-            const int t = t0 + i;
-            const bool in = t >= lo && t < hi;
-            const bool m = ((mw[i >> 2] >> (8 * (i & 3))) & 0xffu) != 0u;
-            inr |= (uint32_t)in << i;
-            msk |= (uint32_t)(in && m) << i;
-            act |= (uint32_t)(in && (m || !p.skip_observations)) << i;
+        for (int w = 0; w < 8; ++w) {
+            const uint32_t x = __vcmpne4(mw[w], 0u) & 0x01010101u;  // one bit per byte
+            mb |= ((x * 0x10204080u) >> 28) << (4 * w);             // gathered into 4 bits
         }
+        const int a = min(max(s_lo - t0, 0), kTok), b = min(max(s_hi - t0, 0), kTok);
+        const uint32_t below_b = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
+        inr = a < b ? (below_b & ~((1u << a) - 1u)) : 0u;
+        msk = mb & inr;
+        act = p.skip_observations ? msk : inr;
     }
     const float gamma = p.gamma, gl = p.gl;
-    const float *row_r = s_r + tid * kRowFloats;
-    const float *row_v = s_v + tid * kRowFloats;
+    const ScaleArgs sargs{p.gl_kind, p.log2_gl_hi, p.log2_gl_lo, p.log2_gl};
+    const float *row_r = s_r + tid * kTok;
+    const float *row_v = s_v + tid * kTok;
+    const int sw = tid & 7;  // this row's swizzle
 
     // fold the thread's tokens, right to left
     GaeMap F = map_identity();
+    if (last == 0u) {
+        // no response end among them: only the action tokens' affine steps
+        float c = 0.f, vf = 0.f;
 #pragma unroll
-    for (int j = kTok / 4 - 1; j >= 0; --j) {
-        const float4 r4 = *reinterpret_cast<const float4 *>(row_r + 4 * j);
-        const float4 v4 = *reinterpret_cast<const float4 *>(row_v + 4 * j);
-        const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, vv[4] = {v4.x, v4.y, v4.z, v4.w};
+        for (int j = kVec - 1; j >= 0; --j) {
+            const float4 r4 = *reinterpret_cast<const float4 *>(row_r + 4 * (j ^ sw));
+            const float4 v4 = *reinterpret_cast<const float4 *>(row_v + 4 * (j ^ sw));
+            const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-        for (int u = 3; u >= 0; --u) {
-            const int i = 4 * j + u;
+            for (int u = 3; u >= 0; --u) {
+                if ((act >> (4 * j + u)) & 1u) {
+                    c = fmaf(gl, c, fmaf(gamma, vf, rr[u] - vv[u]));
+                    vf = vv[u];
+                }
+            }
+        }
+        const int na = __popc(act), n = kCross ? __popc(msk) : 0;
+        F = GaeMap{s_pow[na], s_qpow[na], c, vf, (na ? 0u : kPassV) | kPassRoll, n, n};
+    } else {
+        // a response ends among them (rare): token by token
+#pragma unroll 1
+        for (int i = kTok - 1; i >= 0; --i) {
+            const int o = 4 * ((i >> 2) ^ sw) + (i & 3);
+            const float r = row_r[o], v = row_v[o];
             if ((last >> i) & 1u) {  // a response ends here: the state from the right is dropped
                 const bool c = (cont >> i) & 1u;
                 F.bits = kClosed | ((c && (F.bits & kPassRoll)) ? kPassRoll : 0u);
@@ -401,10 +441,10 @@ __global__ void __launch_bounds__(kThreads, 4) gae_chunk_kernel(GaeParams p) {
                 F.n_roll = c ? F.n_roll : 0;
             }
             if ((act >> i) & 1u) {
-                F.c = fmaf(gl, F.c, fmaf(gamma, F.vf, rr[u] - vv[u]));
+                F.c = fmaf(gl, F.c, fmaf(gamma, F.vf, r - v));
                 F.q = fmaf(gl, F.q, (F.bits & kPassV) ? gamma : 0.f);
                 F.p = gl * F.p;
-                F.vf = vv[u];
+                F.vf = v;
                 F.bits &= ~kPassV;
             }
             if (kCross && ((msk >> i) & 1u)) {
@@ -415,72 +455,94 @@ __global__ void __launch_bounds__(kThreads, 4) gae_chunk_kernel(GaeParams p) {
     }
 
     // exclusive suffix over the block's threads, and the chunk's map
-    const GaeMap incl = warp_suffix(F);
+    const GaeMap incl = warp_suffix<kCross>(F);
     if (lane == 0) s_wtot[warp] = incl;
     __syncthreads();
-    if (warp == 0) {
-        const GaeMap wi = warp_suffix(lane < kThreads / 32 ? s_wtot[lane] : map_identity());
-        GaeMap after = shfl_down_map(wi, 1);
-        if (lane == 31) after = map_identity();
-        if (lane < kThreads / 32) s_after[lane] = after;
-        const GaeMap agg = shfl_map(wi, 0);
-        if (lane == 0) {
-            ChunkRecord *rec = recs + k;
-            *reinterpret_cast<float4 *>(rec) = make_float4(agg.p, agg.q, agg.c, agg.vf);
-            *(reinterpret_cast<int4 *>(rec) + 1) = make_int4((int)agg.bits, agg.n_resp, agg.n_roll, 0);
-            st_release(&rec->flag, 1u);
-        }
-        // Look back over the chunks to the right. The maps: composed in a fixed
-        // tree up to the first chunk that holds a response end. The rollout
-        // count (kCross): summed up to the first chunk with a rollout end or an
-        // inclusive count.
-        GaeMap acc = map_identity();
-        int R = 0;
-        bool need_map = true, need_roll = kCross;
-        for (int base = k + 1; need_map || need_roll; base += 32) {
-            const int j = base + lane;
-            GaeMap m = map_zero();
-            uint32_t f = 0u;
-            int incl_roll = 0;
-            if (j < nchunks) {
-                f = wait_flag(&recs[j].flag, 1u, p.status);
-                if (f) m = load_record(recs + j);
-                if (kCross && f >= 2u) incl_roll = __ldcg(&recs[j].roll_incl);
+    GaeMap agg = map_identity();  // the chunk's map (held by warp 1)
+    if (warp <= 1) {
+        const GaeMap wi = warp_suffix<kCross>(lane < kThreads / 32 ? s_wtot[lane] : map_identity());
+        agg = shfl_map<kCross>(wi, 0);
+        if (warp == 1) {
+            if (lane == 0) {  // publish (the release fence stalls this warp, not the look-back)
+                ChunkRecord *rec = recs + k;
+                *reinterpret_cast<float4 *>(rec) = make_float4(agg.p, agg.q, agg.c, agg.vf);
+                *(reinterpret_cast<int4 *>(rec) + 1) = make_int4((int)agg.bits, agg.n_resp, agg.n_roll, 0);
+                st_release(&rec->flag, 1u);
             }
-            if (need_map) {
-                const unsigned cb = __ballot_sync(kFull, (m.bits & kClosed) != 0u);
-                const int fc = __ffs(cb) - 1;
-                GaeMap mm = (fc >= 0 && lane > fc) ? map_identity() : m;
-                acc = compose(acc, shfl_map(warp_suffix(mm), 0));
-                need_map = fc < 0;
-            }
-            if (kCross && need_roll) {
-                const bool stop = f >= 2u || (m.bits & kPassRoll) == 0u;
-                const unsigned sb = __ballot_sync(kFull, stop);
-                const int fs = __ffs(sb) - 1;
-                int val = f >= 2u ? incl_roll : m.n_roll;
-                if (fs >= 0 && lane > fs) val = 0;
+        } else {
+            GaeMap after = shfl_down_map<kCross>(wi, 1);
+            if (lane == 31) after = map_identity();
+            if (lane < kThreads / 32) s_after[lane] = after;
+            // Look back over the chunks to the right. The maps: composed in a
+            // fixed tree up to the first chunk that holds a response end. The
+            // rollout count (kCross): summed up to the first chunk with a
+            // rollout end or a published inclusive count. Only the chunks up
+            // to those stopping points are waited for.
+            GaeMap acc = map_identity();
+            int R = 0;
+            bool need_map = true, need_roll = kCross;
+            const unsigned long long t_begin = global_ns();
+            for (int base = k + 1; need_map || need_roll; base += 32) {
+                const int j = base + lane;
+                bool ready = j >= nchunks;  // beyond the last chunk: the zero state
+                GaeMap m = map_zero();
+                uint32_t f = 0u;
+                int incl_roll = 0;
+                int fcm = -1, fcr = -1;
+                while (true) {
+                    if (!ready) {
+                        f = ld_acquire(&recs[j].flag);
+                        if (f) {
+                            ready = true;
+                            m = load_record(recs + j);
+                            if (kCross && f >= 2u) incl_roll = __ldcg(&recs[j].roll_incl);
+                        } else if (global_ns() - t_begin > kWaitNs) {
+                            gae_raise(p.status, RL_ERR_TIMEOUT);
+                            ready = true;  // treated as a response end
+                        }
+                    }
+                    const unsigned rdy = __ballot_sync(kFull, ready);
+                    const unsigned stm = __ballot_sync(kFull, ready && (m.bits & kClosed));
+                    const unsigned str = __ballot_sync(kFull, ready && (f >= 2u || !(m.bits & kPassRoll)));
+                    const int pre = rdy == kFull ? 32 : __ffs(~rdy) - 1;  // lanes 0..pre-1 are ready
+                    fcm = __ffs(stm) - 1;
+                    fcr = __ffs(str) - 1;
+                    const bool okm = !need_map || pre == 32 || (fcm >= 0 && fcm < pre);
+                    const bool okr = !need_roll || pre == 32 || (fcr >= 0 && fcr < pre);
+                    if (okm && okr) break;
+                    __nanosleep(32);
+                }
+                if (need_map) {
+                    const GaeMap mm = (fcm >= 0 && lane > fcm) ? map_identity() : m;
+                    acc = compose<kCross>(acc, shfl_map<kCross>(warp_suffix<kCross>(mm), 0));
+                    need_map = fcm < 0;
+                }
+                if (kCross && need_roll) {
+                    int val = f >= 2u ? incl_roll : m.n_roll;
+                    if (fcr >= 0 && lane > fcr) val = 0;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) val += __shfl_xor_sync(kFull, val, off);
-                R += val;
-                need_roll = fs < 0;
+                    for (int off = 16; off > 0; off >>= 1) val += __shfl_xor_sync(kFull, val, off);
+                    R += val;
+                    need_roll = fcr < 0;
+                }
             }
-        }
-        if (lane == 0) {
-            if (kCross) {
-                recs[k].roll_incl = agg.n_roll + ((agg.bits & kPassRoll) ? R : 0);
-                st_release(&recs[k].flag, 2u);
+            if (lane == 0) {  // the state arriving at the chunk's right edge
+                s_EA = acc.c;
+                s_EV = acc.vf;
+                s_EP = acc.n_resp;
+                s_ER = R;
             }
-            // the state arriving at the chunk's right edge
-            s_EA = acc.c;
-            s_EV = acc.vf;
-            s_EP = acc.n_resp;
-            s_ER = R;
         }
     }
     __syncthreads();
-    if (warp == 0) {
-        // past the look-back: the last block to get here leaves the workspace zeroed for the next launch
+    if (warp == 1) {
+        if (lane == 0) {
+            if (kCross) {
+                recs[k].roll_incl = agg.n_roll + ((agg.bits & kPassRoll) ? s_ER : 0);
+                st_release(&recs[k].flag, 2u);
+            }
+        }
+        // past the look-back: the last block to get here leaves the workspace ready for the next launch
         uint32_t d = 0u;
         if (lane == 0) asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(d) : "l"(&hdr->done) : "memory");
         d = __shfl_sync(kFull, d, 0);
@@ -494,27 +556,54 @@ __global__ void __launch_bounds__(kThreads, 4) gae_chunk_kernel(GaeParams p) {
     }
 
     // the state arriving at this thread's tokens
-    GaeMap right = shfl_down_map(incl, 1);
+    GaeMap right = shfl_down_map<kCross>(incl, 1);
     if (lane == 31) right = map_identity();
-    const GaeMap X = compose(right, s_after[warp]);
+    const GaeMap X = compose<kCross>(right, s_after[warp]);
     float A = fmaf(X.p, s_EA, fmaf(X.q, s_EV, X.c));
     float V = (X.bits & kPassV) ? s_EV : X.vf;
     int P = X.n_resp + ((X.bits & kClosed) ? 0 : s_EP);
     int R = X.n_roll + ((X.bits & kPassRoll) ? s_ER : 0);
 
-    // re-walk: advantages, scaled per response; written 4 tokens at a time
-    const bool vec_out = p.vec && inr == 0xffffu;
-    int cached = -1;
-    Scale sc{1.f, 1.f, 1.f, 1.f};
+    // re-walk: advantages (and returns), scaled per response, written in place of the staged rows
+    const bool want_ret = p.returns != nullptr;
+    float *wrow_r = s_r + tid * kTok;
+    float *wrow_v = s_v + tid * kTok;
+    if (last == 0u) {
+        // every token here belongs to one response: one discount factor
+        Scale sc{1.f, 1.f, 1.f, 1.f};
+        if (kCross) sc = cross_scale(R - P, sargs);
+        // a factor whose product with m stays normal folds into one multiplication
+        const bool single = sc.s2 == 1.f && sc.s3 == 1.f && (sc.m == 0.f || sc.s1 >= 0x1p-125f);
+        const float f1 = sc.m * sc.s1;
 #pragma unroll
-    for (int j = kTok / 4 - 1; j >= 0; --j) {
-        const float4 r4 = *reinterpret_cast<const float4 *>(row_r + 4 * j);
-        const float4 v4 = *reinterpret_cast<const float4 *>(row_v + 4 * j);
-        const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, vv[4] = {v4.x, v4.y, v4.z, v4.w};
-        float out[4], ret[4];
+        for (int j = kVec - 1; j >= 0; --j) {
+            const float4 r4 = *reinterpret_cast<const float4 *>(row_r + 4 * (j ^ sw));
+            const float4 v4 = *reinterpret_cast<const float4 *>(row_v + 4 * (j ^ sw));
+            const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, vv[4] = {v4.x, v4.y, v4.z, v4.w};
+            float out[4], ret[4];
 #pragma unroll
-        for (int u = 3; u >= 0; --u) {
-            const int i = 4 * j + u;
+            for (int u = 3; u >= 0; --u) {
+                out[u] = 0.f;
+                ret[u] = 0.f;
+                if ((act >> (4 * j + u)) & 1u) {
+                    A = fmaf(gl, A, fmaf(gamma, V, rr[u] - vv[u]));
+                    V = vv[u];
+                    const float o = !kCross ? A : (single ? A * f1 : apply_scale(A, sc));
+                    out[u] = o;
+                    ret[u] = o + vv[u];
+                }
+            }
+            *reinterpret_cast<float4 *>(wrow_r + 4 * (j ^ sw)) = make_float4(out[0], out[1], out[2], out[3]);
+            if (want_ret)
+                *reinterpret_cast<float4 *>(wrow_v + 4 * (j ^ sw)) = make_float4(ret[0], ret[1], ret[2], ret[3]);
+        }
+    } else {
+        int cached = -1;
+        Scale sc{1.f, 1.f, 1.f, 1.f};
+#pragma unroll 1
+        for (int i = kTok - 1; i >= 0; --i) {
+            const int o = 4 * ((i >> 2) ^ sw) + (i & 3);
+            const float r = row_r[o], v = row_v[o];
             if ((last >> i) & 1u) {
                 A = V = 0.f;
                 P = 0;
@@ -524,38 +613,73 @@ __global__ void __launch_bounds__(kThreads, 4) gae_chunk_kernel(GaeParams p) {
                 P += 1;
                 R += 1;
             }
-            out[u] = 0.f;
-            ret[u] = 0.f;
+            float out = 0.f, ret = 0.f;
             if ((act >> i) & 1u) {
-                A = fmaf(gl, A, fmaf(gamma, V, rr[u] - vv[u]));
-                V = vv[u];
-                float o = A;
+                A = fmaf(gl, A, fmaf(gamma, V, r - v));
+                V = v;
+                out = A;
                 if (kCross) {
                     const int later = R - P;
                     if (later != cached) {
-                        sc = cross_scale(later, p);
+                        sc = cross_scale(later, sargs);
                         cached = later;
                     }
-                    o = apply_scale(o, sc);
+                    out = apply_scale(out, sc);
                 }
-                out[u] = o;
-                ret[u] = o + vv[u];
+                ret = out + v;
             }
-        }
-        if (vec_out) {
-            __stcs(reinterpret_cast<float4 *>(p.adv + t0) + j, make_float4(out[0], out[1], out[2], out[3]));
-            if (p.returns)
-                __stcs(reinterpret_cast<float4 *>(p.returns + t0) + j, make_float4(ret[0], ret[1], ret[2], ret[3]));
-        } else {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = 4 * j + u;
-                if (!((inr >> i) & 1u)) continue;
-                p.adv[t0 + i] = out[u];
-                if (p.returns) p.returns[t0 + i] = ret[u];
-            }
+            wrow_r[o] = out;
+            if (want_ret) wrow_v[o] = ret;
         }
     }
+
+    // store: coalesced 16-byte stores of the rows inside [lo, hi), token by token elsewhere
+    __syncthreads();
+    const int a_in = min(max(s_lo - cs, 0), kChunk), b_in = min(max(min(s_hi, ce) - cs, 0), kChunk);
+    if (p.vec) {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const int f = j * kThreads + tid;
+            const int e0 = 4 * f, off = tile_off(e0);
+            if (e0 >= a_in && e0 + 4 <= b_in) {
+                __stcs(reinterpret_cast<float4 *>(p.adv + cs) + f, *reinterpret_cast<const float4 *>(s_r + off));
+                if (want_ret)
+                    __stcs(reinterpret_cast<float4 *>(p.returns + cs) + f, *reinterpret_cast<const float4 *>(s_v + off));
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (e0 + u < a_in || e0 + u >= b_in) continue;
+                    p.adv[cs + e0 + u] = s_r[off + u];
+                    if (want_ret) p.returns[cs + e0 + u] = s_v[off + u];
+                }
+            }
+        }
+    } else {
+#pragma unroll 4
+        for (int j = 0; j < kTok; ++j) {
+            const int e = j * kThreads + tid;
+            if (e < a_in || e >= b_in) continue;
+            const int off = tile_off(e);
+            p.adv[cs + e] = s_r[off];
+            if (want_ret) p.returns[cs + e] = s_v[off];
+        }
+    }
+}
+
+template <bool kCross>
+cudaError_t launch_chunks(const GaeParams &p, unsigned nchunks, cudaStream_t stream) {
+    static std::atomic<uint64_t> configured{0};  // one bit per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(gae_chunk_kernel<kCross>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
+    gae_chunk_kernel<kCross><<<nchunks, kThreads, kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -572,11 +696,8 @@ cudaError_t launch_gae(GaeParams p, cudaStream_t stream) {
                          reinterpret_cast<uintptr_t>(p.mask) | reinterpret_cast<uintptr_t>(p.adv) |
                          reinterpret_cast<uintptr_t>(p.returns);
     p.vec = (al & 15u) == 0u;
-    if (p.rollout_ids)
-        gae_chunk_kernel<true><<<(unsigned)nchunks, kThreads, 0, stream>>>(p);
-    else
-        gae_chunk_kernel<false><<<(unsigned)nchunks, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return p.rollout_ids ? launch_chunks<true>(p, (unsigned)nchunks, stream)
+                         : launch_chunks<false>(p, (unsigned)nchunks, stream);
 }
 
 }  // namespace rlk

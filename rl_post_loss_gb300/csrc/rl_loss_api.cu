@@ -475,3 +475,33 @@ extern "C" RL_LOSS_API rl_status rl_gae_advantages(const rl_gae_config *config, 
     if (rlk::launch_gae(p, reinterpret_cast<cudaStream_t>(stream_ptr)) != cudaSuccess) return RL_ERR_CUDA;
     return RL_OK;
 }
+
+extern "C" RL_LOSS_API int32_t rl_topk_max_k(void) { return rlk::topk_max_k(); }
+
+extern "C" RL_LOSS_API rl_status rl_topk(const rl_topk_config *config, int32_t rows, const float *scores, int64_t ld,
+                                         const int32_t *lengths, int32_t *out_idx, float *out_val, int64_t ldo,
+                                         uint32_t *device_status, void *stream_ptr) {
+    if (!config) return RL_ERR_INVALID_ARG;
+    const rl_topk_config &c = *config;
+    if (c.order != RL_TOPK_BY_SCORE && c.order != RL_TOPK_BY_POSITION) return RL_ERR_INVALID_ARG;
+    if (c.k < 1 || c.k > rlk::topk_max_k()) return RL_ERR_UNSUPPORTED;
+    if (rows < 0 || ld < 1 || ld > INT32_MAX || ldo < c.k) return RL_ERR_SHAPE;
+    if (rows == 0) return RL_OK;
+    if (!scores || !out_idx) return RL_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(scores) & 15u) || (ld & 3) || (reinterpret_cast<uintptr_t>(out_idx) & 3u) ||
+        (reinterpret_cast<uintptr_t>(out_val) & 3u) || (reinterpret_cast<uintptr_t>(lengths) & 3u))
+        return RL_ERR_ALIGNMENT;
+    rlk::TopkParams p{};
+    p.scores = scores;
+    p.ld = ld;
+    p.lengths = lengths;
+    p.rows = rows;
+    p.k = c.k;
+    p.order_by_score = c.order == RL_TOPK_BY_SCORE ? 1 : 0;
+    p.out_idx = out_idx;
+    p.out_val = out_val;
+    p.ldo = ldo;
+    p.status = device_status;
+    if (rlk::launch_topk(p, reinterpret_cast<cudaStream_t>(stream_ptr)) != cudaSuccess) return RL_ERR_CUDA;
+    return RL_OK;
+}

@@ -27,7 +27,7 @@ def test_library_exports_every_declared_function(lib):
         assert hasattr(lib, n), n
     out = subprocess.check_output(["nm", "-D", "--defined-only", capi.LIB_PATH]).decode()
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
-    api = {n for n in exported if n.startswith(("rl_loss_", "rl_gae_"))}
+    api = {n for n in exported if n.startswith(("rl_loss_", "rl_gae_", "rl_topk"))}
     assert api == set(names), (api ^ set(names))
 
 
@@ -119,3 +119,20 @@ def test_gae_host_side_argument_checks(lib):
     cross = capi.rl_gae_config(1.0, 0.95, 1, 1)
     assert lib.rl_gae_advantages(ctypes.byref(cross), T, 4, fake, fake, fake, fake, None, fake, None, fake, need, None,
                                  None) == capi.CODES["RL_ERR_INVALID_ARG"]
+
+
+def test_topk_host_side_argument_checks(lib):
+    fake = ctypes.c_void_p(0x10000)
+    ok = capi.rl_topk_config(2048, capi.RL_TOPK_BY_SCORE)
+    assert capi.rl_topk_max_k() == 4096
+    call = lambda cfg, rows=4, ld=4096, scores=fake, ldo=2048: lib.rl_topk(
+        ctypes.byref(cfg), rows, scores, ld, None, fake, None, ldo, None, None)
+    assert call(capi.rl_topk_config(0, 0)) == capi.CODES["RL_ERR_UNSUPPORTED"]
+    assert call(capi.rl_topk_config(4097, 0)) == capi.CODES["RL_ERR_UNSUPPORTED"]
+    assert call(capi.rl_topk_config(16, 7)) == capi.CODES["RL_ERR_INVALID_ARG"]
+    assert call(ok, ldo=100) == capi.CODES["RL_ERR_SHAPE"]
+    assert call(ok, rows=-1) == capi.CODES["RL_ERR_SHAPE"]
+    assert call(ok, ld=4098) == capi.CODES["RL_ERR_ALIGNMENT"]
+    assert call(ok, scores=ctypes.c_void_p(0x10004)) == capi.CODES["RL_ERR_ALIGNMENT"]
+    assert call(ok, scores=None) == capi.CODES["RL_ERR_INVALID_ARG"]
+    assert call(ok, rows=0) == capi.CODES["RL_OK"]

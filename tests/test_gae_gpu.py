@@ -4,12 +4,12 @@ determinism.
 
 Tolerance, derived from the kernel's fp32 arithmetic. Every action token's
 advantage is a weighted sum A_t = sum_k x^k delta_{t+k} (x = gamma lambda, k
-counting action tokens), evaluated by the kernel through per-thread folds of 16
-tokens, a fixed tree over the 256 threads of a 4096-token chunk, a look-back
+counting action tokens), evaluated by the kernel through per-thread folds of 32
+tokens, a fixed tree over the 256 threads of an 8192-token chunk, a look-back
 tree over the chunks to the right, and a per-thread re-walk. A composition adds
-at most 3 roundings to a term, so a term passes through at most about 120 fp32
-roundings (fold 17, the chunk's tree 24, the look-back tree 15 plus 3 for every
-further 32 chunks, the exclusive tree 27, the re-walk 32), and the weight x^k
+at most 3 roundings to a term, so a term passes through at most about 170 fp32
+roundings (fold 33, the chunk's tree 24, the look-back tree 15 plus 3 for every
+further 32 chunks, the exclusive tree 27, the re-walk 64), and the weight x^k
 is a product of k rounded factors, so
   |err_t| <= u (256 S0_t + 2 S1_t) + 2 u |A_t|,
   S0_t = sum_k x^k M_{t+k},  S1_t = sum_k k x^k M_{t+k},
@@ -166,8 +166,8 @@ def _workspace_is_clear(T):
 
 
 def test_gae_long_responses_span_many_chunks():
-    # 150000 tokens = 37 chunks: the look-back composes more than one window of 32 chunks
-    gb = synthetic.make_gae_batch("cuda", lengths=[150000, 3, 140000, 70000], segments=2)
+    # 300000 tokens = 37 chunks of 8192: the look-back composes more than one window of 32 chunks
+    gb = synthetic.make_gae_batch("cuda", lengths=[300000, 3, 140000, 70000], segments=2)
     _check(gb, cross=True)
     _check(gb, skip=False)
     assert _workspace_is_clear(gb.num_tokens)
