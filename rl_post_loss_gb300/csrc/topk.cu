@@ -7,7 +7,7 @@
 // above every number, then larger score, then lower position; -0 and +0 tie.
 // Scores map to 32-bit keys whose unsigned order is that order's score part.
 //
-// Design: one CTA per row, one pass over the row in HBM. Any prefix of the
+// Design: one CTA per row at a time, one pass over the row in HBM. Any prefix of the
 // row bounds the final selection: an element that is not among the k best of
 // the prefix seen so far (in the total order) cannot be among the k best of
 // the row. So the CTA streams the row in tiles of 4096 scores and appends to
@@ -19,8 +19,14 @@
 // (by score, ties by position, or by position). The buffer's order of arrival
 // (shared-memory atomics) never decides anything: the kept set is defined by
 // the total order and the output order by the sort, so the result is
-// bit-identical from run to run. All counts are integers.
+// bit-identical from run to run. All counts are integers. The CTAs are
+// persistent (two per SM); thread 0 keeps two 16 KB tiles in flight with bulk
+// copies (TMA) into a shared-memory ring, completing on mbarriers whose waits
+// are bounded, and runs ahead into the next row while this one is finished.
+#include <algorithm>
+
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace rlk {
 
@@ -31,6 +37,7 @@ constexpr int kPer = 8;                 // scores per thread per tile (two float
 constexpr int kTile = kThreads * kPer;  // 4096
 constexpr int kCap = 8192;              // buffer entries
 constexpr int kBins = 2048;
+constexpr int kStages = 2;              // tiles in flight per CTA (16 KB each)
 constexpr unsigned kFull = 0xffffffffu;
 
 // Unsigned order = score order; NaN above +inf; -0 folded onto +0. Every number maps to >= 0x007fffff,
@@ -43,14 +50,24 @@ __device__ __forceinline__ uint32_t order_key(float x) {
 }
 
 struct TopkSmem {
+    float ring[kStages][kTile];  // tiles of scores, filled by bulk copies
     uint32_t key[kCap];
     uint32_t idx[kCap];
     uint32_t hist[kBins];
+    unsigned long long full[kStages];  // mbarriers: a tile has landed
     uint32_t warp_tot[kThreads / 32];
     int count;      // entries in the buffer
     int found_bin;  // result of the last histogram search
     int found_before;
+    int failed;     // a bounded wait ran out
 };
+
+// hist[digit] += 1 for every lane with `valid`, one atomic per distinct digit of the warp (the
+// scores tie often, so many lanes share a digit). All 32 lanes must call it.
+__device__ __forceinline__ void hist_add_warp(uint32_t *hist, uint32_t digit, bool valid) {
+    const unsigned peers = __match_any_sync(kFull, valid ? digit : 0xffffffffu);
+    if (valid && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+}
 
 // Finds, over hist[0..kBins), the bin b at which the running count (from the top bin down when
 // `from_top`, from bin 0 up otherwise) first reaches `target`; stores b and the count of the bins
@@ -93,7 +110,7 @@ __device__ void find_bin(TopkSmem &s, uint32_t target, bool from_top) {
 // `target` in the total order); otherwise keeps the entries whose key reaches a lower bound, at
 // least `target` of them and at most `limit`. Returns the new lower bound for incoming scores
 // (as a 64-bit value: 2^32 admits nothing). Block-wide.
-__device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact) {
+__device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int idx_bits) {
     const int tid = threadIdx.x;
     const int cnt = s.count;
     // the key prefix fixed so far, and how many buffer entries lie strictly above it
@@ -108,9 +125,11 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact) {
         const int sh = shift - w;
         for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0u;
         __syncthreads();
-        for (int i = tid; i < cnt; i += kThreads) {
-            const uint32_t k = s.key[i];
-            if (shift == 32 || (k >> shift) == prefix) atomicAdd(&s.hist[(k >> sh) & ((1u << w) - 1u)], 1u);
+        for (int i0 = tid & ~31; i0 < cnt; i0 += kThreads) {  // warp-uniform trip count
+            const int i = i0 + (tid & 31);
+            const uint32_t k = i < cnt ? s.key[i] : 0u;
+            const bool in = i < cnt && (shift == 32 || (k >> shift) == prefix);
+            hist_add_warp(s.hist, (k >> sh) & ((1u << w) - 1u), in);
         }
         __syncthreads();
         find_bin(s, (uint32_t)(target - above), true);
@@ -134,20 +153,22 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact) {
             // keep only the (target - above) equal entries with the lowest positions
             const int need = target - above;
             uint32_t ipre = 0u;
-            int ishift = 32, ibelow = 0;
-            for (int level = 0; level < 3; ++level) {
-                const int w = level == 2 ? 10 : 11;
+            int ishift = idx_bits, ibelow = 0;  // positions are below 2^idx_bits
+            while (ishift > 0) {
+                const int w = min(11, ishift);
                 const int sh = ishift - w;
                 for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0u;
                 __syncthreads();
-                for (int i = tid; i < cnt; i += kThreads) {
-                    if (s.key[i] != key_star) continue;
-                    const uint32_t ix = s.idx[i];
-                    if (ishift == 32 || (ix >> ishift) == ipre) atomicAdd(&s.hist[(ix >> sh) & ((1u << w) - 1u)], 1u);
+                for (int i0 = tid & ~31; i0 < cnt; i0 += kThreads) {
+                    const int i = i0 + (tid & 31);
+                    const bool eq = i < cnt && s.key[i] == key_star;
+                    const uint32_t ix = eq ? s.idx[i] : 0u;
+                    const bool in = eq && (ishift >= 32 || (ix >> ishift) == ipre);
+                    hist_add_warp(s.hist, (ix >> sh) & ((1u << w) - 1u), in);
                 }
                 __syncthreads();
                 find_bin(s, (uint32_t)(need - ibelow), false);
-                ipre = (ishift == 32 ? 0u : (ipre << w)) | (uint32_t)s.found_bin;
+                ipre = (ishift >= 32 ? 0u : (ipre << w)) | (uint32_t)s.found_bin;
                 ibelow += s.found_before;
                 ishift = sh;
                 __syncthreads();
@@ -212,84 +233,170 @@ __device__ void bitonic(TopkSmem &s, int n2, bool by_score) {
     }
 }
 
+// The score test equivalent to key >= bound. mode 0: !(x < thr), thr the smallest score whose key
+// reaches the bound (NaN passes it, and -0 and +0 compare equal, as their keys do); mode 1 (bound
+// above the key of +inf): NaN only; mode 2 (bound above every key): nothing.
+__device__ __forceinline__ void set_threshold(uint64_t bound, float &thr, int &mode) {
+    mode = bound > 0xffffffffull ? 2 : (bound > 0xff800000ull ? 1 : 0);
+    const uint32_t b = bound > 0xff800000ull ? 0xff800000u : (uint32_t)bound;
+    if (b < 0x007fffffu) {  // at or below the key of -inf: every number
+        thr = -INFINITY;
+    } else {
+        thr = __uint_as_float((b & 0x80000000u) ? (b & 0x7fffffffu) : ~b);
+    }
+}
+
+// The valid length of row r (clamped to [0, ld]).
+__device__ __forceinline__ int row_length(const TopkParams &p, int r) {
+    const int n = p.lengths ? __ldg(p.lengths + r) : (int)p.ld;
+    return min(max(n, 0), (int)p.ld);
+}
+
+// Persistent CTAs, each taking rows blockIdx.x, blockIdx.x + gridDim.x, ... Thread 0 keeps
+// kStages tiles of 4096 scores in flight (bulk copies into a shared-memory ring, one mbarrier
+// per stage), running ahead across row boundaries, and waits for each tile just before the
+// barrier that ends the previous one; every thread filters the landed tile into the candidate
+// buffer.
 __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     TopkSmem &s = *reinterpret_cast<TopkSmem *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31;
-    const int row = blockIdx.x;
-    const float *x = p.scores + (size_t)row * (size_t)p.ld;
-    int n = p.lengths ? __ldg(p.lengths + row) : (int)p.ld;
-    if (n < 0 || n > p.ld) {
-        if (tid == 0 && p.status) raise_status(p.status, RL_ERR_SEQLENS);
-        n = min(max(n, 0), (int)p.ld);
-    }
-    const int k = p.k, kk = min(k, n);
-    if (tid == 0) s.count = 0;
-    __syncthreads();
-
-    uint64_t bound = 0u;  // incoming scores are kept when key >= bound
-    const int ntiles = (n + kTile - 1) / kTile;
-    float4 cur[2], nxt[2];
-    auto load_tile = [&](int t, float4 (&v)[2]) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int e = t * kTile + 4 * (j * kThreads + tid);
-            v[j] = e < n ? __ldcs(reinterpret_cast<const float4 *>(x + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int k = p.k;
+    const int idx_bits = p.ld <= (1 << 22) ? 22 : 32;
+    // producer cursor (thread 0): the next tile to copy
+    int prow = blockIdx.x, ptile = 0, pn = prow < p.rows ? row_length(p, prow) : 0;
+    uint32_t issued = 0u, landed = 0u;  // thread 0: tiles copied so far / known to have landed
+    const uint64_t policy = ptx::policy_evict_first();
+    auto issue_next = [&](int stage) {
+        while (prow < p.rows && ptile * kTile >= pn) {
+            prow += gridDim.x;
+            ptile = 0;
+            pn = prow < p.rows ? row_length(p, prow) : 0;
         }
+        if (prow >= p.rows) return;
+        ++issued;
+        const int cnt = min(kTile, pn - ptile * kTile);
+        const uint32_t bytes = (uint32_t)((cnt + 3) & ~3) * 4u;  // whole 16-byte groups: ld % 4 == 0 keeps it in the row
+        const uint32_t bar = ptx::smem_u32(&s.full[stage]);
+        ptx::mbar_arrive_expect_tx(bar, bytes);
+        ptx::bulk_g2s(ptx::smem_u32(s.ring[stage]), p.scores + (size_t)prow * (size_t)p.ld + (size_t)ptile * kTile,
+                      bytes, bar, policy);
+        ++ptile;
     };
-    if (ntiles > 0) load_tile(0, cur);
-    for (int t = 0; t < ntiles; ++t) {
-        if (t + 1 < ntiles) load_tile(t + 1, nxt);
+    if (tid == 0) {
+        for (int st = 0; st < kStages; ++st) ptx::mbar_init(ptx::smem_u32(&s.full[st]), 1);
+        ptx::fence_mbar_init();
+        s.failed = 0;
+    }
+    __syncthreads();
+    // Only thread 0 waits for a tile, just before a barrier: the barrier then releases everybody with
+    // the tile in shared memory (no other thread spins on the mbarrier).
+    auto wait_tile = [&](uint32_t gi) {
+        if (gi >= issued) return;
+        if (!s.failed && !ptx::mbar_wait(ptx::smem_u32(&s.full[gi % kStages]), (gi / kStages) & 1u)) {
+            s.failed = 1;
+            if (p.status) raise_status(p.status, RL_ERR_TIMEOUT);
+        }
+        if (!s.failed) landed = gi + 1u;
+    };
+    if (tid == 0) {
+        for (int st = 0; st < kStages; ++st) issue_next(st);
+        wait_tile(0u);
+    }
+
+    uint32_t g = 0;  // tiles consumed by this CTA
+    for (int row = blockIdx.x; row < p.rows; row += gridDim.x) {
+        const float *x = p.scores + (size_t)row * (size_t)p.ld;
+        const int nraw = p.lengths ? __ldg(p.lengths + row) : (int)p.ld;
+        if (tid == 0 && p.status && (nraw < 0 || nraw > p.ld)) raise_status(p.status, RL_ERR_SEQLENS);
+        const int n = row_length(p, row);
+        const int kk = min(k, n);
+        if (tid == 0) s.count = 0;
+        __syncthreads();
+        uint64_t bound = 0u;  // incoming scores are kept when key >= bound
+        float thr = -INFINITY;  // the same test on the score itself
+        int mode = 0;
+        const int ntiles = (n + kTile - 1) / kTile;
+        for (int t = 0; t < ntiles; ++t, ++g) {
+            const int st = (int)(g % kStages);
+            const float4 *tile4 = reinterpret_cast<const float4 *>(s.ring[st]);
+            // keep a score when its key reaches the bound: one float compare (NaN passes !(x < thr))
+            float vals[kPer];
+            uint32_t keepm = 0u;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int e = t * kTile + 4 * (j * kThreads + tid);
-            const float v4[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
+            for (int j = 0; j < kPer / 4; ++j) {
+                const float4 v = tile4[j * kThreads + tid];
+                vals[4 * j] = v.x, vals[4 * j + 1] = v.y, vals[4 * j + 2] = v.z, vals[4 * j + 3] = v.w;
+            }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t key = order_key(v4[u]);
-                const bool keep = e + u < n && (uint64_t)key >= bound;
-                const unsigned m = __ballot_sync(kFull, keep);
-                if (m) {
-                    int base = 0;
-                    if (lane == __ffs(m) - 1) base = atomicAdd(&s.count, __popc(m));
-                    base = __shfl_sync(kFull, base, __ffs(m) - 1);
-                    if (keep) {
-                        const int pos = base + __popc(m & ((1u << lane) - 1u));
-                        s.key[pos] = key;
-                        s.idx[pos] = (uint32_t)(e + u);
+            for (int q = 0; q < kPer; ++q) {
+                const int e = t * kTile + 4 * ((q >> 2) * kThreads + tid) + (q & 3);
+                const bool keep = e < n && (mode == 0 ? !(vals[q] < thr) : (mode == 1 && isnan(vals[q])));
+                keepm |= (uint32_t)keep << q;
+            }
+            if (__any_sync(kFull, keepm != 0u)) {
+                // one atomic per warp: an exclusive scan of the lanes' counts
+                const int c = __popc(keepm);
+                int incl = c;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int o = __shfl_up_sync(kFull, incl, off);
+                    if (lane >= off) incl += o;
+                }
+                int base = 0;
+                if (lane == 31) base = atomicAdd(&s.count, incl);
+                int pos = __shfl_sync(kFull, base, 31) + incl - c;
+#pragma unroll
+                for (int q = 0; q < kPer; ++q) {
+                    if ((keepm >> q) & 1u) {
+                        s.key[pos] = order_key(vals[q]);
+                        s.idx[pos] = (uint32_t)(t * kTile + 4 * ((q >> 2) * kThreads + tid) + (q & 3));
+                        ++pos;
                     }
                 }
             }
+            if (tid == 0) wait_tile(g + 1u);
+            __syncthreads();  // the stage is free again, the count is final and the next tile has landed
+            if (tid == 0) issue_next(st);
+            if (s.count > kCap - kTile) {
+                // compact well below the trigger, so that many tiles fit before the next one
+                bound = compact(s, k, k + (kCap - kTile - k) / 2, false, idx_bits);
+                set_threshold(bound, thr, mode);
+            }
+        }
+        // exactly the best min(k, n)
+        if (s.count > kk) compact(s, kk, kk, true, idx_bits);
+        // order them: pad to a power of two with entries that sort last
+        int n2 = 1;
+        while (n2 < kk) n2 <<= 1;
+        for (int i = kk + tid; i < n2; i += kThreads) {
+            s.key[i] = 0u;
+            s.idx[i] = 0xffffffffu;
         }
         __syncthreads();
-        if (s.count > kCap - kTile) bound = compact(s, k, kCap - kTile, false);
-        if (t + 1 < ntiles) {
-            cur[0] = nxt[0];
-            cur[1] = nxt[1];
+        if (kk > 1) bitonic(s, n2, p.order_by_score != 0);
+        int32_t *oi = p.out_idx + (size_t)row * (size_t)p.ldo;
+        float *ov = p.out_val ? p.out_val + (size_t)row * (size_t)p.ldo : nullptr;
+        for (int i = tid; i < k; i += kThreads) {
+            if (i < kk) {
+                const uint32_t key = s.key[i], ix = s.idx[i];
+                oi[i] = (int32_t)ix;
+                if (ov) {
+                    // the score back from its key; -0 and NaN payloads were folded, so those are re-read
+                    const uint32_t bits = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
+                    ov[i] = (bits == 0u || key == 0xffffffffu) ? __ldg(x + ix) : __uint_as_float(bits);
+                }
+            } else {
+                oi[i] = -1;
+                if (ov) ov[i] = -INFINITY;
+            }
         }
+        __syncthreads();  // the buffer is reused by the next row
     }
-    // exactly the best min(k, n)
-    if (s.count > kk) compact(s, kk, kk, true);
-    // order them: pad to a power of two with entries that sort last
-    int n2 = 1;
-    while (n2 < kk) n2 <<= 1;
-    for (int i = kk + tid; i < n2; i += kThreads) {
-        s.key[i] = 0u;
-        s.idx[i] = 0xffffffffu;
-    }
-    __syncthreads();
-    if (kk > 1) bitonic(s, n2, p.order_by_score != 0);
-    int32_t *oi = p.out_idx + (size_t)row * (size_t)p.ldo;
-    float *ov = p.out_val ? p.out_val + (size_t)row * (size_t)p.ldo : nullptr;
-    for (int i = tid; i < k; i += kThreads) {
-        if (i < kk) {
-            const uint32_t ix = s.idx[i];
-            oi[i] = (int32_t)ix;
-            if (ov) ov[i] = __ldg(x + ix);
-        } else {
-            oi[i] = -1;
-            if (ov) ov[i] = -INFINITY;
-        }
+    // after a timeout: let the copies that may still be in flight land before the CTA leaves (bounded)
+    if (tid == 0 && s.failed) {
+        for (uint32_t gi = landed; gi < issued; ++gi)
+            ptx::mbar_wait(ptx::smem_u32(&s.full[gi % kStages]), (gi / kStages) & 1u, 100000000ull);
     }
 }
 
@@ -299,16 +406,19 @@ int topk_max_k() { return kCap - kTile; }
 
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t stream) {
     if (p.rows <= 0) return cudaSuccess;
-    static int configured_dev = -1;
+    static int configured_dev = -1, sms = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_dev != dev) {
         e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(TopkSmem));
         if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    topk_kernel<<<p.rows, kThreads, sizeof(TopkSmem), stream>>>(p);
+    const int grid = std::min(p.rows, 2 * sms);  // persistent: two CTAs per SM
+    topk_kernel<<<grid, kThreads, sizeof(TopkSmem), stream>>>(p);
     return cudaGetLastError();
 }
 
