@@ -72,13 +72,17 @@ def measured_peaks(key: str = "hbm_gbs"):
 KERNEL_SOURCES = {
     "row_loss": ["row_loss.cu", "common.cuh"],
     "proj_gemm": ["proj_gemm.cu", "proj.cuh", "ptx.cuh", "common.cuh"],
+    "gae": ["gae.cu", "common.cuh"],
+    "topk": ["topk.cu", "ptx.cuh", "common.cuh"],
 }
 
 
-def kernel_traffic(kernel: str, case_id: int):
+def kernel_traffic(kernel: str, case_id):
     """Per-launch DRAM bytes of ``kernel`` from the committed ncu summary, or
-    None when that summary was taken on another version of the kernel source."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_case{case_id}.md")
+    None when that summary was taken on another version of the kernel source.
+    ``case_id``: a loss case number, or the name of a profile's workload."""
+    name = f"{kernel}_case{case_id}.md" if isinstance(case_id, int) else f"{kernel}_{case_id}.md"
+    path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -656,7 +660,7 @@ def main_gae(args):
                                  % (T * 9 / 1e6, T * 4 / 1e6)},
                 "roofline": {"bound": "hbm", "kernel": "gae", "achieved": achieved, "peak": peak,
                              "peak_kind": f"{kind} copy bandwidth", "unit": "GB/s", "frac": achieved / peak,
-                             "traffic": None, "algorithmic_bytes_per_launch": T * bytes_per_token,
+                             "traffic": kernel_traffic("gae", "256x65536"), "algorithmic_bytes_per_launch": T * bytes_per_token,
                              "avg_launch_ms": ms / args.steps},
                 "clocks": clocks,
                 "e2e": {"value": replica_throughput(T, 1, world, e2e_ms), "unit": "tokens/s",
@@ -767,7 +771,7 @@ def main_topk(args):
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": _topk_config(b),
                 "roofline": {"bound": "hbm", "kernel": "topk", "achieved": achieved, "peak": peak,
                              "peak_kind": f"{kind} copy bandwidth", "unit": "GB/s", "frac": achieved / peak,
-                             "traffic": None, "algorithmic_bytes_per_launch": bytes_per_launch,
+                             "traffic": kernel_traffic("topk", "4096x202752"), "algorithmic_bytes_per_launch": bytes_per_launch,
                              "avg_launch_ms": ms / args.steps},
                 "clocks": clocks,
                 "e2e": {"value": replica_throughput(b.rows, 1, world, e2e_ms), "unit": "rows/s",
