@@ -47,6 +47,7 @@ def parse_args():
                     help="use only the first P prompts' responses (small profiling runs); 0 = the whole case")
     ap.add_argument("--max-len", type=int, default=0, help="cap every response length (small profiling runs)")
     ap.add_argument("--vocab", type=int, default=0, help="case 4: vocabulary override (small profiling runs)")
+    ap.add_argument("--rows", type=int, default=0, help="topk: query rows override (small profiling runs)")
     return ap.parse_args()
 
 
@@ -72,8 +73,8 @@ def measured_peaks(key: str = "hbm_gbs"):
 KERNEL_SOURCES = {
     "row_loss": ["row_loss.cu", "common.cuh"],
     "proj_gemm": ["proj_gemm.cu", "proj.cuh", "ptx.cuh", "common.cuh"],
-    "gae": ["gae.cu", "common.cuh"],
-    "topk": ["topk.cu", "ptx.cuh", "common.cuh"],
+    "gae": ["gae.cu", "scan_select.cuh", "common.cuh"],
+    "topk": ["topk.cu", "scan_select.cuh", "ptx.cuh", "common.cuh"],
 }
 
 
@@ -735,7 +736,7 @@ def main_topk(args):
         return 0
     from rl_post_loss_gb300 import capi
     capi.load()
-    b = synthetic.make_topk_batch("cuda", seed=rank)
+    b = synthetic.make_topk_batch("cuda", seed=rank, **({"rows": args.rows} if args.rows else {}))
     out_idx = torch.empty((b.rows, b.k), dtype=torch.int32, device="cuda")
     out_val = torch.empty((b.rows, b.k), dtype=torch.float32, device="cuda")
     run = lambda: capi.topk(b.scores, b.k, lengths=b.lengths, out_idx=out_idx, out_val=out_val)

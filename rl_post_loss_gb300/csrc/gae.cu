@@ -36,6 +36,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "scan_select.cuh"
 
 namespace rlk {
 

@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "scan_select.cuh"
 
 #include "handle.cuh"
 

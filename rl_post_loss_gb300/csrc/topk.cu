@@ -26,6 +26,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "scan_select.cuh"
 #include "ptx.cuh"
 
 namespace rlk {
