@@ -72,7 +72,8 @@ typedef enum rl_status {
     RL_ERR_TIMEOUT = 10,      /* device bit: a bounded wait ran out */
     RL_ERR_UNSUPPORTED = 11,  /* valid request this build does not implement */
     RL_ERR_SEQLENS = 12,      /* device bit: cu_seqlens not monotone or not ending at num_tokens */
-    RL_ERR_DEVICE = 13        /* called with another CUDA device current than the handle's */
+    RL_ERR_DEVICE = 13,       /* called with another CUDA device current than the handle's */
+    RL_ERR_INTERNAL = 14      /* device bit: an internal consistency check failed; that result is invalid */
 } rl_status;
 
 typedef enum rl_dtype { RL_F32 = 0, RL_BF16 = 1 } rl_dtype;

@@ -25,7 +25,7 @@ RL_FLAG_POP_IN_BOUNDS, RL_FLAG_CLIP_ACTIVE, RL_FLAG_MASKED, RL_FLAG_BAD_TARGET =
 STATUS_NAMES = {0: "RL_OK", 1: "RL_ERR_INVALID_ARG", 2: "RL_ERR_SHAPE", 3: "RL_ERR_DTYPE",
                 4: "RL_ERR_ALIGNMENT", 5: "RL_ERR_CAPACITY", 6: "RL_ERR_CUDA", 7: "RL_ERR_TARGET_RANGE",
                 8: "RL_ERR_NONFINITE", 9: "RL_ERR_EMPTY_SEQ", 10: "RL_ERR_TIMEOUT", 11: "RL_ERR_UNSUPPORTED",
-                12: "RL_ERR_SEQLENS", 13: "RL_ERR_DEVICE"}
+                12: "RL_ERR_SEQLENS", 13: "RL_ERR_DEVICE", 14: "RL_ERR_INTERNAL"}
 CODES = {v: k for k, v in STATUS_NAMES.items()}
 
 

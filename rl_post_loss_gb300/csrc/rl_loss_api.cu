@@ -105,6 +105,7 @@ RL_LOSS_API const char *rl_loss_status_string(rl_status s) {
         case RL_ERR_UNSUPPORTED: return "unsupported request";
         case RL_ERR_SEQLENS: return "malformed cu_seqlens";
         case RL_ERR_DEVICE: return "handle used on another device";
+        case RL_ERR_INTERNAL: return "internal consistency check failed";
     }
     return "unknown status";
 }

@@ -61,6 +61,7 @@ struct TopkSmem {
     int found_bin;  // result of the last histogram search
     int found_before;
     int failed;     // a bounded wait ran out
+    int broken;     // an internal check failed (the row's result is invalid; no access left its array)
 };
 
 // hist[digit] += 1 for every lane with `valid`, one atomic per distinct digit of the warp (the
@@ -75,6 +76,7 @@ __device__ __forceinline__ void hist_add_warp(uint32_t *hist, uint32_t digit, bo
 // passed before it. Needs target <= total. Block-wide; ends with a barrier.
 __device__ void find_bin(TopkSmem &s, uint32_t target, bool from_top) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s.found_bin = -1;  // stays -1 if no bin reaches the target (a broken invariant)
     constexpr int per = kBins / kThreads;  // 4 bins per thread
     // thread t owns a run of 4 bins; in scan order, the runs go t = 0, 1, ... (from_top: highest bins first)
     const int base = from_top ? (kBins - per * (tid + 1)) : per * tid;
@@ -134,7 +136,8 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
         }
         __syncthreads();
         find_bin(s, (uint32_t)(target - above), true);
-        const uint32_t d = (uint32_t)s.found_bin;
+        if (s.found_bin < 0 && tid == 0) s.broken = 1;
+        const uint32_t d = (uint32_t)max(s.found_bin, 0);
         const int before = s.found_before;  // entries in the open range above the chosen digit
         const int in_bin = (int)s.hist[d];
         __syncthreads();
@@ -169,7 +172,8 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
                 }
                 __syncthreads();
                 find_bin(s, (uint32_t)(need - ibelow), false);
-                ipre = (ishift >= 32 ? 0u : (ipre << w)) | (uint32_t)s.found_bin;
+                if (s.found_bin < 0 && tid == 0) s.broken = 1;
+                ipre = (ishift >= 32 ? 0u : (ipre << w)) | (uint32_t)max(s.found_bin, 0);
                 ibelow += s.found_before;
                 ishift = sh;
                 __syncthreads();
@@ -201,7 +205,7 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
     int pos = atomicAdd(&s.count, __popc(keepm));
 #pragma unroll
     for (int j = 0; j < kMine; ++j) {
-        if ((keepm >> j) & 1u) {
+        if (((keepm >> j) & 1u) && pos < kCap) {
             s.key[pos] = mk[j];
             s.idx[pos] = mi[j];
             ++pos;
@@ -209,6 +213,109 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
     }
     __syncthreads();
     return resolved ? bound : (uint64_t)key_star + 1u;
+}
+
+// a comes before b in the output order
+__device__ __forceinline__ bool out_first(uint32_t ka, uint32_t ia, uint32_t kb, uint32_t ib, bool by_score) {
+    return by_score ? (ka > kb || (ka == kb && ia < ib)) : (ia < ib);
+}
+
+// The same bitonic network for n2 = kThreads * E entries with E per thread in registers: strides
+// below E inside a thread, below 32 E by warp shuffles, and only the wider strides through shared
+// memory (one barrier each). Thread t holds entries [E t, E t + E).
+template <int E>
+__device__ void bitonic_regs(TopkSmem &s, bool by_score) {
+    constexpr int n2 = kThreads * E;
+    const int tid = threadIdx.x;
+    uint32_t k[E], ix[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        k[j] = s.key[E * tid + j];
+        ix[j] = s.idx[E * tid + j];
+    }
+    bool in_regs = true;
+#pragma unroll
+    for (int size = 2; size <= n2; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            if (stride >= 32 * E) {  // across warps: through shared memory
+                if (in_regs) {
+#pragma unroll
+                    for (int j = 0; j < E; ++j) {
+                        s.key[E * tid + j] = k[j];
+                        s.idx[E * tid + j] = ix[j];
+                    }
+                    in_regs = false;
+                }
+                __syncthreads();
+                for (int t = tid; t < n2 / 2; t += kThreads) {
+                    const int i = 2 * t - (t & (stride - 1));
+                    const int jj = i + stride;
+                    const bool up = (i & size) == 0;
+                    const uint32_t ka = s.key[i], kb = s.key[jj], ia = s.idx[i], ib = s.idx[jj];
+                    if (out_first(ka, ia, kb, ib, by_score) != up) {
+                        s.key[i] = kb;
+                        s.key[jj] = ka;
+                        s.idx[i] = ib;
+                        s.idx[jj] = ia;
+                    }
+                }
+                continue;
+            }
+            if (!in_regs) {
+                __syncthreads();
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    k[j] = s.key[E * tid + j];
+                    ix[j] = s.idx[E * tid + j];
+                }
+                in_regs = true;
+            }
+            if (stride >= E) {  // across lanes of the warp
+                const int lmask = stride / E;
+                const bool lower = ((tid & 31) & lmask) == 0;
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    const uint32_t ok = __shfl_xor_sync(kFull, k[j], lmask);
+                    const uint32_t oi = __shfl_xor_sync(kFull, ix[j], lmask);
+                    const int i = E * tid + j;
+                    const bool up = (i & size) == 0;
+                    // the lower position keeps the entry that comes first in a rising run
+                    const bool mine_first = out_first(k[j], ix[j], ok, oi, by_score);
+                    const bool keep_mine = (lower == up) ? mine_first : !mine_first;
+                    if (!keep_mine) {
+                        k[j] = ok;
+                        ix[j] = oi;
+                    }
+                }
+            } else {  // inside the thread
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    const int jp = j ^ stride;
+                    if (jp > j) {
+                        const int i = E * tid + j;
+                        const bool up = (i & size) == 0;
+                        if (out_first(k[j], ix[j], k[jp], ix[jp], by_score) != up) {
+                            const uint32_t tk = k[j], ti = ix[j];
+                            k[j] = k[jp];
+                            ix[j] = ix[jp];
+                            k[jp] = tk;
+                            ix[jp] = ti;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    if (!in_regs) __syncthreads();
+    else {
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+            s.key[E * tid + j] = k[j];
+            s.idx[E * tid + j] = ix[j];
+        }
+    }
+    __syncthreads();
 }
 
 // Bitonic sort of s.key/s.idx[0..n2) (n2 a power of two): by (key desc, idx asc) or by idx asc.
@@ -288,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
         for (int st = 0; st < kStages; ++st) ptx::mbar_init(ptx::smem_u32(&s.full[st]), 1);
         ptx::fence_mbar_init();
         s.failed = 0;
+        s.broken = 0;
     }
     __syncthreads();
     // Only thread 0 waits for a tile, just before a barrier: the barrier then releases everybody with
@@ -349,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
                 int pos = __shfl_sync(kFull, base, 31) + incl - c;
 #pragma unroll
                 for (int q = 0; q < kPer; ++q) {
-                    if ((keepm >> q) & 1u) {
+                    if (((keepm >> q) & 1u) && pos < kCap) {
                         s.key[pos] = order_key(vals[q]);
                         s.idx[pos] = (uint32_t)(t * kTile + 4 * ((q >> 2) * kThreads + tid) + (q & 3));
                         ++pos;
@@ -375,7 +483,16 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
             s.idx[i] = 0xffffffffu;
         }
         __syncthreads();
-        if (kk > 1) bitonic(s, n2, p.order_by_score != 0);
+        if (n2 == 2 * kThreads)
+            bitonic_regs<2>(s, p.order_by_score != 0);
+        else if (n2 == 4 * kThreads)
+            bitonic_regs<4>(s, p.order_by_score != 0);
+        else if (kk > 1)
+            bitonic(s, n2, p.order_by_score != 0);
+        if (tid == 0 && (s.broken || s.count > kCap)) {
+            if (p.status) raise_status(p.status, RL_ERR_INTERNAL);
+            s.broken = 0;
+        }
         int32_t *oi = p.out_idx + (size_t)row * (size_t)p.ldo;
         float *ov = p.out_val ? p.out_val + (size_t)row * (size_t)p.ldo : nullptr;
         for (int i = tid; i < k; i += kThreads) {
@@ -385,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
                 if (ov) {
                     // the score back from its key; -0 and NaN payloads were folded, so those are re-read
                     const uint32_t bits = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
-                    ov[i] = (bits == 0u || key == 0xffffffffu) ? __ldg(x + ix) : __uint_as_float(bits);
+                    ov[i] = ((bits == 0u || key == 0xffffffffu) && ix < (uint32_t)n) ? __ldg(x + ix) : __uint_as_float(bits);
                 }
             } else {
                 oi[i] = -1;

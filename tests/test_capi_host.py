@@ -71,7 +71,7 @@ int main(void) {
 def test_host_only_entry_points(lib):
     assert capi.rl_loss_version() >= 100
     assert capi.rl_loss_status_string(0) == "ok"
-    for code in range(1, 14):
+    for code in range(1, 15):
         assert capi.rl_loss_status_string(code) not in ("", "unknown status")
     assert capi.rl_loss_status_string(99) == "unknown status"
     assert set(capi.STATUS_NAMES.values()) >= {"RL_OK", "RL_ERR_SEQLENS"}
