@@ -11,6 +11,8 @@
 //           stays one read and one write per element).
 // Rows with g == 0 (masked, popped, clipped, zero advantage) are written as
 // +0.0 without evaluating the softmax a second time.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace rlk {
@@ -22,7 +24,10 @@ namespace {
 // 1024-thread blocks and evict-first loads in the second pass and evict-first
 // stores, so the dlogits stream does not push rows awaiting their second read
 // out of L2. Chosen from GB300 sweeps over 256/512/1024 threads and both hints.
+// Long rows also keep their first kStageBytes in shared memory from the first
+// pass to the second (two blocks per SM), which shrinks what must stay in L2.
 constexpr size_t kShortRowBytes = 128 * 1024;
+constexpr int kStageBytes = 96 * 1024;
 
 template <typename T, bool CS>
 struct VecTraits;
@@ -85,6 +90,19 @@ struct VecTraits<__nv_bfloat16, CS> {
     }
 };
 
+// One 16-byte group of logits as floats.
+template <typename T>
+__device__ __forceinline__ void decode16(const uint4 &v, float (&x)[16 / sizeof(T)]);
+template <>
+__device__ __forceinline__ void decode16<float>(const uint4 &v, float (&x)[4]) {
+    x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y); x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+}
+template <>
+__device__ __forceinline__ void decode16<__nv_bfloat16>(const uint4 &v, float (&x)[8]) {
+    x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+    x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+}
+
 // Fold a group of values into running base-2 statistics (one rescale per group).
 template <int N>
 __device__ __forceinline__ void accumulate(RowStats2 &st, const float (&x)[N]) {
@@ -110,10 +128,13 @@ __device__ __forceinline__ void accumulate(RowStats2 &st, const float (&x)[N]) {
     }
 }
 
-template <typename T, int kRowThreads, bool CS>
-__global__ void __launch_bounds__(kRowThreads) row_loss_twopass_kernel(RowParams p) {
+// kStage: the first stage_vecs 16-byte groups of the row are kept in shared memory between the
+// passes (each thread re-reads only the groups it wrote).
+template <typename T, int kRowThreads, bool CS, bool kStage>
+__global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twopass_kernel(RowParams p, int stage_vecs) {
     using VT = VecTraits<T, CS>;
     constexpr int VEC = VT::kElems;
+    extern __shared__ uint4 s_row[];
     __shared__ RowStats2 warp_stats[kRowThreads / 32];
     __shared__ float s_logZ2, s_g;
     __shared__ uint32_t s_y;
@@ -130,7 +151,13 @@ __global__ void __launch_bounds__(kRowThreads) row_loss_twopass_kernel(RowParams
     RowStats2 st = empty_stats();
     for (int k = threadIdx.x; k < nvec; k += kRowThreads) {
         float x[VEC];
-        VT::load(z + (size_t)k * 16, x);
+        if (kStage && k < stage_vecs) {
+            const uint4 raw = __ldcs(reinterpret_cast<const uint4 *>(z + (size_t)k * 16));  // not needed in L2 again
+            s_row[k] = raw;
+            decode16<T>(raw, x);
+        } else {
+            VT::load(z + (size_t)k * 16, x);
+        }
         accumulate(st, x);
     }
     if (tail0 + (int)threadIdx.x < V) {
@@ -171,7 +198,10 @@ __global__ void __launch_bounds__(kRowThreads) row_loss_twopass_kernel(RowParams
     const int y = (int)s_y;  // g != 0 implies a valid target
     for (int k = threadIdx.x; k < nvec; k += kRowThreads) {
         float x[VEC];
-        VT::load_last(z + (size_t)k * 16, x);
+        if (kStage && k < stage_vecs)
+            decode16<T>(s_row[k], x);
+        else
+            VT::load_last(z + (size_t)k * 16, x);
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
             const float pr = ex2_approx(fmaf(x[j], kLog2e, nlz2));
@@ -188,10 +218,23 @@ __global__ void __launch_bounds__(kRowThreads) row_loss_twopass_kernel(RowParams
 
 template <typename T>
 cudaError_t launch_for(const RowParams &p, cudaStream_t stream) {
-    if ((size_t)p.vocab * sizeof(T) <= kShortRowBytes)
-        row_loss_twopass_kernel<T, 512, false><<<p.num_tokens, 512, 0, stream>>>(p);
-    else
-        row_loss_twopass_kernel<T, 1024, true><<<p.num_tokens, 1024, 0, stream>>>(p);
+    if ((size_t)p.vocab * sizeof(T) <= kShortRowBytes) {
+        row_loss_twopass_kernel<T, 512, false, false><<<p.num_tokens, 512, 0, stream>>>(p, 0);
+        return cudaGetLastError();
+    }
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_dev != dev) {
+        e = cudaFuncSetAttribute(row_loss_twopass_kernel<T, 1024, true, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
+        if (e != cudaSuccess) return e;
+        configured_dev = dev;
+    }
+    const int nvec = p.vocab / (16 / (int)sizeof(T));
+    const int stage_vecs = std::min(nvec, kStageBytes / 16);
+    row_loss_twopass_kernel<T, 1024, true, true><<<p.num_tokens, 1024, (size_t)stage_vecs * 16, stream>>>(p, stage_vecs);
     return cudaGetLastError();
 }
 
