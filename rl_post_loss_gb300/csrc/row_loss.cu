@@ -149,6 +149,7 @@ __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twop
     const uint32_t meta = __ldg(p.meta + row);
 
     RowStats2 st = empty_stats();
+#pragma unroll 4  // several 16-byte loads in flight per thread
     for (int k = threadIdx.x; k < nvec; k += kRowThreads) {
         float x[VEC];
         if (kStage && k < stage_vecs) {
@@ -196,6 +197,7 @@ __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twop
     const float nlz2 = -s_logZ2;
     const float c = -g;
     const int y = (int)s_y;  // g != 0 implies a valid target
+#pragma unroll 4
     for (int k = threadIdx.x; k < nvec; k += kRowThreads) {
         float x[VEC];
         if (kStage && k < stage_vecs)
