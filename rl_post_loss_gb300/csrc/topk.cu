@@ -114,24 +114,48 @@ __device__ void find_bin(TopkSmem &s, uint32_t target, bool from_top) {
 // least `target` of them and at most `limit`. Returns the new lower bound for incoming scores
 // (as a 64-bit value: 2^32 admits nothing). Block-wide.
 __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int idx_bits) {
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cnt = s.count;
+    // Every key shares the bits above the highest bit where the smallest and the largest differ
+    // (after the first compaction they all lie above the bound), so the radix starts below them.
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (int i = tid; i < cnt; i += kThreads) {
+        const uint32_t k = s.key[i];
+        kmin = min(kmin, k);
+        kmax = max(kmax, k);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(kFull, kmin, off));
+        kmax = max(kmax, __shfl_xor_sync(kFull, kmax, off));
+    }
+    if (lane == 0) {
+        s.hist[warp] = kmin;
+        s.hist[kThreads / 32 + warp] = kmax;
+    }
+    __syncthreads();
+    for (int w = 0; w < kThreads / 32; ++w) {
+        kmin = min(kmin, s.hist[w]);
+        kmax = max(kmax, s.hist[kThreads / 32 + w]);
+    }
+    __syncthreads();
+    const uint32_t diff = kmin ^ kmax;
     // the key prefix fixed so far, and how many buffer entries lie strictly above it
-    uint32_t prefix = 0u;
+    int shift = diff ? 32 - __clz(diff) : 0;  // bits of the key still open: the prefix covers key >> shift
+    uint32_t prefix = shift >= 32 ? 0u : (kmax >> shift);
     int above = 0;
-    int shift = 32;  // bits of the key still open: the prefix covers key >> shift
     int kept = cnt;
-    uint64_t bound = 0u;
+    uint64_t bound = shift >= 32 ? 0u : ((uint64_t)prefix << shift);
     bool resolved = false;
-    for (int level = 0; level < 3 && !resolved; ++level) {
-        const int w = level == 2 ? 10 : 11;
+    while (shift > 0 && !resolved) {
+        const int w = min(11, shift);
         const int sh = shift - w;
         for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0u;
         __syncthreads();
         for (int i0 = tid & ~31; i0 < cnt; i0 += kThreads) {  // warp-uniform trip count
             const int i = i0 + (tid & 31);
             const uint32_t k = i < cnt ? s.key[i] : 0u;
-            const bool in = i < cnt && (shift == 32 || (k >> shift) == prefix);
+            const bool in = i < cnt && (shift >= 32 || (k >> shift) == prefix);
             hist_add_warp(s.hist, (k >> sh) & ((1u << w) - 1u), in);
         }
         __syncthreads();
@@ -141,7 +165,7 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
         const int before = s.found_before;  // entries in the open range above the chosen digit
         const int in_bin = (int)s.hist[d];
         __syncthreads();
-        prefix = (shift == 32 ? 0u : (prefix << w)) | d;
+        prefix = (shift >= 32 ? 0u : (prefix << w)) | d;
         above += before;
         shift = sh;
         kept = above + in_bin;  // everything at or above this prefix
@@ -437,12 +461,18 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
                 const float4 v = tile4[j * kThreads + tid];
                 vals[4 * j] = v.x, vals[4 * j + 1] = v.y, vals[4 * j + 2] = v.z, vals[4 * j + 3] = v.w;
             }
+            if (mode == 0 && (t + 1) * kTile <= n) {  // a full tile and a plain threshold: one compare per score
 #pragma unroll
-            for (int q = 0; q < kPer; ++q) {
-                const int e = t * kTile + 4 * ((q >> 2) * kThreads + tid) + (q & 3);
-                const bool keep = e < n && (mode == 0 ? !(vals[q] < thr) : (mode == 1 && isnan(vals[q])));
-                keepm |= (uint32_t)keep << q;
+                for (int q = 0; q < kPer; ++q) keepm |= (uint32_t)!(vals[q] < thr) << q;
+            } else {
+#pragma unroll
+                for (int q = 0; q < kPer; ++q) {
+                    const int e = t * kTile + 4 * ((q >> 2) * kThreads + tid) + (q & 3);
+                    const bool keep = e < n && (mode == 0 ? !(vals[q] < thr) : (mode == 1 && isnan(vals[q])));
+                    keepm |= (uint32_t)keep << q;
+                }
             }
+            int after_add = 0;  // the buffer count right after this warp's append
             if (__any_sync(kFull, keepm != 0u)) {
                 // one atomic per warp: an exclusive scan of the lanes' counts
                 const int c = __popc(keepm);
@@ -454,7 +484,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
                 }
                 int base = 0;
                 if (lane == 31) base = atomicAdd(&s.count, incl);
-                int pos = __shfl_sync(kFull, base, 31) + incl - c;
+                base = __shfl_sync(kFull, base, 31);
+                after_add = base + __shfl_sync(kFull, incl, 31);
+                int pos = base + incl - c;
 #pragma unroll
                 for (int q = 0; q < kPer; ++q) {
                     if (((keepm >> q) & 1u) && pos < kCap) {
@@ -465,9 +497,13 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
                 }
             }
             if (tid == 0) wait_tile(g + 1u);
-            __syncthreads();  // the stage is free again, the count is final and the next tile has landed
+            // The stage is free again and the next tile has landed. Whether to compact is decided by
+            // the barrier itself (the count passed the trigger iff some warp's append took it past):
+            // a thread must not read s.count here, because a faster warp may already be appending
+            // the next tile.
+            const bool over = __syncthreads_or(after_add > kCap - kTile) != 0;
             if (tid == 0) issue_next(st);
-            if (s.count > kCap - kTile) {
+            if (over) {
                 // compact well below the trigger, so that many tiles fit before the next one
                 bound = compact(s, k, k + (kCap - kTile - k) / 2, false, idx_bits);
                 set_threshold(bound, thr, mode);
