@@ -24,6 +24,7 @@
 // copies (TMA) into a shared-memory ring, completing on mbarriers whose waits
 // are bounded, and runs ahead into the next row while this one is finished.
 #include <algorithm>
+#include <climits>
 
 #include "common.cuh"
 #include "scan_select.cuh"
@@ -36,10 +37,19 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kPer = 8;                 // scores per thread per tile (two float4)
 constexpr int kTile = kThreads * kPer;  // 4096
-constexpr int kCap = 8192;              // buffer entries
+constexpr int kCap = 5120;              // buffer entries
+constexpr int kSlice = 512;             // positions per slice of a tile that overflowed the buffer
+constexpr int kSoft = kCap - kSlice;    // a count above this compacts after the tile
 constexpr int kBins = 2048;
-constexpr int kStages = 2;              // tiles in flight per CTA (16 KB each)
+constexpr int kStages = 4;              // tiles in flight per CTA (16 KB each)
 constexpr unsigned kFull = 0xffffffffu;
+// The sampled starting bound: 16 runs of 512 scores spread evenly over the row.
+constexpr int kSampleRuns = 16;
+constexpr int kSampleRun = 512;
+constexpr int kSample = kSampleRuns * kSampleRun;  // 8192 keys, held in the (still empty) buffer's storage
+constexpr int kSampleMinLen = 4 * kTile;           // shorter rows start from -inf
+static_assert(kSample <= 2 * kCap, "the sample is held in the candidate buffer's storage");
+static_assert(kTile == 8 * kSlice && kThreads == 4 * (kSlice / 4), "a slice is a quarter of the threads' first or second float4");
 
 // Unsigned order = score order; NaN above +inf; -0 folded onto +0. Every number maps to >= 0x007fffff,
 // so key 0 is free for padding.
@@ -50,14 +60,25 @@ __device__ __forceinline__ uint32_t order_key(float x) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-struct TopkSmem {
-    float ring[kStages][kTile];  // tiles of scores, filled by bulk copies
+// Entries [0, keyed) hold order keys; entries appended since the last compaction hold the raw
+// score bits until the next compaction (or the final selection) turns them into keys.
+struct Candidates {
     uint32_t key[kCap];
     uint32_t idx[kCap];
+};
+
+struct TopkSmem {
+    float ring[kStages][kTile];  // tiles of scores, filled by bulk copies
+    union {
+        Candidates cb;              // the candidate buffer
+        uint32_t sample[kSample];   // at the start of a row: the sampled keys
+    };
     uint32_t hist[kBins];
     unsigned long long full[kStages];  // mbarriers: a tile has landed
     uint32_t warp_tot[kThreads / 32];
+    int warp_base[kThreads / 32];      // where each warp's append of the current tile started (INT_MAX: none)
     int count;      // entries in the buffer
+    int keyed;      // leading entries that already hold order keys
     int found_bin;  // result of the last histogram search
     int found_before;
     int failed;     // a bounded wait ran out
@@ -109,52 +130,77 @@ __device__ void find_bin(TopkSmem &s, uint32_t target, bool from_top) {
     __syncthreads();
 }
 
-// Reduces the buffer to its best entries. With `exact`, keeps exactly `target` entries (the first
-// `target` in the total order); otherwise keeps the entries whose key reaches a lower bound, at
-// least `target` of them and at most `limit`. Returns the new lower bound for incoming scores
-// (as a 64-bit value: 2^32 admits nothing). Block-wide.
-__device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int idx_bits) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Turns the raw scores appended since the last compaction into order keys. Block-wide; ends with
+// a barrier, so every thread sees the new `keyed` before it can call this again.
+__device__ void make_keys(TopkSmem &s) {
     const int cnt = s.count;
+    for (int i = s.keyed + (int)threadIdx.x; i < cnt; i += kThreads) s.cb.key[i] = order_key(__uint_as_float(s.cb.key[i]));
+    __syncthreads();
+    if (threadIdx.x == 0) s.keyed = cnt;
+    __syncthreads();
+}
+
+// The outcome of a radix descent over the first `cnt` buffer keys.
+struct Descent {
+    uint32_t prefix;  // the key bits fixed so far (key >> shift)
+    int shift;        // key bits still open
+    int above;        // entries whose key lies strictly above the prefix
+    int kept;         // entries at or above the prefix
+    bool resolved;    // the stopping rule was met before every bit was fixed
+};
+
+// Fixes the key from the top, up to 11 bits at a time, over the bits where the keys differ (below
+// the common prefix of the smallest and the largest key, above the lowest bit that is not the same
+// in every key), until at least `target` keys lie at or above the fixed prefix and, with `exact`,
+// exactly `target`, otherwise at most `limit`; or until every bit is fixed (then `kept` may
+// exceed the rule by keys equal to the prefix). Needs target <= cnt. Block-wide.
+__device__ Descent radix_descent(TopkSmem &s, const uint32_t *keys, int cnt, int target, int limit, bool exact) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // Every key shares the bits above the highest bit where the smallest and the largest differ
     // (after the first compaction they all lie above the bound), so the radix starts below them.
-    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    // the smallest and the largest key, and the bits in which any key differs from the first one
+    const uint32_t k0 = cnt > 0 ? keys[0] : 0u;
+    uint32_t kmin = 0xffffffffu, kmax = 0u, vary = 0u;
     for (int i = tid; i < cnt; i += kThreads) {
-        const uint32_t k = s.key[i];
+        const uint32_t k = keys[i];
         kmin = min(kmin, k);
         kmax = max(kmax, k);
+        vary |= k ^ k0;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         kmin = min(kmin, __shfl_xor_sync(kFull, kmin, off));
         kmax = max(kmax, __shfl_xor_sync(kFull, kmax, off));
+        vary |= __shfl_xor_sync(kFull, vary, off);
     }
     if (lane == 0) {
         s.hist[warp] = kmin;
         s.hist[kThreads / 32 + warp] = kmax;
+        s.hist[2 * (kThreads / 32) + warp] = vary;
     }
     __syncthreads();
     for (int w = 0; w < kThreads / 32; ++w) {
         kmin = min(kmin, s.hist[w]);
         kmax = max(kmax, s.hist[kThreads / 32 + w]);
+        vary |= s.hist[2 * (kThreads / 32) + w];
     }
     __syncthreads();
+    const int low = vary ? __ffs(vary) - 1 : 32;  // bits below `low` are the same in every key
     const uint32_t diff = kmin ^ kmax;
     // the key prefix fixed so far, and how many buffer entries lie strictly above it
     int shift = diff ? 32 - __clz(diff) : 0;  // bits of the key still open: the prefix covers key >> shift
     uint32_t prefix = shift >= 32 ? 0u : (kmax >> shift);
     int above = 0;
     int kept = cnt;
-    uint64_t bound = shift >= 32 ? 0u : ((uint64_t)prefix << shift);
-    bool resolved = false;
-    while (shift > 0 && !resolved) {
-        const int w = min(11, shift);
+    bool resolved = exact ? kept == target : kept <= limit;
+    while (shift > low && !resolved) {
+        const int w = min(11, shift - low);
         const int sh = shift - w;
         for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0u;
         __syncthreads();
         for (int i0 = tid & ~31; i0 < cnt; i0 += kThreads) {  // warp-uniform trip count
             const int i = i0 + (tid & 31);
-            const uint32_t k = i < cnt ? s.key[i] : 0u;
+            const uint32_t k = i < cnt ? keys[i] : 0u;
             const bool in = i < cnt && (shift >= 32 || (k >> shift) == prefix);
             hist_add_warp(s.hist, (k >> sh) & ((1u << w) - 1u), in);
         }
@@ -169,11 +215,30 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
         above += before;
         shift = sh;
         kept = above + in_bin;  // everything at or above this prefix
-        bound = (uint64_t)prefix << shift;
         if (!exact && kept <= limit) resolved = true;
         if (exact && kept == target) resolved = true;
     }
-    uint32_t key_star = prefix;  // when every level ran, the exact threshold key
+    if (!resolved && shift > 0) {  // only bits that every key shares are left: fix them too
+        prefix = (prefix << shift) | (kmax & ((1u << shift) - 1u));
+        shift = 0;
+    }
+    return Descent{prefix, shift, above, kept, resolved};
+}
+
+// Reduces the buffer to its best entries. With `exact`, keeps exactly `target` entries (the first
+// `target` in the total order); otherwise keeps the entries whose key reaches a lower bound, at
+// least `target` of them and at most `limit`. Returns the new lower bound for incoming scores
+// (as a 64-bit value: 2^32 admits nothing). Block-wide.
+__device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int idx_bits) {
+    const int tid = threadIdx.x;
+    make_keys(s);
+    const int cnt = s.count;
+    const Descent dsc = radix_descent(s, s.cb.key, cnt, target, limit, exact);
+    const bool resolved = dsc.resolved;
+    const int above = dsc.above;
+    int kept = dsc.kept;
+    uint64_t bound = (uint64_t)dsc.prefix << dsc.shift;
+    uint32_t key_star = dsc.prefix;  // when every level ran, the exact threshold key
     uint32_t idx_star = 0u;
     if (!resolved) {
         // all 32 bits fixed: key_star is the key of the target-th entry; `above` entries are larger
@@ -189,8 +254,8 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
                 __syncthreads();
                 for (int i0 = tid & ~31; i0 < cnt; i0 += kThreads) {
                     const int i = i0 + (tid & 31);
-                    const bool eq = i < cnt && s.key[i] == key_star;
-                    const uint32_t ix = eq ? s.idx[i] : 0u;
+                    const bool eq = i < cnt && s.cb.key[i] == key_star;
+                    const uint32_t ix = eq ? s.cb.idx[i] : 0u;
                     const bool in = eq && (ishift >= 32 || (ix >> ishift) == ipre);
                     hist_add_warp(s.hist, (ix >> sh) & ((1u << w) - 1u), in);
                 }
@@ -214,8 +279,8 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
 #pragma unroll
     for (int j = 0; j < kMine; ++j) {
         const int i = j * kThreads + tid;
-        mk[j] = i < cnt ? s.key[i] : 0u;
-        mi[j] = i < cnt ? s.idx[i] : 0u;
+        mk[j] = i < cnt ? s.cb.key[i] : 0u;
+        mi[j] = i < cnt ? s.cb.idx[i] : 0u;
         bool keep;
         if (resolved)
             keep = (uint64_t)mk[j] >= bound;
@@ -230,12 +295,13 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
 #pragma unroll
     for (int j = 0; j < kMine; ++j) {
         if (((keepm >> j) & 1u) && pos < kCap) {
-            s.key[pos] = mk[j];
-            s.idx[pos] = mi[j];
+            s.cb.key[pos] = mk[j];
+            s.cb.idx[pos] = mi[j];
             ++pos;
         }
     }
     __syncthreads();
+    if (tid == 0) s.keyed = s.count;
     return resolved ? bound : (uint64_t)key_star + 1u;
 }
 
@@ -254,8 +320,8 @@ __device__ void bitonic_regs(TopkSmem &s, bool by_score) {
     uint32_t k[E], ix[E];
 #pragma unroll
     for (int j = 0; j < E; ++j) {
-        k[j] = s.key[E * tid + j];
-        ix[j] = s.idx[E * tid + j];
+        k[j] = s.cb.key[E * tid + j];
+        ix[j] = s.cb.idx[E * tid + j];
     }
     bool in_regs = true;
 #pragma unroll
@@ -266,8 +332,8 @@ __device__ void bitonic_regs(TopkSmem &s, bool by_score) {
                 if (in_regs) {
 #pragma unroll
                     for (int j = 0; j < E; ++j) {
-                        s.key[E * tid + j] = k[j];
-                        s.idx[E * tid + j] = ix[j];
+                        s.cb.key[E * tid + j] = k[j];
+                        s.cb.idx[E * tid + j] = ix[j];
                     }
                     in_regs = false;
                 }
@@ -276,12 +342,12 @@ __device__ void bitonic_regs(TopkSmem &s, bool by_score) {
                     const int i = 2 * t - (t & (stride - 1));
                     const int jj = i + stride;
                     const bool up = (i & size) == 0;
-                    const uint32_t ka = s.key[i], kb = s.key[jj], ia = s.idx[i], ib = s.idx[jj];
+                    const uint32_t ka = s.cb.key[i], kb = s.cb.key[jj], ia = s.cb.idx[i], ib = s.cb.idx[jj];
                     if (out_first(ka, ia, kb, ib, by_score) != up) {
-                        s.key[i] = kb;
-                        s.key[jj] = ka;
-                        s.idx[i] = ib;
-                        s.idx[jj] = ia;
+                        s.cb.key[i] = kb;
+                        s.cb.key[jj] = ka;
+                        s.cb.idx[i] = ib;
+                        s.cb.idx[jj] = ia;
                     }
                 }
                 continue;
@@ -290,8 +356,8 @@ __device__ void bitonic_regs(TopkSmem &s, bool by_score) {
                 __syncthreads();
 #pragma unroll
                 for (int j = 0; j < E; ++j) {
-                    k[j] = s.key[E * tid + j];
-                    ix[j] = s.idx[E * tid + j];
+                    k[j] = s.cb.key[E * tid + j];
+                    ix[j] = s.cb.idx[E * tid + j];
                 }
                 in_regs = true;
             }
@@ -335,14 +401,14 @@ __device__ void bitonic_regs(TopkSmem &s, bool by_score) {
     else {
 #pragma unroll
         for (int j = 0; j < E; ++j) {
-            s.key[E * tid + j] = k[j];
-            s.idx[E * tid + j] = ix[j];
+            s.cb.key[E * tid + j] = k[j];
+            s.cb.idx[E * tid + j] = ix[j];
         }
     }
     __syncthreads();
 }
 
-// Bitonic sort of s.key/s.idx[0..n2) (n2 a power of two): by (key desc, idx asc) or by idx asc.
+// Bitonic sort of s.key/s.cb.idx[0..n2) (n2 a power of two): by (key desc, idx asc) or by idx asc.
 __device__ void bitonic(TopkSmem &s, int n2, bool by_score) {
     const int tid = threadIdx.x;
     for (int size = 2; size <= n2; size <<= 1) {
@@ -351,13 +417,13 @@ __device__ void bitonic(TopkSmem &s, int n2, bool by_score) {
                 const int i = 2 * t - (t & (stride - 1));
                 const int j = i + stride;
                 const bool up = (i & size) == 0;  // this run ascends in the output order
-                const uint32_t ka = s.key[i], kb = s.key[j], ia = s.idx[i], ib = s.idx[j];
+                const uint32_t ka = s.cb.key[i], kb = s.cb.key[j], ia = s.cb.idx[i], ib = s.cb.idx[j];
                 const bool a_first = by_score ? (ka > kb || (ka == kb && ia < ib)) : (ia < ib);
                 if (a_first != up) {
-                    s.key[i] = kb;
-                    s.key[j] = ka;
-                    s.idx[i] = ib;
-                    s.idx[j] = ia;
+                    s.cb.key[i] = kb;
+                    s.cb.key[j] = ka;
+                    s.cb.idx[i] = ib;
+                    s.cb.idx[j] = ia;
                 }
             }
             __syncthreads();
@@ -384,6 +450,184 @@ __device__ __forceinline__ int row_length(const TopkParams &p, int r) {
     return min(max(n, 0), (int)p.ld);
 }
 
+// A position in this CTA's sequence of tiles: tile `tile` of row `row`, a row of n valid scores.
+struct TileCursor {
+    int row, tile, n;
+};
+
+// Moves the cursor past finished rows; false once this CTA has no tile left.
+__device__ __forceinline__ bool cursor_settle(const TopkParams &p, TileCursor &c) {
+    while (c.row < p.rows && c.tile * kTile >= c.n) {
+        c.row += gridDim.x;
+        c.tile = 0;
+        c.n = c.row < p.rows ? row_length(p, c.row) : 0;
+    }
+    return c.row < p.rows;
+}
+
+// The tile's first score and its length in bytes, rounded up to whole 16-byte groups (ld % 4 == 0
+// keeps them inside the row).
+__device__ __forceinline__ const float *cursor_src(const TopkParams &p, const TileCursor &c, uint32_t &bytes) {
+    const int cnt = min(kTile, c.n - c.tile * kTile);
+    bytes = (uint32_t)((cnt + 3) & ~3) * 4u;
+    return p.scores + (size_t)c.row * (size_t)p.ld + (size_t)c.tile * kTile;
+}
+
+// First score of sample run j of a row of n scores (n >= kSampleMinLen): runs spread evenly,
+// starting on a multiple of 4, inside the row and not overlapping.
+__device__ __forceinline__ int sample_run_start(int j, int n) {
+    return (int)(((long long)j * (n - kSampleRun) / (kSampleRuns - 1)) & ~3ll);
+}
+
+// Element of the row held by value q of this thread in tile t (two float4 per thread, 512 floats apart).
+__device__ __forceinline__ int tile_elem(int t, int q) {
+    return t * kTile + 4 * ((q >> 2) * kThreads + (int)threadIdx.x) + (q & 3);
+}
+
+// Appends this thread's scores of tile t whose key reaches the bound (the test on the score itself,
+// see set_threshold) to the buffer, one shared atomic per warp; with slice >= 0, only the scores at
+// the tile's positions [512 slice, 512 slice + 512). Entries that would land at kCap or beyond are
+// not written. Records where the warp's append started in warp_base and returns the buffer count
+// right after it (0 when the warp appends nothing).
+__device__ __forceinline__ int filter_append(TopkSmem &s, const float (&vals)[kPer], int t, int n, float thr,
+                                             int mode, int slice) {
+    const int lane = threadIdx.x & 31;
+    uint32_t keepm = 0u;
+    if (mode == 0 && (t + 1) * kTile <= n) {  // a full tile and a plain threshold: one compare per score
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) keepm |= (uint32_t)!(vals[q] < thr) << q;
+    } else {
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const bool keep = tile_elem(t, q) < n && (mode == 0 ? !(vals[q] < thr) : (mode == 1 && isnan(vals[q])));
+            keepm |= (uint32_t)keep << q;
+        }
+    }
+    if (slice >= 0)  // slice j: threads [128 (j % 4), +128), first (j < 4) or second float4
+        keepm &= ((int)threadIdx.x >> 7) == (slice & 3) ? (0x0fu << (4 * (slice >> 2))) : 0u;
+    if (!__any_sync(kFull, keepm != 0u)) {
+        if (lane == 0) s.warp_base[threadIdx.x >> 5] = INT_MAX;
+        return 0;
+    }
+    // an exclusive scan of the lanes' counts
+    const int c = __popc(keepm);
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += o;
+    }
+    const int total = __shfl_sync(kFull, incl, 31);
+    int base = 0;
+    if (lane == 31) base = atomicAdd(&s.count, total);
+    base = __shfl_sync(kFull, base, 31);
+    if (lane == 0) s.warp_base[threadIdx.x >> 5] = base;
+    int pos = base + incl - c;
+    const uint32_t e0 = (uint32_t)tile_elem(t, 0);  // value q sits at e0 + 2048 (q / 4) + q % 4
+    // raw score bits; the next compaction turns them into keys
+    if (base + total <= kCap) {  // the whole warp's append fits
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            if ((keepm >> q) & 1u) {
+                s.cb.key[pos] = __float_as_uint(vals[q]);
+                s.cb.idx[pos] = e0 + (uint32_t)(4 * kThreads * (q >> 2) + (q & 3));
+                ++pos;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            if (((keepm >> q) & 1u) && pos < kCap) {
+                s.cb.key[pos] = __float_as_uint(vals[q]);
+                s.cb.idx[pos] = e0 + (uint32_t)(4 * kThreads * (q >> 2) + (q & 3));
+                ++pos;
+            }
+        }
+    }
+    return base + total;
+}
+
+// This thread's kPer scores of tile t, read from `tile` (the tile's first score, in the ring or in
+// global memory); float4 groups that start at or beyond n are not read.
+__device__ __forceinline__ void load_tile_vals(const float *tile, int t, int n, float (&vals)[kPer]) {
+    const float4 *t4 = reinterpret_cast<const float4 *>(tile);
+#pragma unroll
+    for (int j = 0; j < kPer / 4; ++j) {
+        // a float4 that starts inside the row ends inside it too (ld is a multiple of 4)
+        const float4 v = tile_elem(t, 4 * j) < n ? t4[j * kThreads + threadIdx.x] : make_float4(0.f, 0.f, 0.f, 0.f);
+        vals[4 * j] = v.x, vals[4 * j + 1] = v.y, vals[4 * j + 2] = v.z, vals[4 * j + 3] = v.w;
+    }
+}
+
+// The rare path of a tile whose appends took the buffer past kSoft (block-wide, right after the
+// barrier that ends the tile's appends). If nothing was lost, the buffer is compacted. If some
+// entries did not fit (count beyond kCap), the tile's appends are undone (they start at the lowest
+// warp base) and the tile, read again from `tile`, is appended one slice of 512 positions at a time
+// in position order, with a compaction before any slice that might not fit. Every entry then
+// enters after all entries of lower position, as the compaction's tie rule assumes.
+__device__ void settle_tile(TopkSmem &s, const float *tile, int t, int n, int k, int idx_bits, bool overflow,
+                            float &thr, int &mode) {
+    const int limit = k + (kSoft - k) / 2;  // compact well below kSoft, so that many tiles fit after it
+    if (!overflow) {
+        set_threshold(compact(s, k, limit, false, idx_bits), thr, mode);
+        return;
+    }
+    int start = INT_MAX;
+    for (int w = 0; w < kThreads / 32; ++w) start = min(start, s.warp_base[w]);
+    __syncthreads();  // every thread has read warp_base
+    if (threadIdx.x == 0) s.count = start;
+    __syncthreads();
+    int cnt = start;
+    float vals[kPer];
+    load_tile_vals(tile, t, n, vals);
+    for (int j = 0; j < kTile / kSlice; ++j) {
+        if (cnt > kCap - kSlice) {
+            set_threshold(compact(s, k, limit, false, idx_bits), thr, mode);
+        }
+        filter_append(s, vals, t, n, thr, mode, j);
+        __syncthreads();
+        cnt = s.count;
+        __syncthreads();  // every thread has read the count before it changes again
+    }
+}
+
+// The sample rank r of the starting bound: with r0 = kk m / n the sample rank expected for the
+// row's kk-th best score (m = sample size), r solves r - 5 sqrt(r) = r0, so a row whose scores
+// are exchangeable holds fewer than kk keys at or above the bound only about 5 standard
+// deviations below the mean. Any outcome is correct (a row that falls short is scanned again);
+// r only trades that rescan against the number of compactions.
+__device__ __forceinline__ int sample_rank(int kk, int n) {
+    const float r0 = (float)kk * (float)kSample / (float)n;
+    const float sq = 0.5f * (5.0f + sqrtf(25.0f + 4.0f * r0));
+    return (int)ceilf(sq * sq);
+}
+
+// A starting lower bound for row x of n scores (n >= kSampleMinLen): a key with at least r of the
+// sampled keys at or above it. The sample is 16 runs of 512 consecutive scores, run j starting at
+// floor(j (n - 512) / 15) rounded down to a multiple of 4, so every run lies inside the row and
+// the runs do not overlap. Uses the buffer and the histogram (the buffer must be empty).
+__device__ uint64_t sampled_bound(TopkSmem &s, const float *x, int n, int r) {
+    constexpr int kRunVec = kSampleRun / 4;
+    const float4 *x4 = reinterpret_cast<const float4 *>(x);
+    float4 v[kSample / 4 / kThreads];
+#pragma unroll
+    for (int j = 0; j < kSample / 4 / kThreads; ++j) {
+        const int w = j * kThreads + (int)threadIdx.x;  // float4 of the sample
+        v[j] = __ldg(x4 + sample_run_start(w / kRunVec, n) / 4 + (w % kRunVec));
+    }
+#pragma unroll
+    for (int j = 0; j < kSample / 4 / kThreads; ++j) {
+        const int w = j * kThreads + (int)threadIdx.x;
+        s.sample[4 * w] = order_key(v[j].x);
+        s.sample[4 * w + 1] = order_key(v[j].y);
+        s.sample[4 * w + 2] = order_key(v[j].z);
+        s.sample[4 * w + 3] = order_key(v[j].w);
+    }
+    __syncthreads();
+    const Descent d = radix_descent(s, s.sample, kSample, r, r + r / 4, false);
+    return (uint64_t)d.prefix << d.shift;
+}
+
 // Persistent CTAs, each taking rows blockIdx.x, blockIdx.x + gridDim.x, ... Thread 0 keeps
 // kStages tiles of 4096 scores in flight (bulk copies into a shared-memory ring, one mbarrier
 // per stage), running ahead across row boundaries, and waits for each tile just before the
@@ -392,28 +636,21 @@ __device__ __forceinline__ int row_length(const TopkParams &p, int r) {
 __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     TopkSmem &s = *reinterpret_cast<TopkSmem *>(smem_raw);
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int k = p.k;
     const int idx_bits = p.ld <= (1 << 22) ? 22 : 32;
-    // producer cursor (thread 0): the next tile to copy
-    int prow = blockIdx.x, ptile = 0, pn = prow < p.rows ? row_length(p, prow) : 0;
+    // producer cursor (thread 0): the next tile to copy into the ring, running ahead across rows
+    TileCursor ld_cur{(int)blockIdx.x, 0, blockIdx.x < p.rows ? row_length(p, blockIdx.x) : 0};
     uint32_t issued = 0u, landed = 0u;  // thread 0: tiles copied so far / known to have landed
-    const uint64_t policy = ptx::policy_evict_first();
     auto issue_next = [&](int stage) {
-        while (prow < p.rows && ptile * kTile >= pn) {
-            prow += gridDim.x;
-            ptile = 0;
-            pn = prow < p.rows ? row_length(p, prow) : 0;
-        }
-        if (prow >= p.rows) return;
+        if (!cursor_settle(p, ld_cur)) return;
         ++issued;
-        const int cnt = min(kTile, pn - ptile * kTile);
-        const uint32_t bytes = (uint32_t)((cnt + 3) & ~3) * 4u;  // whole 16-byte groups: ld % 4 == 0 keeps it in the row
+        uint32_t bytes;
+        const float *src = cursor_src(p, ld_cur, bytes);
         const uint32_t bar = ptx::smem_u32(&s.full[stage]);
         ptx::mbar_arrive_expect_tx(bar, bytes);
-        ptx::bulk_g2s(ptx::smem_u32(s.ring[stage]), p.scores + (size_t)prow * (size_t)p.ld + (size_t)ptile * kTile,
-                      bytes, bar, policy);
-        ++ptile;
+        ptx::bulk_g2s(ptx::smem_u32(s.ring[stage]), src, bytes, bar, ptx::policy_evict_first());
+        ++ld_cur.tile;
     };
     if (tid == 0) {
         for (int st = 0; st < kStages; ++st) ptx::mbar_init(ptx::smem_u32(&s.full[st]), 1);
@@ -439,84 +676,87 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
 
     uint32_t g = 0;  // tiles consumed by this CTA
     for (int row = blockIdx.x; row < p.rows; row += gridDim.x) {
-        const float *x = p.scores + (size_t)row * (size_t)p.ld;
         const int nraw = p.lengths ? __ldg(p.lengths + row) : (int)p.ld;
         if (tid == 0 && p.status && (nraw < 0 || nraw > p.ld)) raise_status(p.status, RL_ERR_SEQLENS);
         const int n = row_length(p, row);
         const int kk = min(k, n);
-        if (tid == 0) s.count = 0;
+        if (tid == 0) {
+            s.count = 0;
+            s.keyed = 0;
+        }
         __syncthreads();
-        uint64_t bound = 0u;  // incoming scores are kept when key >= bound
-        float thr = -INFINITY;  // the same test on the score itself
+        // incoming scores are kept when their key reaches a lower bound, tested on the score itself
+        float thr = -INFINITY;
         int mode = 0;
+        // Long rows start from a bound taken from a sample of the row instead of -inf. Whatever
+        // the sample holds, the scores kept are all those whose key reaches the bound (compactions
+        // drop only what the rows' kk best cannot contain), so if at least kk reach it they
+        // contain the kk best; if fewer reach it, the row is scanned again from -inf below.
+        const int r = n >= kSampleMinLen ? sample_rank(kk, n) : kSample;
+        const bool sampled = r <= kSample / 4;
+        if (sampled) {
+            set_threshold(sampled_bound(s, p.scores + (size_t)row * (size_t)p.ld, n, r), thr, mode);
+        }
         const int ntiles = (n + kTile - 1) / kTile;
         for (int t = 0; t < ntiles; ++t, ++g) {
             const int st = (int)(g % kStages);
             const float4 *tile4 = reinterpret_cast<const float4 *>(s.ring[st]);
-            // keep a score when its key reaches the bound: one float compare (NaN passes !(x < thr))
-            float vals[kPer];
-            uint32_t keepm = 0u;
+            int after_add;
+            {
+                float vals[kPer];
 #pragma unroll
-            for (int j = 0; j < kPer / 4; ++j) {
-                const float4 v = tile4[j * kThreads + tid];
-                vals[4 * j] = v.x, vals[4 * j + 1] = v.y, vals[4 * j + 2] = v.z, vals[4 * j + 3] = v.w;
-            }
-            if (mode == 0 && (t + 1) * kTile <= n) {  // a full tile and a plain threshold: one compare per score
-#pragma unroll
-                for (int q = 0; q < kPer; ++q) keepm |= (uint32_t)!(vals[q] < thr) << q;
-            } else {
-#pragma unroll
-                for (int q = 0; q < kPer; ++q) {
-                    const int e = t * kTile + 4 * ((q >> 2) * kThreads + tid) + (q & 3);
-                    const bool keep = e < n && (mode == 0 ? !(vals[q] < thr) : (mode == 1 && isnan(vals[q])));
-                    keepm |= (uint32_t)keep << q;
+                for (int j = 0; j < kPer / 4; ++j) {
+                    const float4 v = tile4[j * kThreads + tid];
+                    vals[4 * j] = v.x, vals[4 * j + 1] = v.y, vals[4 * j + 2] = v.z, vals[4 * j + 3] = v.w;
                 }
-            }
-            int after_add = 0;  // the buffer count right after this warp's append
-            if (__any_sync(kFull, keepm != 0u)) {
-                // one atomic per warp: an exclusive scan of the lanes' counts
-                const int c = __popc(keepm);
-                int incl = c;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const int o = __shfl_up_sync(kFull, incl, off);
-                    if (lane >= off) incl += o;
-                }
-                int base = 0;
-                if (lane == 31) base = atomicAdd(&s.count, incl);
-                base = __shfl_sync(kFull, base, 31);
-                after_add = base + __shfl_sync(kFull, incl, 31);
-                int pos = base + incl - c;
-#pragma unroll
-                for (int q = 0; q < kPer; ++q) {
-                    if (((keepm >> q) & 1u) && pos < kCap) {
-                        s.key[pos] = order_key(vals[q]);
-                        s.idx[pos] = (uint32_t)(t * kTile + 4 * ((q >> 2) * kThreads + tid) + (q & 3));
-                        ++pos;
-                    }
-                }
+                after_add = filter_append(s, vals, t, n, thr, mode, -1);
             }
             if (tid == 0) wait_tile(g + 1u);
-            // The stage is free again and the next tile has landed. Whether to compact is decided by
-            // the barrier itself (the count passed the trigger iff some warp's append took it past):
-            // a thread must not read s.count here, because a faster warp may already be appending
-            // the next tile.
-            const bool over = __syncthreads_or(after_add > kCap - kTile) != 0;
-            if (tid == 0) issue_next(st);
-            if (over) {
-                // compact well below the trigger, so that many tiles fit before the next one
-                bound = compact(s, k, k + (kCap - kTile - k) / 2, false, idx_bits);
-                set_threshold(bound, thr, mode);
+            // The next tile has landed. Whether the buffer needs attention is decided by the barrier
+            // itself (the count passed kSoft iff some warp's append took it past): a thread must not
+            // read s.count here, because a faster warp may already be appending the next tile.
+            if (__syncthreads_or(after_add > kSoft)) {
+                const bool overflow = __syncthreads_or(after_add > kCap) != 0;
+                settle_tile(s, s.ring[st], t, n, k, idx_bits, overflow, thr, mode);
+            }
+            if (tid == 0) issue_next(st);  // the stage is free again
+        }
+        // The sampled bound was above the row's kk-th best score (fewer than kk reached it, so no
+        // compaction ran): scan the row again from -inf with plain loads (the tile ring has moved
+        // on to the next row).
+        if (__syncthreads_or(sampled && s.count < kk)) {
+            if (tid == 0) {
+                s.count = 0;
+                s.keyed = 0;
+            }
+            __syncthreads();
+            thr = -INFINITY;
+            mode = 0;
+            for (int t = 0; t < ntiles; ++t) {
+                const float *tile = p.scores + (size_t)row * (size_t)p.ld + (size_t)t * kTile;
+                int after_add;
+                {
+                    float vals[kPer];
+                    load_tile_vals(tile, t, n, vals);
+                    after_add = filter_append(s, vals, t, n, thr, mode, -1);
+                }
+                if (__syncthreads_or(after_add > kSoft)) {
+                    const bool overflow = __syncthreads_or(after_add > kCap) != 0;
+                    settle_tile(s, tile, t, n, k, idx_bits, overflow, thr, mode);
+                }
             }
         }
-        // exactly the best min(k, n)
-        if (s.count > kk) compact(s, kk, kk, true, idx_bits);
+        // exactly the best min(k, n), as keys
+        if (s.count > kk)
+            compact(s, kk, kk, true, idx_bits);
+        else
+            make_keys(s);
         // order them: pad to a power of two with entries that sort last
         int n2 = 1;
         while (n2 < kk) n2 <<= 1;
         for (int i = kk + tid; i < n2; i += kThreads) {
-            s.key[i] = 0u;
-            s.idx[i] = 0xffffffffu;
+            s.cb.key[i] = 0u;
+            s.cb.idx[i] = 0xffffffffu;
         }
         __syncthreads();
         if (n2 == 2 * kThreads)
@@ -533,12 +773,12 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
         float *ov = p.out_val ? p.out_val + (size_t)row * (size_t)p.ldo : nullptr;
         for (int i = tid; i < k; i += kThreads) {
             if (i < kk) {
-                const uint32_t key = s.key[i], ix = s.idx[i];
+                const uint32_t key = s.cb.key[i], ix = s.cb.idx[i];
                 oi[i] = (int32_t)ix;
                 if (ov) {
                     // the score back from its key; -0 and NaN payloads were folded, so those are re-read
                     const uint32_t bits = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
-                    ov[i] = ((bits == 0u || key == 0xffffffffu) && ix < (uint32_t)n) ? __ldg(x + ix) : __uint_as_float(bits);
+                    ov[i] = ((bits == 0u || key == 0xffffffffu) && ix < (uint32_t)n) ? __ldg(p.scores + (size_t)row * (size_t)p.ld + ix) : __uint_as_float(bits);
                 }
             } else {
                 oi[i] = -1;
@@ -556,7 +796,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
 
 }  // namespace
 
-int topk_max_k() { return kCap - kTile; }
+int topk_max_k() { return 4096; }  // the final sort pads to a power of two <= kCap
+static_assert(4096 <= kSoft && 4096 <= kCap, "k up to 4096: compaction targets and the final sort fit");
 
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t stream) {
     if (p.rows <= 0) return cudaSuccess;

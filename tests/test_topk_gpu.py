@@ -44,9 +44,10 @@ def test_indexer_scores_small(order):
     _run_and_check(b.scores, b.lengths, b.k, order)
 
 
+@pytest.mark.parametrize("context", [12000, 40000])
 @pytest.mark.parametrize("k", [1, 2, 7, 100, 2047, 2048, 2049, 4096])
-def test_every_k(k):
-    b = synthetic.make_topk_batch("cuda", rows=6, context=12000, k=k, seed=3)
+def test_every_k(k, context):
+    b = synthetic.make_topk_batch("cuda", rows=6, context=context, k=k, seed=3)
     _run_and_check(b.scores, b.lengths, k, "score")
 
 
@@ -77,14 +78,29 @@ def _adversarial_rows(n):
     nan_payloads.view(np.uint32)[::97] = 0x7fc00001
     nan_payloads.view(np.uint32)[::89] = 0xffc12345
     rows.append(nan_payloads)
+    nan_heavy = rng.standard_normal(n).astype(np.float32)  # enough NaN that a sampled bound admits NaN only
+    nan_heavy[rng.random(n) < 0.3] = np.nan
+    rows.append(nan_heavy)
     return np.stack(rows)
 
 
+# Rows of 16384 scores or more start from a bound taken from a sample of the row; the ascending and
+# descending rows put the sample's best scores where the row has fewer than k at or above them, so
+# those rows are scanned a second time.
+@pytest.mark.parametrize("n", [12004, 20004, 70004])
 @pytest.mark.parametrize("order", ["score", "index"])
 @pytest.mark.parametrize("k", [1, 2048, 4096])
-def test_adversarial_rows(order, k):
-    s = torch.from_numpy(_adversarial_rows(20004)).cuda()
+def test_adversarial_rows(n, order, k):
+    s = torch.from_numpy(_adversarial_rows(n)).cuda()
     _run_and_check(s, None, k, order)
+
+
+def test_long_ragged_rows():
+    b = synthetic.make_topk_batch("cuda", rows=10, context=70000, seed=8)
+    b.lengths.copy_(torch.tensor([16383, 16384, 16385, 16387, 32769, 50001, 65537, 69999, 70000, 4097],
+                                 dtype=torch.int32))
+    for k in (1, 100, 2048, 4096):
+        _run_and_check(b.scores, b.lengths, k, "score")
 
 
 def test_unaligned_length_rejected_and_bad_lengths_flagged():
