@@ -12,15 +12,18 @@
 // the prefix seen so far (in the total order) cannot be among the k best of
 // the row. So the CTA streams the row in tiles of 4096 scores and appends to
 // a shared-memory buffer only the scores whose key reaches a lower bound L;
-// when the buffer fills, a radix select over the buffer (11, 11 and 10 bits of
-// the key, then the position for ties) raises L and drops what can no longer
-// be selected. At the end the same select, run to the exact k-th element, keeps
-// exactly min(k, n) entries, and a bitonic sort in shared memory orders them
+// when the buffer fills, a radix select over the buffer (over the key bits
+// that differ, then the position for ties) raises L and drops what can no
+// longer be selected. Long rows start with L taken from a sample of the row
+// rather than -inf, so most rows need no compaction at all; a row where fewer
+// than k scores reach the sampled L is scanned again from -inf. At the end
+// the same select, run to the exact k-th element, keeps exactly min(k, n)
+// entries, and a bitonic sort in registers and shared memory orders them
 // (by score, ties by position, or by position). The buffer's order of arrival
 // (shared-memory atomics) never decides anything: the kept set is defined by
 // the total order and the output order by the sort, so the result is
 // bit-identical from run to run. All counts are integers. The CTAs are
-// persistent (two per SM); thread 0 keeps two 16 KB tiles in flight with bulk
+// persistent (two per SM); thread 0 keeps four 16 KB tiles in flight with bulk
 // copies (TMA) into a shared-memory ring, completing on mbarriers whose waits
 // are bounded, and runs ahead into the next row while this one is finished.
 #include <algorithm>
