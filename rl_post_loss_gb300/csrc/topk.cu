@@ -75,6 +75,7 @@ struct TopkSmem {
     union {
         Candidates cb;              // the candidate buffer
         uint32_t sample[kSample];   // at the start of a row: the sampled keys
+        uint64_t packed[kCap];      // at the end of a row: the selection by bucket, then sorted (see pack_out)
     };
     uint32_t hist[kBins];
     unsigned long long full[kStages];  // mbarriers: a tile has landed
@@ -248,8 +249,45 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
         if (exact || kept > limit) {
             // keep only the (target - above) equal entries with the lowest positions
             const int need = target - above;
+            const int ties = kept - above;  // the entries whose key is key_star
             uint32_t ipre = 0u;
             int ishift = idx_bits, ibelow = 0;  // positions are below 2^idx_bits
+            if (ties <= kBins) {
+                // few enough: gather their positions into the histogram's storage and take the
+                // need-th smallest directly (positions are distinct, so exactly one has that rank)
+                const int lane = tid & 31;
+                if (tid == 0) {
+                    s.found_bin = 0;
+                    s.found_before = -1;  // stays -1 only if the invariant broke
+                }
+                __syncthreads();
+                for (int i0 = tid & ~31; i0 < cnt; i0 += kThreads) {  // warp-uniform trip count
+                    const int i = i0 + lane;
+                    const bool eq = i < cnt && s.cb.key[i] == key_star;
+                    const unsigned m = __ballot_sync(kFull, eq);
+                    int b0 = 0;
+                    if (lane == 0 && m) b0 = atomicAdd(&s.found_bin, __popc(m));
+                    b0 = __shfl_sync(kFull, b0, 0);
+                    if (eq) {
+                        const int slot = b0 + __popc(m & ((1u << lane) - 1u));
+                        if (slot < kBins) s.hist[slot] = s.cb.idx[i];
+                    }
+                }
+                __syncthreads();
+                const int nt = min(s.found_bin, kBins);
+                if (tid == 0 && nt != ties) s.broken = 1;
+                for (int t = tid; t < nt; t += kThreads) {
+                    const uint32_t x = s.hist[t];
+                    int r = 0;
+#pragma unroll 4
+                    for (int j = 0; j < nt; ++j) r += s.hist[j] < x ? 1 : 0;
+                    if (r == need - 1) s.found_before = (int)x;
+                }
+                __syncthreads();
+                if (tid == 0 && s.found_before < 0) s.broken = 1;
+                ipre = (uint32_t)max(s.found_before, 0);
+                ishift = 0;  // no radix passes
+            }
             while (ishift > 0) {
                 const int w = min(11, ishift);
                 const int sh = ishift - w;
@@ -306,6 +344,18 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
     __syncthreads();
     if (tid == 0) s.keyed = s.count;
     return resolved ? bound : (uint64_t)key_star + 1u;
+}
+
+// The output order as one 64-bit value, larger first. By score: the key, then the complement of
+// the position (ties to the lower position); by position: the complement of the position, then the
+// key. Positions are distinct, so no two entries of a row pack to the same value.
+__device__ __forceinline__ uint64_t pack_out(uint32_t key, uint32_t ix, bool by_score) {
+    return by_score ? (((uint64_t)key << 32) | (uint64_t)(~ix)) : (((uint64_t)(~ix) << 32) | (uint64_t)key);
+}
+__device__ __forceinline__ void unpack_out(uint64_t c, bool by_score, uint32_t &key, uint32_t &ix) {
+    const uint32_t hi = (uint32_t)(c >> 32), lo = (uint32_t)c;
+    key = by_score ? hi : lo;
+    ix = by_score ? ~lo : ~hi;
 }
 
 // a comes before b in the output order
@@ -432,6 +482,133 @@ __device__ void bitonic(TopkSmem &s, int n2, bool by_score) {
             __syncthreads();
         }
     }
+}
+
+constexpr int kSortMax = kCap / 2;                             // entries bucket_sort takes
+constexpr int kSortPer = (kSortMax + kThreads - 1) / kThreads;  // per thread
+constexpr int kSortBudget = 128;  // allowed sum of squared bucket sizes, per entry
+
+// Sorts the buffer's first n entries (n <= kSortMax) into output order through buckets of the
+// leading bits in which the entries' high words (see pack_out) differ: the histogram of those
+// bits gives each bucket's start (larger buckets first), the entries are scattered by bucket, and
+// each entry's position is its bucket's start plus the number of entries of its bucket that come
+// before it. The cost is the sum of the squared bucket sizes; when that exceeds kSortBudget n,
+// nothing is written and false is returned (the caller sorts with the bitonic network). On
+// success s.packed[n + i] holds the i-th entry in output order. Block-wide; ends with a barrier.
+__device__ bool bucket_sort(TopkSmem &s, int n, bool by_score) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (n == 0) return true;
+    // the entries, packed, and the bits in which their high words differ
+    uint64_t c[kSortPer];
+    const uint32_t h0 = (uint32_t)(pack_out(s.cb.key[0], s.cb.idx[0], by_score) >> 32);
+    uint32_t hmin = 0xffffffffu, hmax = 0u, vary = 0u;
+#pragma unroll
+    for (int j = 0; j < kSortPer; ++j) {
+        const int i = j * kThreads + tid;
+        c[j] = i < n ? pack_out(s.cb.key[i], s.cb.idx[i], by_score) : 0ull;
+        if (i < n) {
+            const uint32_t h = (uint32_t)(c[j] >> 32);
+            hmin = min(hmin, h);
+            hmax = max(hmax, h);
+            vary |= h ^ h0;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        hmin = min(hmin, __shfl_xor_sync(kFull, hmin, off));
+        hmax = max(hmax, __shfl_xor_sync(kFull, hmax, off));
+        vary |= __shfl_xor_sync(kFull, vary, off);
+    }
+    if (lane == 0) {
+        s.hist[warp] = hmin;
+        s.hist[kThreads / 32 + warp] = hmax;
+        s.hist[2 * (kThreads / 32) + warp] = vary;
+    }
+    __syncthreads();  // also: every entry of the buffer is in registers (s.packed overlays it)
+    for (int w = 0; w < kThreads / 32; ++w) {
+        hmin = min(hmin, s.hist[w]);
+        hmax = max(hmax, s.hist[kThreads / 32 + w]);
+        vary |= s.hist[2 * (kThreads / 32) + w];
+    }
+    __syncthreads();
+    // the digit: up to 11 bits below the common prefix, above the lowest bit that varies
+    const uint32_t diff = hmin ^ hmax;
+    const int shift = diff ? 32 - __clz(diff) : 0;
+    const int low = vary ? __ffs(vary) - 1 : 0;
+    const int w = min(11, max(shift - low, 0));
+    const int sh = shift - w;
+    const uint32_t dmask = w ? (1u << w) - 1u : 0u;
+    auto digit = [&](uint64_t cc) { return ((uint32_t)(cc >> 32) >> sh) & dmask; };
+
+    for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kSortPer; ++j) hist_add_warp(s.hist, digit(c[j]), j * kThreads + tid < n);
+    __syncthreads();
+
+    // bucket starts from the top bin down, and the cost (sum of squared sizes)
+    constexpr int per = kBins / kThreads;
+    const int base = kBins - per * (tid + 1);  // this thread's bins, scanned from base + per - 1 down
+    uint32_t h[per], local = 0u, sq = 0u;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+        h[i] = s.hist[base + per - 1 - i];
+        local += h[i];
+        sq += h[i] * h[i];
+    }
+    uint32_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t o = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += o;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(kFull, sq, off);
+    if (lane == 31) s.warp_tot[warp] = incl;
+    if (lane == 0) s.warp_base[warp] = (int)sq;
+    __syncthreads();
+    uint32_t run = incl - local, cost = 0u;
+    for (int v = 0; v < kThreads / 32; ++v) {
+        if (v < warp) run += s.warp_tot[v];
+        cost += (uint32_t)s.warp_base[v];
+    }
+    const bool ok = cost <= (uint32_t)kSortBudget * (uint32_t)n;
+    if (ok) {
+#pragma unroll
+        for (int i = 0; i < per; ++i) {  // the bin's start, then the scatter's cursor
+            s.hist[base + per - 1 - i] = run;
+            run += h[i];
+        }
+    }
+    __syncthreads();
+    if (!ok) return false;
+
+    // scatter by bucket: one shared atomic per distinct digit of a warp
+#pragma unroll
+    for (int j = 0; j < kSortPer; ++j) {
+        const bool valid = j * kThreads + tid < n;
+        const uint32_t d = digit(c[j]);
+        const unsigned peers = __match_any_sync(kFull, valid ? d : 0xffffffffu);
+        const int leader = __ffs(peers) - 1;
+        uint32_t b0 = 0u;
+        if (valid && lane == leader) b0 = atomicAdd(&s.hist[d], (uint32_t)__popc(peers));
+        b0 = __shfl_sync(kFull, b0, leader);
+        if (valid) s.packed[b0 + __popc(peers & ((1u << lane) - 1u))] = c[j];
+    }
+    __syncthreads();
+    // hist[d] is now the end of bucket d, and hist[d + 1] its start (buckets run from the top bin down)
+    for (int i = tid; i < n; i += kThreads) {
+        const uint64_t cc = s.packed[i];
+        const uint32_t d = digit(cc);
+        const int st = d + 1 < (uint32_t)kBins ? (int)s.hist[d + 1] : 0;
+        const int en = (int)s.hist[d];
+        int rank = 0;
+#pragma unroll 4
+        for (int j = st; j < en; ++j) rank += s.packed[j] > cc ? 1 : 0;
+        s.packed[n + st + rank] = cc;
+    }
+    __syncthreads();
+    return true;
 }
 
 // The score test equivalent to key >= bound. mode 0: !(x < thr), thr the smallest score whose key
@@ -754,20 +931,25 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
             compact(s, kk, kk, true, idx_bits);
         else
             make_keys(s);
-        // order them: pad to a power of two with entries that sort last
-        int n2 = 1;
-        while (n2 < kk) n2 <<= 1;
-        for (int i = kk + tid; i < n2; i += kThreads) {
-            s.cb.key[i] = 0u;
-            s.cb.idx[i] = 0xffffffffu;
+        // order them: by buckets of the key (or position) when they are even enough, else with the
+        // bitonic network over the selection padded to a power of two with entries that sort last
+        const bool by_score = p.order_by_score != 0;
+        const bool bucketed = kk <= kSortMax && bucket_sort(s, kk, by_score);
+        if (!bucketed) {
+            int n2 = 1;
+            while (n2 < kk) n2 <<= 1;
+            for (int i = kk + tid; i < n2; i += kThreads) {
+                s.cb.key[i] = 0u;
+                s.cb.idx[i] = 0xffffffffu;
+            }
+            __syncthreads();
+            if (n2 == 2 * kThreads)
+                bitonic_regs<2>(s, by_score);
+            else if (n2 == 4 * kThreads)
+                bitonic_regs<4>(s, by_score);
+            else if (kk > 1)
+                bitonic(s, n2, by_score);
         }
-        __syncthreads();
-        if (n2 == 2 * kThreads)
-            bitonic_regs<2>(s, p.order_by_score != 0);
-        else if (n2 == 4 * kThreads)
-            bitonic_regs<4>(s, p.order_by_score != 0);
-        else if (kk > 1)
-            bitonic(s, n2, p.order_by_score != 0);
         if (tid == 0 && (s.broken || s.count > kCap)) {
             if (p.status) raise_status(p.status, RL_ERR_INTERNAL);
             s.broken = 0;
@@ -776,7 +958,13 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
         float *ov = p.out_val ? p.out_val + (size_t)row * (size_t)p.ldo : nullptr;
         for (int i = tid; i < k; i += kThreads) {
             if (i < kk) {
-                const uint32_t key = s.cb.key[i], ix = s.cb.idx[i];
+                uint32_t key, ix;
+                if (bucketed) {
+                    unpack_out(s.packed[kk + i], by_score, key, ix);
+                } else {
+                    key = s.cb.key[i];
+                    ix = s.cb.idx[i];
+                }
                 oi[i] = (int32_t)ix;
                 if (ov) {
                     // the score back from its key; -0 and NaN payloads were folded, so those are re-read
