@@ -611,6 +611,152 @@ __device__ bool bucket_sort(TopkSmem &s, int n, bool by_score) {
     return true;
 }
 
+// The score of an entry back from its key: -0 and NaN payloads were folded into the key, so those
+// are read again from the row (x, n valid scores).
+__device__ __forceinline__ float score_of(uint32_t key, uint32_t ix, const float *x, int n) {
+    const uint32_t bits = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
+    return ((bits == 0u || key == 0xffffffffu) && ix < (uint32_t)n) ? __ldg(x + ix) : __uint_as_float(bits);
+}
+
+// Output by score only: selects the kk best of the buffer's entries (all keyed) and writes them in
+// output order to oi / ov (ov may be null), in one pass of buckets over the keys' leading varying
+// bits: the histogram's scan gives every bucket's start, the buckets that start below kk are
+// scattered, and each of their entries is ranked within its bucket as in bucket_sort; ranks below
+// kk are written. Returns false with nothing written when the buckets are too uneven for the
+// ranking to pay (the caller then selects and sorts separately). Block-wide; ends with a barrier.
+__device__ bool select_sort_by_score(TopkSmem &s, int kk, int32_t *oi, float *ov, const float *x, int n) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cnt = s.count;
+    if (kk == 0) return true;
+    constexpr int kPerT = kCap / kThreads;
+    uint64_t c[kPerT];
+    const uint32_t h0 = s.cb.key[0];
+    uint32_t hmin = 0xffffffffu, hmax = 0u, vary = 0u;
+#pragma unroll
+    for (int j = 0; j < kPerT; ++j) {
+        const int i = j * kThreads + tid;
+        c[j] = i < cnt ? pack_out(s.cb.key[i], s.cb.idx[i], true) : 0ull;
+        if (i < cnt) {
+            const uint32_t h = (uint32_t)(c[j] >> 32);
+            hmin = min(hmin, h);
+            hmax = max(hmax, h);
+            vary |= h ^ h0;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        hmin = min(hmin, __shfl_xor_sync(kFull, hmin, off));
+        hmax = max(hmax, __shfl_xor_sync(kFull, hmax, off));
+        vary |= __shfl_xor_sync(kFull, vary, off);
+    }
+    if (lane == 0) {
+        s.hist[warp] = hmin;
+        s.hist[kThreads / 32 + warp] = hmax;
+        s.hist[2 * (kThreads / 32) + warp] = vary;
+    }
+    __syncthreads();  // also: every entry of the buffer is in registers (s.packed overlays it)
+    for (int w = 0; w < kThreads / 32; ++w) {
+        hmin = min(hmin, s.hist[w]);
+        hmax = max(hmax, s.hist[kThreads / 32 + w]);
+        vary |= s.hist[2 * (kThreads / 32) + w];
+    }
+    __syncthreads();
+    const uint32_t diff = hmin ^ hmax;
+    const int shift = diff ? 32 - __clz(diff) : 0;
+    const int low = vary ? __ffs(vary) - 1 : 0;
+    const int w = min(11, max(shift - low, 0));
+    const int sh = shift - w;
+    const uint32_t dmask = w ? (1u << w) - 1u : 0u;
+    auto digit = [&](uint64_t cc) { return ((uint32_t)(cc >> 32) >> sh) & dmask; };
+
+    for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0u;
+    if (tid == 0) s.found_bin = -1;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kPerT; ++j) hist_add_warp(s.hist, digit(c[j]), j * kThreads + tid < cnt);
+    __syncthreads();
+
+    // bucket starts from the top bin down, the cost (sum of squared sizes), and the bucket holding
+    // the kk-th entry
+    constexpr int per = kBins / kThreads;
+    const int base = kBins - per * (tid + 1);
+    uint32_t h[per], local = 0u, sq = 0u;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+        h[i] = s.hist[base + per - 1 - i];
+        local += h[i];
+        sq += h[i] * h[i];
+    }
+    uint32_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t o = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += o;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(kFull, sq, off);
+    if (lane == 31) s.warp_tot[warp] = incl;
+    if (lane == 0) s.warp_base[warp] = (int)sq;
+    __syncthreads();
+    uint32_t run = incl - local, cost = 0u;
+    for (int v = 0; v < kThreads / 32; ++v) {
+        if (v < warp) run += s.warp_tot[v];
+        cost += (uint32_t)s.warp_base[v];
+    }
+    const bool ok = cost <= (uint32_t)kSortBudget * (uint32_t)cnt;
+    if (ok) {
+#pragma unroll
+        for (int i = 0; i < per; ++i) {
+            const int b = base + per - 1 - i;
+            if (run < (uint32_t)kk && run + h[i] >= (uint32_t)kk) s.found_bin = b;
+            s.hist[b] = run;  // the bucket's start, then the scatter's cursor
+            run += h[i];
+        }
+    }
+    __syncthreads();
+    if (!ok) return false;
+    const int cut = s.found_bin;
+    if (cut < 0) {  // kk entries exist, so some bucket holds the kk-th (a broken invariant otherwise)
+        if (tid == 0) s.broken = 1;
+        __syncthreads();
+        return false;
+    }
+
+    // scatter the buckets at or above the cut
+#pragma unroll
+    for (int j = 0; j < kPerT; ++j) {
+        const uint32_t d = digit(c[j]);
+        const bool valid = j * kThreads + tid < cnt && d >= (uint32_t)cut;
+        const unsigned peers = __match_any_sync(kFull, valid ? d : 0xffffffffu);
+        const int leader = __ffs(peers) - 1;
+        uint32_t b0 = 0u;
+        if (valid && lane == leader) b0 = atomicAdd(&s.hist[d], (uint32_t)__popc(peers));
+        b0 = __shfl_sync(kFull, b0, leader);
+        if (valid) s.packed[b0 + __popc(peers & ((1u << lane) - 1u))] = c[j];
+    }
+    __syncthreads();
+    // hist[d] is now the end of bucket d and hist[d + 1] its start; the cut bucket ends the scatter
+    const int kept = (int)s.hist[cut];
+    for (int i = tid; i < kept; i += kThreads) {
+        const uint64_t cc = s.packed[i];
+        const uint32_t d = digit(cc);
+        const int st = d + 1 < (uint32_t)kBins ? (int)s.hist[d + 1] : 0;
+        const int en = (int)s.hist[d];
+        int rank = 0;
+#pragma unroll 4
+        for (int j = st; j < en; ++j) rank += s.packed[j] > cc ? 1 : 0;
+        const int pos = st + rank;
+        if (pos < kk) {
+            uint32_t key, ix;
+            unpack_out(cc, true, key, ix);
+            oi[pos] = (int32_t)ix;
+            if (ov) ov[pos] = score_of(key, ix, x, n);
+        }
+    }
+    __syncthreads();
+    return true;
+}
+
 // The score test equivalent to key >= bound. mode 0: !(x < thr), thr the smallest score whose key
 // reaches the bound (NaN passes it, and -0 and +0 compare equal, as their keys do); mode 1 (bound
 // above the key of +inf): NaN only; mode 2 (bound above every key): nothing.
@@ -926,38 +1072,44 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
                 }
             }
         }
-        // exactly the best min(k, n), as keys
-        if (s.count > kk)
-            compact(s, kk, kk, true, idx_bits);
-        else
-            make_keys(s);
-        // order them: by buckets of the key (or position) when they are even enough, else with the
-        // bitonic network over the selection padded to a power of two with entries that sort last
         const bool by_score = p.order_by_score != 0;
-        const bool bucketed = kk <= kSortMax && bucket_sort(s, kk, by_score);
-        if (!bucketed) {
-            int n2 = 1;
-            while (n2 < kk) n2 <<= 1;
-            for (int i = kk + tid; i < n2; i += kThreads) {
-                s.cb.key[i] = 0u;
-                s.cb.idx[i] = 0xffffffffu;
+        const float *x = p.scores + (size_t)row * (size_t)p.ld;
+        int32_t *oi = p.out_idx + (size_t)row * (size_t)p.ldo;
+        float *ov = p.out_val ? p.out_val + (size_t)row * (size_t)p.ldo : nullptr;
+        make_keys(s);
+        // by score: select the best min(k, n) and order them in one pass of buckets when the
+        // buckets are even enough
+        const bool direct = by_score && select_sort_by_score(s, kk, oi, ov, x, n);
+        bool bucketed = false;
+        if (!direct) {
+            // exactly the best min(k, n)
+            if (s.count > kk) compact(s, kk, kk, true, idx_bits);
+            // order them: by buckets of the key (or position) when they are even enough, else with
+            // the bitonic network over the selection padded to a power of two with entries that sort last
+            bucketed = kk <= kSortMax && bucket_sort(s, kk, by_score);
+            if (!bucketed) {
+                int n2 = 1;
+                while (n2 < kk) n2 <<= 1;
+                for (int i = kk + tid; i < n2; i += kThreads) {
+                    s.cb.key[i] = 0u;
+                    s.cb.idx[i] = 0xffffffffu;
+                }
+                __syncthreads();
+                if (n2 == 2 * kThreads)
+                    bitonic_regs<2>(s, by_score);
+                else if (n2 == 4 * kThreads)
+                    bitonic_regs<4>(s, by_score);
+                else if (kk > 1)
+                    bitonic(s, n2, by_score);
             }
-            __syncthreads();
-            if (n2 == 2 * kThreads)
-                bitonic_regs<2>(s, by_score);
-            else if (n2 == 4 * kThreads)
-                bitonic_regs<4>(s, by_score);
-            else if (kk > 1)
-                bitonic(s, n2, by_score);
         }
         if (tid == 0 && (s.broken || s.count > kCap)) {
             if (p.status) raise_status(p.status, RL_ERR_INTERNAL);
             s.broken = 0;
         }
-        int32_t *oi = p.out_idx + (size_t)row * (size_t)p.ldo;
-        float *ov = p.out_val ? p.out_val + (size_t)row * (size_t)p.ldo : nullptr;
         for (int i = tid; i < k; i += kThreads) {
             if (i < kk) {
+                if (direct) continue;  // written by the bucket pass
                 uint32_t key, ix;
                 if (bucketed) {
                     unpack_out(s.packed[kk + i], by_score, key, ix);
@@ -966,11 +1118,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
                     ix = s.cb.idx[i];
                 }
                 oi[i] = (int32_t)ix;
-                if (ov) {
-                    // the score back from its key; -0 and NaN payloads were folded, so those are re-read
-                    const uint32_t bits = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
-                    ov[i] = ((bits == 0u || key == 0xffffffffu) && ix < (uint32_t)n) ? __ldg(p.scores + (size_t)row * (size_t)p.ld + ix) : __uint_as_float(bits);
-                }
+                if (ov) ov[i] = score_of(key, ix, x, n);
             } else {
                 oi[i] = -1;
                 if (ov) ov[i] = -INFINITY;
