@@ -931,25 +931,47 @@ __device__ __forceinline__ int sample_rank(int kk, int n) {
 // A starting lower bound for row x of n scores (n >= kSampleMinLen): a key with at least r of the
 // sampled keys at or above it. The sample is 16 runs of 512 consecutive scores, run j starting at
 // floor(j (n - 512) / 15) rounded down to a multiple of 4, so every run lies inside the row and
-// the runs do not overlap. Uses the buffer and the histogram (the buffer must be empty).
+// the runs do not overlap. The bound is read off one histogram of the sampled keys in the window
+// of 2^24 keys below the largest (two binades of positive scores, in 2048 bins of 2^13 keys): the
+// lower edge of the bin holding the r-th largest. If fewer than r keys fall in the window, a radix
+// descent over the whole sample finds it instead. Uses the buffer's storage and the histogram
+// (the buffer must be empty).
 __device__ uint64_t sampled_bound(TopkSmem &s, const float *x, int n, int r) {
     constexpr int kRunVec = kSampleRun / 4;
+    constexpr int kWinBits = 24, kBinBits = kWinBits - 11;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0u;
     const float4 *x4 = reinterpret_cast<const float4 *>(x);
     float4 v[kSample / 4 / kThreads];
 #pragma unroll
     for (int j = 0; j < kSample / 4 / kThreads; ++j) {
-        const int w = j * kThreads + (int)threadIdx.x;  // float4 of the sample
+        const int w = j * kThreads + tid;  // float4 of the sample
         v[j] = __ldg(x4 + sample_run_start(w / kRunVec, n) / 4 + (w % kRunVec));
     }
+    uint32_t kmax = 0u;
 #pragma unroll
     for (int j = 0; j < kSample / 4 / kThreads; ++j) {
-        const int w = j * kThreads + (int)threadIdx.x;
-        s.sample[4 * w] = order_key(v[j].x);
-        s.sample[4 * w + 1] = order_key(v[j].y);
-        s.sample[4 * w + 2] = order_key(v[j].z);
-        s.sample[4 * w + 3] = order_key(v[j].w);
+        const int w = j * kThreads + tid;
+        const uint32_t a = order_key(v[j].x), b = order_key(v[j].y), c = order_key(v[j].z), d = order_key(v[j].w);
+        s.sample[4 * w] = a;
+        s.sample[4 * w + 1] = b;
+        s.sample[4 * w + 2] = c;
+        s.sample[4 * w + 3] = d;
+        kmax = max(kmax, max(max(a, b), max(c, d)));
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) kmax = max(kmax, __shfl_xor_sync(kFull, kmax, off));
+    if (lane == 0) s.warp_tot[warp] = kmax;
     __syncthreads();
+    for (int w = 0; w < kThreads / 32; ++w) kmax = max(kmax, s.warp_tot[w]);
+    const uint32_t wlo = kmax >= (1u << kWinBits) ? kmax - ((1u << kWinBits) - 1u) : 0u;
+    for (int i0 = tid & ~31; i0 < kSample; i0 += kThreads) {  // warp-uniform trip count
+        const uint32_t key = s.sample[i0 + lane];
+        hist_add_warp(s.hist, (key - wlo) >> kBinBits, key >= wlo);
+    }
+    __syncthreads();  // also: every thread has read warp_tot (find_bin rewrites it)
+    find_bin(s, (uint32_t)r, true);
+    if (s.found_bin >= 0) return (uint64_t)wlo + ((uint64_t)s.found_bin << kBinBits);
     const Descent d = radix_descent(s, s.sample, kSample, r, r + r / 4, false);
     return (uint64_t)d.prefix << d.shift;
 }
