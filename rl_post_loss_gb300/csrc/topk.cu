@@ -835,8 +835,27 @@ __device__ __forceinline__ int filter_append(TopkSmem &s, const float (&vals)[kP
         if (lane == 0) s.warp_base[threadIdx.x >> 5] = INT_MAX;
         return 0;
     }
-    // an exclusive scan of the lanes' counts
     const int c = __popc(keepm);
+    if (!__any_sync(kFull, c > 1)) {
+        // the common case: every lane keeps at most one score, so one ballot gives the positions
+        const unsigned m = __ballot_sync(kFull, c != 0);
+        const int total = __popc(m);
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&s.count, total);
+        base = __shfl_sync(kFull, base, 0);
+        if (lane == 0) s.warp_base[threadIdx.x >> 5] = base;
+        const int pos = base + __popc(m & ((1u << lane) - 1u));
+        if (c != 0 && pos < kCap) {
+            const int q = __ffs(keepm) - 1;
+            float v = vals[0];
+#pragma unroll
+            for (int qq = 1; qq < kPer; ++qq) v = q == qq ? vals[qq] : v;
+            s.cb.key[pos] = __float_as_uint(v);  // raw bits; the next compaction makes the key
+            s.cb.idx[pos] = (uint32_t)(tile_elem(t, 0) + 4 * kThreads * (q >> 2) + (q & 3));
+        }
+        return base + total;
+    }
+    // an exclusive scan of the lanes' counts
     int incl = c;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
