@@ -17,9 +17,12 @@
 // longer be selected. Long rows start with L taken from a sample of the row
 // rather than -inf, so most rows need no compaction at all; a row where fewer
 // than k scores reach the sampled L is scanned again from -inf. At the end
-// the same select, run to the exact k-th element, keeps exactly min(k, n)
-// entries, and a bitonic sort in registers and shared memory orders them
-// (by score, ties by position, or by position). The buffer's order of arrival
+// one pass of buckets over the keys' leading varying bits selects the
+// min(k, n) best and orders them (by score, ties by position): each entry's
+// output position is its bucket's start plus its rank within the bucket.
+// Where the buckets are too uneven, or the order is by position, the radix
+// select run to the exact k-th element keeps min(k, n) entries and a bucket
+// ranking or a bitonic sort orders them. The buffer's order of arrival
 // (shared-memory atomics) never decides anything: the kept set is defined by
 // the total order and the output order by the sort, so the result is
 // bit-identical from run to run. All counts are integers. The CTAs are
