@@ -139,3 +139,24 @@ def test_full_size_sampled_rows_and_properties():
     again = capi.topk(b.scores, b.k, lengths=b.lengths)
     torch.cuda.synchronize()
     assert torch.equal(again[0], idx)
+
+
+# The final pass ranks the selection within buckets of the key's leading bits when the buckets
+# are even enough (sum of squared sizes at most 128 per entry) and falls back to an exact select
+# plus a separate sort otherwise; rows with few distinct values land on either side of that.
+@pytest.mark.parametrize("distinct", [3, 40, 1000, 5000])
+@pytest.mark.parametrize("order", ["score", "index"])
+def test_few_distinct_values_long_rows(distinct, order):
+    rng = np.random.default_rng(20 + distinct)
+    n = 60004
+    s = (rng.integers(0, distinct, (4, n)).astype(np.float32) * np.float32(0.25)) - np.float32(100.0)
+    _run_and_check(torch.from_numpy(s).cuda(), None, 2048, order)
+
+
+# k on both sides of the largest selection the bucket ranking orders (2560) and of the power of
+# two the bitonic fallback pads to.
+@pytest.mark.parametrize("k", [2559, 2560, 2561, 3000])
+@pytest.mark.parametrize("order", ["score", "index"])
+def test_k_around_the_bucket_limit(k, order):
+    b = synthetic.make_topk_batch("cuda", rows=5, context=50000, k=k, seed=9)
+    _run_and_check(b.scores, b.lengths, k, order)
