@@ -243,7 +243,7 @@ RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(rl_loss_t handle
  * cross_trajectory, consecutive responses sharing a rollout id are segments
  * of one rollout and segment s is scaled by (gamma lambda)^{N_{>s}}, N_{>s}
  * the mask=1 tokens of its later segments. Computed in fp32 in one pass over
- * the token arrays: 4096-token chunks, each folded into an affine map, a fixed
+ * the token arrays: 8192-token chunks, each folded into an affine map, a fixed
  * tree inside a chunk and a look-back over the chunks to the right in a fixed
  * order; bit-identical run to run. The result feeds RL_ADV_PER_TOKEN. */
 typedef struct rl_gae_config {
@@ -255,7 +255,7 @@ typedef struct rl_gae_config {
 } rl_gae_config;
 
 /* Bytes of device workspace rl_gae_advantages needs for num_tokens tokens
- * (a 256-byte header and a 48-byte slot per 4096-token chunk). */
+ * (a 256-byte header and a 48-byte slot per 8192-token chunk). */
 RL_LOSS_API size_t rl_gae_workspace_bytes(int32_t num_tokens);
 
 /* Device pointers: rewards [T], values [T] fp32, mask [T] u8 (nonzero =
@@ -288,9 +288,10 @@ RL_LOSS_API rl_status rl_gae_advantages(const rl_gae_config *config, int32_t num
  * non-deterministic CUDA top-k collapsed RL; torch.topk was used instead).
  * Selection: the first k positions of a row under one total order: NaN above
  * every number, then larger score, then lower position; -0 and +0 tie. The
- * result (set and order) is unique and bit-identical from run to run. One
- * read of each row from HBM (a CTA per row streams it through a shared-memory
- * candidate buffer with a rising lower bound). */
+ * result (set and order) is unique and bit-identical from run to run. A CTA
+ * per row streams it once from HBM through a shared-memory candidate buffer
+ * behind a lower bound taken from a 4% sample of the row (a row where fewer
+ * than k scores reach that bound is read a second time from the start). */
 typedef enum rl_topk_order {
     RL_TOPK_BY_SCORE = 0,    /* (score desc, position asc): what a sorted torch.topk returns, ties fixed */
     RL_TOPK_BY_POSITION = 1  /* the same set by increasing position */
@@ -310,7 +311,10 @@ RL_LOSS_API int32_t rl_topk_max_k(void);
  * i32 positions and, if non-NULL, out_val [rows x ldo] fp32 (the scores
  * themselves, bit for bit). When lengths[q] < k the missing entries are -1 and
  * -inf. `device_status` (optional, device uint32) receives RL_ERR_SEQLENS for
- * a length outside [0, ld] (clamped). Host-side errors: RL_ERR_INVALID_ARG
+ * a length outside [0, ld] (clamped), RL_ERR_TIMEOUT if a tile copy did not
+ * land within its bounded wait, and RL_ERR_INTERNAL if an internal consistency
+ * check failed; after either of the last two that row's output is not valid.
+ * Host-side errors: RL_ERR_INVALID_ARG
  * (NULL pointer, bad order), RL_ERR_SHAPE (rows < 0, ld < 1, ldo < k),
  * RL_ERR_UNSUPPORTED (k outside [1, rl_topk_max_k()]), RL_ERR_ALIGNMENT.
  * Needs no handle and allocates nothing; one launch on `stream`. */
