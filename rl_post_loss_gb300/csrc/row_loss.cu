@@ -12,6 +12,7 @@
 // Rows with g == 0 (masked, popped, clipped, zero advantage) are written as
 // +0.0 without evaluating the softmax a second time.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -224,15 +225,21 @@ cudaError_t launch_for(const RowParams &p, cudaStream_t stream) {
         row_loss_twopass_kernel<T, 512, false, false><<<p.num_tokens, 512, 0, stream>>>(p, 0);
         return cudaGetLastError();
     }
-    static int configured_dev = -1;
+    // per device, once: the shared-memory opt-in (host threads may launch on different devices at
+    // the same time)
+    static std::mutex mu;
+    static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured_dev != dev) {
-        e = cudaFuncSetAttribute(row_loss_twopass_kernel<T, 1024, true, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
-        if (e != cudaSuccess) return e;
-        configured_dev = dev;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 64 || !configured[dev]) {
+            e = cudaFuncSetAttribute(row_loss_twopass_kernel<T, 1024, true, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
+            if (e != cudaSuccess) return e;
+            if (dev < 64) configured[dev] = true;
+        }
     }
     const int nvec = p.vocab / (16 / (int)sizeof(T));
     const int stage_vecs = std::min(nvec, kStageBytes / 16);

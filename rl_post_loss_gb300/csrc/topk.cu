@@ -31,6 +31,7 @@
 // are bounded, and runs ahead into the next row while this one is finished.
 #include <algorithm>
 #include <climits>
+#include <mutex>
 
 #include "common.cuh"
 #include "scan_select.cuh"
@@ -1184,16 +1185,25 @@ static_assert(4096 <= kSoft && 4096 <= kCap, "k up to 4096: compaction targets a
 
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t stream) {
     if (p.rows <= 0) return cudaSuccess;
-    static int configured_dev = -1, sms = 0;
+    // per device, once: the shared-memory opt-in and the SM count (host threads may launch on
+    // different devices at the same time)
+    static std::mutex mu;
+    static int sms_of[64] = {};  // 0: this device is not configured yet
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured_dev != dev) {
-        e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(TopkSmem));
-        if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        configured_dev = dev;
+    int sms = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 64 || sms_of[dev] == 0) {
+            e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(TopkSmem));
+            if (e != cudaSuccess) return e;
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return e;
+            if (dev < 64) sms_of[dev] = sms;
+        } else {
+            sms = sms_of[dev];
+        }
     }
     const int grid = std::min(p.rows, 2 * sms);  // persistent: two CTAs per SM
     topk_kernel<<<grid, kThreads, sizeof(TopkSmem), stream>>>(p);
