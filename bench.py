@@ -48,6 +48,9 @@ def parse_args():
     ap.add_argument("--max-len", type=int, default=0, help="cap every response length (small profiling runs)")
     ap.add_argument("--vocab", type=int, default=0, help="case 4: vocabulary override (small profiling runs)")
     ap.add_argument("--rows", type=int, default=0, help="topk: query rows override (small profiling runs)")
+    ap.add_argument("--graph", action="store_true",
+                    help="loss cases 0-3: capture one step in a CUDA graph and time its replays (the per-kernel "
+                         "profile is then not taken; the roofline uses the whole step)")
     return ap.parse_args()
 
 
@@ -323,7 +326,17 @@ def main():
     torch.cuda.synchronize()
     bits = rl.device_status()
 
-    rl.profile_start(args.steps)
+    graph = None
+    if args.graph:
+        # one step captured once (the warm-up above did the per-device setup); replays launch nothing from the host
+        graph = torch.cuda.CUDAGraph()
+        l0 = rl.launch_count()
+        with torch.cuda.graph(graph):
+            capi.run_batch(rl, batch, out)
+        launches_per_step = rl.launch_count() - l0
+        torch.cuda.synchronize()
+    else:
+        rl.profile_start(args.steps)
     launches0 = rl.launch_count()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
@@ -334,20 +347,30 @@ def main():
         for _ in range(args.steps):
             if flush is not None:
                 flush.zero_()
-            capi.run_batch(rl, batch, out)
+            if graph is not None:
+                graph.replay()
+            else:
+                capi.run_batch(rl, batch, out)
         stop.record(stream)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
     ms = start.elapsed_time(stop)
-    launches = rl.launch_count() - launches0
-    prof = rl.profile_read()
+    if graph is not None:
+        launches = launches_per_step * args.steps
+        prof = {}
+    else:
+        launches = rl.launch_count() - launches0
+        prof = rl.profile_read()
     ms = max_over_ranks(ms)
 
     T = batch.num_tokens
     value = replica_throughput(T, args.steps, world, ms)
-    row_n, row_ms = prof["row_loss"]
-    row_avg_ms = row_ms / max(1, row_n)
+    if graph is not None:  # no per-kernel times: the whole step stands in for the row kernel
+        row_avg_ms = ms / args.steps
+    else:
+        row_n, row_ms = prof["row_loss"]
+        row_avg_ms = row_ms / max(1, row_n)
     bytes_per_launch = algorithmic_bytes(batch)
     peak, peak_kind = measured_peaks()
     achieved = bytes_per_launch / (row_avg_ms / 1e3) / 1e9
@@ -384,9 +407,10 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": workload_config(batch, args.case),
+                "config": dict(workload_config(batch, args.case), **({"cuda_graph": True} if graph is not None else {})),
                 "hbm_gbs": world * args.steps * bytes_per_launch / (ms / 1e3) / 1e9,
-                "roofline": {"bound": "hbm", "kernel": "row_loss", "achieved": achieved, "peak": peak,
+                "roofline": {"bound": "hbm", "kernel": "row_loss" if graph is None else "whole step (CUDA graph)",
+                             "achieved": achieved, "peak": peak,
                              "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s", "frac": achieved / peak,
                              "traffic": traffic, "algorithmic_bytes_per_launch": bytes_per_launch,
                              "avg_launch_ms": row_avg_ms},
