@@ -198,8 +198,11 @@ __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twop
     const float nlz2 = -s_logZ2;
     const float c = -g;
     const int y = (int)s_y;  // g != 0 implies a valid target
+    // Pass 2 walks this thread's groups in reverse: the ones pass 1 loaded last are the likeliest
+    // to still be in L1 / L2 (and, with staging, the oldest ones are the shared-memory prefix).
+    const int k_last = (int)threadIdx.x < nvec ? (int)threadIdx.x + ((nvec - 1 - (int)threadIdx.x) / kRowThreads) * kRowThreads : -1;
 #pragma unroll 4
-    for (int k = threadIdx.x; k < nvec; k += kRowThreads) {
+    for (int k = k_last; k >= (int)threadIdx.x; k -= kRowThreads) {
         float x[VEC];
         if (kStage && k < stage_vecs)
             decode16<T>(s_row[k], x);
