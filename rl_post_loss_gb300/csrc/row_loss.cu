@@ -44,8 +44,13 @@ struct VecTraits<float, CS> {
     __device__ __forceinline__ static float load1(const void *p, int64_t v) {
         return __ldg(reinterpret_cast<const float *>(p) + v);
     }
+    // the second read: evict-first from L2 (CS, long rows) or from L1 (short rows), since nothing reads it again
     __device__ __forceinline__ static void load_last(const void *p, float (&x)[4]) {
-        const float4 v = CS ? __ldcs(reinterpret_cast<const float4 *>(p)) : __ldg(reinterpret_cast<const float4 *>(p));
+        float4 v;
+        if (CS)
+            v = __ldcs(reinterpret_cast<const float4 *>(p));
+        else
+            asm("ld.global.nc.L1::evict_first.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
         x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
     }
     __device__ __forceinline__ static void store(void *p, const float (&x)[4]) {
@@ -72,8 +77,13 @@ struct VecTraits<__nv_bfloat16, CS> {
         const uint16_t b = __ldg(reinterpret_cast<const unsigned short *>(p) + v);
         return __uint_as_float(static_cast<uint32_t>(b) << 16);
     }
+    // the second read: evict-first from L2 (CS, long rows) or from L1 (short rows), since nothing reads it again
     __device__ __forceinline__ static void load_last(const void *p, float (&x)[8]) {
-        const uint4 v = CS ? __ldcs(reinterpret_cast<const uint4 *>(p)) : __ldg(reinterpret_cast<const uint4 *>(p));
+        uint4 v;
+        if (CS)
+            v = __ldcs(reinterpret_cast<const uint4 *>(p));
+        else
+            asm("ld.global.nc.L1::evict_first.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
         x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
         x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
     }
