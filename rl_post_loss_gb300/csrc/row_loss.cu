@@ -20,13 +20,15 @@ namespace rlk {
 
 namespace {
 
-// Rows of at most this many bytes use 512-thread blocks with default caching
-// (four rows per SM; the second read of a row hits L1). Longer rows use
-// 1024-thread blocks and evict-first loads in the second pass and evict-first
-// stores, so the dlogits stream does not push rows awaiting their second read
-// out of L2. Chosen from GB300 sweeps over 256/512/1024 threads and both hints.
-// Long rows also keep their first kStageBytes in shared memory from the first
-// pass to the second (two blocks per SM), which shrinks what must stay in L2.
+// Rows of at most this many bytes use 512-thread blocks (four rows per SM) and
+// read the second pass with an L1 evict-first hint. Longer rows use 1024-thread
+// blocks (two per SM) with evict-first (L2) loads in the second pass, and keep
+// their first kStageBytes in shared memory from the first pass to the second,
+// which shrinks what must stay in L2. Every row streams its dlogits out with
+// evict-first stores, so they do not push rows still waiting for their second
+// read out of L2, and the second pass walks each thread's groups in reverse
+// (most recently loaded first). Chosen from GB300 sweeps over 256/512/1024
+// threads, staging sizes and the cache hints.
 constexpr size_t kShortRowBytes = 128 * 1024;
 constexpr int kStageBytes = 96 * 1024;
 
@@ -53,11 +55,10 @@ struct VecTraits<float, CS> {
             asm("ld.global.nc.L1::evict_first.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
         x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
     }
+    // streaming stores: dz is not read again here, and keeping it out of L2 leaves room for the rows
+    // still waiting for their second read
     __device__ __forceinline__ static void store(void *p, const float (&x)[4]) {
-        if (CS)
-            __stcs(reinterpret_cast<float4 *>(p), make_float4(x[0], x[1], x[2], x[3]));
-        else
-            *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+        __stcs(reinterpret_cast<float4 *>(p), make_float4(x[0], x[1], x[2], x[3]));
     }
     __device__ __forceinline__ static void store1(void *p, int64_t v, float x) {
         reinterpret_cast<float *>(p)[v] = x;
@@ -91,10 +92,7 @@ struct VecTraits<__nv_bfloat16, CS> {
         uint4 v;
         v.x = pack_bf16x2(x[0], x[1]); v.y = pack_bf16x2(x[2], x[3]);
         v.z = pack_bf16x2(x[4], x[5]); v.w = pack_bf16x2(x[6], x[7]);
-        if (CS)
-            __stcs(reinterpret_cast<uint4 *>(p), v);
-        else
-            *reinterpret_cast<uint4 *>(p) = v;
+        __stcs(reinterpret_cast<uint4 *>(p), v);  // streaming, as for fp32
     }
     __device__ __forceinline__ static void store1(void *p, int64_t v, float x) {
         reinterpret_cast<__nv_bfloat16 *>(p)[v] = __float2bfloat16_rn(x);
