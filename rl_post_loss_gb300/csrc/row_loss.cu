@@ -20,8 +20,9 @@ namespace rlk {
 
 namespace {
 
-// Rows of at most this many bytes use 512-thread blocks (four rows per SM) and
-// read the second pass with an L1 evict-first hint. Longer rows use 1024-thread
+// Rows of at most this many bytes use 256-thread blocks (eight rows per SM, eight
+// 16-byte loads in flight per thread) and read the second pass with an L1
+// evict-first hint. Longer rows use 1024-thread
 // blocks (two per SM) with evict-first (L2) loads in the second pass, and keep
 // their first kStageBytes in shared memory from the first pass to the second,
 // which shrinks what must stay in L2. Every row streams its dlogits out with
@@ -143,6 +144,7 @@ template <typename T, int kRowThreads, bool CS, bool kStage>
 __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twopass_kernel(RowParams p, int stage_vecs) {
     using VT = VecTraits<T, CS>;
     constexpr int VEC = VT::kElems;
+    constexpr int kUnroll = kRowThreads <= 256 ? 8 : 4;  // 16-byte loads in flight per thread
     extern __shared__ uint4 s_row[];
     __shared__ RowStats2 warp_stats[kRowThreads / 32];
     __shared__ float s_logZ2, s_g;
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twop
     const uint32_t meta = __ldg(p.meta + row);
 
     RowStats2 st = empty_stats();
-#pragma unroll 4  // several 16-byte loads in flight per thread
+#pragma unroll kUnroll
     for (int k = threadIdx.x; k < nvec; k += kRowThreads) {
         float x[VEC];
         if (kStage && k < stage_vecs) {
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twop
     // Pass 2 walks this thread's groups in reverse: the ones pass 1 loaded last are the likeliest
     // to still be in L1 / L2 (and, with staging, the oldest ones are the shared-memory prefix).
     const int k_last = (int)threadIdx.x < nvec ? (int)threadIdx.x + ((nvec - 1 - (int)threadIdx.x) / kRowThreads) * kRowThreads : -1;
-#pragma unroll 4
+#pragma unroll kUnroll
     for (int k = k_last; k >= (int)threadIdx.x; k -= kRowThreads) {
         float x[VEC];
         if (kStage && k < stage_vecs)
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twop
 template <typename T>
 cudaError_t launch_for(const RowParams &p, cudaStream_t stream) {
     if ((size_t)p.vocab * sizeof(T) <= kShortRowBytes) {
-        row_loss_twopass_kernel<T, 512, false, false><<<p.num_tokens, 512, 0, stream>>>(p, 0);
+        row_loss_twopass_kernel<T, 256, false, false><<<p.num_tokens, 256, 0, stream>>>(p, 0);
         return cudaGetLastError();
     }
     // per device, once: the shared-memory opt-in (host threads may launch on different devices at
