@@ -21,23 +21,22 @@ namespace rlk {
 namespace {
 
 // Rows of at most this many bytes use 256-thread blocks (eight rows per SM, eight
-// 16-byte loads in flight per thread) and read the second pass with an L1
-// evict-first hint. Longer rows use 1024-thread
-// blocks (two per SM) with evict-first (L2) loads in the second pass, and keep
-// their first kStageBytes in shared memory from the first pass to the second,
-// which shrinks what must stay in L2. Every row streams its dlogits out with
-// evict-first stores, so they do not push rows still waiting for their second
-// read out of L2, and the second pass walks each thread's groups in reverse
-// (most recently loaded first). Chosen from GB300 sweeps over 256/512/1024
-// threads, staging sizes and the cache hints.
+// 16-byte loads in flight per thread). Longer rows use 1024-thread blocks (two
+// per SM) and keep their first kStageBytes in shared memory from the first pass
+// to the second, which shrinks what must stay in L2. Every row reads its second
+// pass with an L1 evict-first hint, streams its dlogits out with evict-first
+// stores (so they do not push rows still waiting for their second read out of
+// L2), and walks each thread's groups in reverse in the second pass (most
+// recently loaded first). Chosen from GB300 sweeps over 128/256/512/1024
+// threads, staging sizes, unrolling and the cache hints.
 constexpr size_t kShortRowBytes = 128 * 1024;
 constexpr int kStageBytes = 96 * 1024;
 
-template <typename T, bool CS>
+template <typename T>
 struct VecTraits;
 
-template <bool CS>
-struct VecTraits<float, CS> {
+template <>
+struct VecTraits<float> {
     static constexpr int kElems = 4;
     __device__ __forceinline__ static void load(const void *p, float (&x)[4]) {
         const float4 v = __ldg(reinterpret_cast<const float4 *>(p));
@@ -47,13 +46,10 @@ struct VecTraits<float, CS> {
     __device__ __forceinline__ static float load1(const void *p, int64_t v) {
         return __ldg(reinterpret_cast<const float *>(p) + v);
     }
-    // the second read: evict-first from L2 (CS, long rows) or from L1 (short rows), since nothing reads it again
+    // the second read, evict-first from L1: nothing reads it again, and it leaves L1 to the other rows
     __device__ __forceinline__ static void load_last(const void *p, float (&x)[4]) {
         float4 v;
-        if (CS)
-            v = __ldcs(reinterpret_cast<const float4 *>(p));
-        else
-            asm("ld.global.nc.L1::evict_first.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+        asm("ld.global.nc.L1::evict_first.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
         x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
     }
     // streaming stores: dz is not read again here, and keeping it out of L2 leaves room for the rows
@@ -66,8 +62,8 @@ struct VecTraits<float, CS> {
     }
 };
 
-template <bool CS>
-struct VecTraits<__nv_bfloat16, CS> {
+template <>
+struct VecTraits<__nv_bfloat16> {
     static constexpr int kElems = 8;
     __device__ __forceinline__ static void load(const void *p, float (&x)[8]) {
         const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
@@ -79,13 +75,10 @@ struct VecTraits<__nv_bfloat16, CS> {
         const uint16_t b = __ldg(reinterpret_cast<const unsigned short *>(p) + v);
         return __uint_as_float(static_cast<uint32_t>(b) << 16);
     }
-    // the second read: evict-first from L2 (CS, long rows) or from L1 (short rows), since nothing reads it again
+    // the second read, evict-first from L1 (as for fp32)
     __device__ __forceinline__ static void load_last(const void *p, float (&x)[8]) {
         uint4 v;
-        if (CS)
-            v = __ldcs(reinterpret_cast<const uint4 *>(p));
-        else
-            asm("ld.global.nc.L1::evict_first.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+        asm("ld.global.nc.L1::evict_first.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
         x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
         x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
     }
@@ -140,9 +133,9 @@ __device__ __forceinline__ void accumulate(RowStats2 &st, const float (&x)[N]) {
 
 // kStage: the first stage_vecs 16-byte groups of the row are kept in shared memory between the
 // passes (each thread re-reads only the groups it wrote).
-template <typename T, int kRowThreads, bool CS, bool kStage>
+template <typename T, int kRowThreads, bool kStage>
 __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twopass_kernel(RowParams p, int stage_vecs) {
-    using VT = VecTraits<T, CS>;
+    using VT = VecTraits<T>;
     constexpr int VEC = VT::kElems;
     constexpr int kUnroll = kRowThreads <= 256 ? 8 : 4;  // 16-byte loads in flight per thread
     extern __shared__ uint4 s_row[];
@@ -235,7 +228,7 @@ __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twop
 template <typename T>
 cudaError_t launch_for(const RowParams &p, cudaStream_t stream) {
     if ((size_t)p.vocab * sizeof(T) <= kShortRowBytes) {
-        row_loss_twopass_kernel<T, 256, false, false><<<p.num_tokens, 256, 0, stream>>>(p, 0);
+        row_loss_twopass_kernel<T, 256, false><<<p.num_tokens, 256, 0, stream>>>(p, 0);
         return cudaGetLastError();
     }
     // per device, once: the shared-memory opt-in (host threads may launch on different devices at
@@ -248,7 +241,7 @@ cudaError_t launch_for(const RowParams &p, cudaStream_t stream) {
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev >= 64 || !configured[dev]) {
-            e = cudaFuncSetAttribute(row_loss_twopass_kernel<T, 1024, true, true>,
+            e = cudaFuncSetAttribute(row_loss_twopass_kernel<T, 1024, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
             if (e != cudaSuccess) return e;
             if (dev < 64) configured[dev] = true;
@@ -256,7 +249,7 @@ cudaError_t launch_for(const RowParams &p, cudaStream_t stream) {
     }
     const int nvec = p.vocab / (16 / (int)sizeof(T));
     const int stage_vecs = std::min(nvec, kStageBytes / 16);
-    row_loss_twopass_kernel<T, 1024, true, true><<<p.num_tokens, 1024, (size_t)stage_vecs * 16, stream>>>(p, stage_vecs);
+    row_loss_twopass_kernel<T, 1024, true><<<p.num_tokens, 1024, (size_t)stage_vecs * 16, stream>>>(p, stage_vecs);
     return cudaGetLastError();
 }
 
