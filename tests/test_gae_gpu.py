@@ -237,3 +237,21 @@ def test_gae_repeated_calls_are_bit_identical_and_leave_the_workspace_clear():
         assert _workspace_is_clear(gb.num_tokens)
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
+
+
+@pytest.mark.slow
+def test_gae_full_size_repeated_launches_are_bit_identical():
+    """Ten launches on the full workload (2048 chunks, several waves): the tickets go to whichever
+    block asks first and the look-back waits on whatever is published, yet every advantage must
+    come out bit-identical and the workspace clear."""
+    gb = synthetic.make_gae_batch("cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    run = lambda: capi.gae(gb.rewards, gb.values, gb.mask, gb.cu_seqlens, gb.gamma, gb.lam, True,
+                           rollout_ids=gb.rollout_ids, device_status=st)
+    a0 = run().clone()
+    for _ in range(10):
+        a1 = run()
+        torch.cuda.synchronize()
+        assert torch.equal(a0.view(torch.int32), a1.view(torch.int32))
+    assert st.item() == 0
+    assert _workspace_is_clear(gb.num_tokens)

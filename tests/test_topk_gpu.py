@@ -160,3 +160,17 @@ def test_few_distinct_values_long_rows(distinct, order):
 def test_k_around_the_bucket_limit(k, order):
     b = synthetic.make_topk_batch("cuda", rows=5, context=50000, k=k, seed=9)
     _run_and_check(b.scores, b.lengths, k, order)
+
+
+@pytest.mark.slow
+def test_full_size_repeated_launches_are_bit_identical():
+    """Ten launches on the full workload (2 persistent CTAs per SM, every SM busy): the result must
+    not depend on which CTA takes which row or on the timing of the tile copies."""
+    b = synthetic.make_topk_batch("cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    i0, v0 = capi.topk(b.scores, b.k, lengths=b.lengths, device_status=st)
+    for _ in range(10):
+        i1, v1 = capi.topk(b.scores, b.k, lengths=b.lengths, device_status=st)
+        torch.cuda.synchronize()
+        assert torch.equal(i0, i1) and torch.equal(v0.view(torch.int32), v1.view(torch.int32))
+    assert st.item() == 0
