@@ -59,8 +59,9 @@ def test_cases_reduced_length_full_vocab(case_id, n_prompts, lo, hi, dz_rows):
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("V", [1, 2, 13, 1001, 4097, 8961, 40000, 70001, 151553, 200003])
 def test_ragged_vocab_and_padded_rows(dtype, V):
-    # covers every single-read configuration (C = 1, 2, 4, 8) and, at V = 200003,
-    # the two-pass kernel used beyond them
+    # rows up to 128 KB take the 256-thread kernel, longer ones the 1024-thread kernel with a
+    # staged shared-memory prefix (fp32 from V = 40000, bf16 from V = 70001); every V leaves a
+    # ragged tail for some thread, and the padded strides check that columns >= V stay untouched
     lengths = _lengths(0, 1, 3, 40)
     ld = synthetic.padded_ld(V, dtype) + (64 if V % 2 else 0)
     b = synthetic.make_batch(0, "cuda", lengths=lengths, vocab=V, ld=ld, case_overrides={"dtype": dtype})
@@ -141,7 +142,7 @@ def test_bad_targets_are_flagged_and_excluded():
 
 
 def test_nonfinite_and_malformed_offsets_raise_device_bits():
-    for dtype, V in (("f32", 4096), ("bf16", 200003)):  # single-read and two-pass kernels
+    for dtype, V in (("f32", 4096), ("bf16", 200003)):  # the short-row and the long-row kernel
         for bad in (float("nan"), float("inf")):
             b = synthetic.make_batch(0, "cuda", lengths=_lengths(0, 1, 4, 20), vocab=V,
                                      case_overrides={"dtype": dtype})
@@ -214,8 +215,8 @@ def test_profile_and_launch_count():
 
 
 def test_alternating_vocab_sizes_on_one_kernel_configuration():
-    # the same cluster configuration serves V = 151552 and V = 70001 with different
-    # shared-memory sizes; launching them in turn must keep working
+    # the long-row kernel serves V = 151552 and V = 70001 with different dynamic shared-memory
+    # sizes (its staged prefix); launching them in turn must keep working
     for V in (151552, 70001, 151552, 70001):
         b = synthetic.make_batch(2, "cuda", lengths=_lengths(2, 1, 8, 24), vocab=V)
         _, out, bits = _run(b)
