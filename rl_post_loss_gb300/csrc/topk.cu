@@ -814,14 +814,6 @@ __device__ __forceinline__ int tile_elem(int t, int q) {
     return t * kTile + 4 * ((q >> 2) * kThreads + (int)threadIdx.x) + (q & 3);
 }
 
-// A bulk copy of `bytes` from global memory into shared memory, completing on mbarrier `bar`, with
-// the default L2 policy (an evict-first policy measured 1% slower here).
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
 // Appends this thread's scores of tile t whose key reaches the bound (the test on the score itself,
 // see set_threshold) to the buffer, one shared atomic per warp; with slice >= 0, only the scores at
 // the tile's positions [512 slice, 512 slice + 512). Entries that would land at kCap or beyond are
@@ -1028,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
         const float *src = cursor_src(p, ld_cur, bytes);
         const uint32_t bar = ptx::smem_u32(&s.full[stage]);
         ptx::mbar_arrive_expect_tx(bar, bytes);
-        bulk_copy(ptx::smem_u32(s.ring[stage]), src, bytes, bar);
+        ptx::bulk_g2s(ptx::smem_u32(s.ring[stage]), src, bytes, bar);  // default L2 policy: 1% faster than evict-first
         ++ld_cur.tile;
     };
     if (tid == 0) {
