@@ -820,7 +820,7 @@ __device__ __forceinline__ int tile_elem(int t, int q) {
 // not written. Records where the warp's append started in warp_base and returns the buffer count
 // right after it (0 when the warp appends nothing).
 __device__ __forceinline__ int filter_append(TopkSmem &s, const float (&vals)[kPer], int t, int n, float thr,
-                                             int mode, int slice) {
+                                             int mode, int slice, int stage = -1) {
     const int lane = threadIdx.x & 31;
     uint32_t keepm = 0u;
     if (mode == 0 && (t + 1) * kTile <= n) {  // a full tile and a plain threshold: one compare per score
@@ -851,9 +851,15 @@ __device__ __forceinline__ int filter_append(TopkSmem &s, const float (&vals)[kP
         const int pos = base + __popc(m & ((1u << lane) - 1u));
         if (c != 0 && pos < kCap) {
             const int q = __ffs(keepm) - 1;
-            float v = vals[0];
+            const int o = 4 * (int)threadIdx.x + 4 * kThreads * (q >> 2) + (q & 3);  // offset within the tile
+            float v;
+            if (stage >= 0) {  // the tile is in the ring: read the one score back
+                v = s.ring[stage][o];
+            } else {
+                v = vals[0];
 #pragma unroll
-            for (int qq = 1; qq < kPer; ++qq) v = q == qq ? vals[qq] : v;
+                for (int qq = 1; qq < kPer; ++qq) v = q == qq ? vals[qq] : v;
+            }
             s.cb.key[pos] = __float_as_uint(v);  // raw bits; the next compaction makes the key
             s.cb.idx[pos] = (uint32_t)(tile_elem(t, 0) + 4 * kThreads * (q >> 2) + (q & 3));
         }
@@ -1080,7 +1086,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
                     const float4 v = tile4[j * kThreads + tid];
                     vals[4 * j] = v.x, vals[4 * j + 1] = v.y, vals[4 * j + 2] = v.z, vals[4 * j + 3] = v.w;
                 }
-                after_add = filter_append(s, vals, t, n, thr, mode, -1);
+                after_add = filter_append(s, vals, t, n, thr, mode, -1, st);
             }
             if (tid == 0) wait_tile(g + 1u);
             // The next tile has landed. Whether the buffer needs attention is decided by the barrier
