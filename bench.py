@@ -41,6 +41,9 @@ def parse_args():
                          "GAE; topk: deterministic top-k")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-chunks", type=int, default=8,
+                    help="loss cases 0-3: logits row blocks of the host-input call timed as e2e (each computed as "
+                         "soon as it lands); 0 = copy every input first, then the device call")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prompts", type=int, default=0,
@@ -376,9 +379,11 @@ def main():
     achieved = bytes_per_launch / (row_avg_ms / 1e3) / 1e9
     traffic = kernel_traffic("row_loss", args.case)
 
-    # end to end through the public API: pinned host inputs -> device, call, loss -> host
-    host = {k: getattr(batch, k).cpu().pin_memory() for k in
-            ("logits", "targets", "logp_old", "logp_infer", "mask", "cu_seqlens", "rewards_or_adv")}
+    # end to end through the public API: pinned host inputs -> device, call, loss -> host. With
+    # --e2e-chunks N > 0 the host-input entry point copies the logits in N row blocks and computes
+    # each block as soon as it lands; with 0, every input is copied first and the device call follows.
+    dev_in = capi.batch_inputs(batch)
+    host = {k: t.cpu().pin_memory() for k, t in dev_in.items()}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     loss_host = torch.empty(1, dtype=torch.float64).pin_memory()
     e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -386,9 +391,12 @@ def main():
         if k == 1:
             torch.cuda.synchronize()
             e_start.record(stream)
-        for name, t in host.items():
-            getattr(batch, name).copy_(t, non_blocking=True)
-        capi.run_batch(rl, batch, out)
+        if args.e2e_chunks > 0:
+            capi.run_batch_from_host(rl, host, dev_in, out, num_chunks=args.e2e_chunks)
+        else:
+            for name, t in host.items():
+                dev_in[name].copy_(t, non_blocking=True)
+            capi.run_batch(rl, batch, out)
         loss_host.copy_(out["loss_f64"], non_blocking=True)
         stream.synchronize()
         _ = float(loss_host[0])
@@ -417,7 +425,9 @@ def main():
                 "kernel_ms": {k: v[1] / max(1, v[0]) for k, v in prof.items()},
                 "clocks": clocks.summary(),
                 "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                        "d2h_bytes_per_step": 8, "ms_per_step": e2e_ms},
+                        "d2h_bytes_per_step": 8, "ms_per_step": e2e_ms,
+                        "call": ("rl_loss_forward_backward_from_host, %d logits blocks" % args.e2e_chunks
+                                 if args.e2e_chunks > 0 else "copies, then rl_loss_forward_backward")},
                 "gpu_launches": launches, "device_status": capi.status_bits_to_names(bits),
                 "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)

@@ -189,6 +189,31 @@ RL_LOSS_API rl_status rl_loss_destroy(rl_loss_t handle);
 RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t handle, const rl_loss_inputs *inputs,
                                                const rl_loss_outputs *outputs, void *stream);
 
+/* The same pass for inputs that start in HOST memory, with the host-to-device
+ * copy overlapped with the computation. `host` holds the batch in host memory
+ * (page-locked, e.g. cudaHostAlloc, for the copies to run asynchronously and
+ * overlap); `device` names device buffers of the same shapes that receive it
+ * (device->ld_logits may differ from host->ld_logits; num_tokens / num_seqs
+ * are taken from `host` and those of `device` are ignored). Both follow the
+ * rules of rl_loss_inputs; outputs as for rl_loss_forward_backward.
+ * The small per-token and per-response arrays are copied on `stream` first.
+ * The logits go in `num_chunks` blocks of consecutive rows (1 <= num_chunks
+ * <= 64, fewer if T is smaller) on a copy stream of the handle, which starts
+ * after the work enqueued on `stream` before the call; the token preparation
+ * and the row kernel of a block start on `stream` as soon as that block has
+ * landed, so all but the last block's computation hides under the copy. The
+ * two reductions follow on `stream`, which at the end depends on every copy.
+ * Results are bit-identical to rl_loss_forward_backward on the copied inputs
+ * (every row is computed the same way; the reductions run once over all rows).
+ * The first call on a handle creates its copy stream and events (kept until
+ * rl_loss_destroy); nothing is allocated on the device. Returns without
+ * synchronising: the host buffers must stay unchanged until `stream` has
+ * passed the call. Not for use inside a CUDA graph capture. Errors as for
+ * rl_loss_forward_backward, checked before anything is enqueued. */
+RL_LOSS_API rl_status rl_loss_forward_backward_from_host(rl_loss_t handle, const rl_loss_inputs *host,
+                                                         const rl_loss_inputs *device, const rl_loss_outputs *outputs,
+                                                         int32_t num_chunks, void *stream);
+
 /* ---- Sequence-chunked output projection + loss ------------------------------
  * "GLM-5: from Vibe Coding to Agentic Engineering", section 2.4.1, "Sequence-
  * chunked output projection for peak memory reduction" (also "GLM-5 Notes",

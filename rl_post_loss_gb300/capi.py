@@ -92,6 +92,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "rl_loss_create": ([ctypes.POINTER(rl_loss_config), ctypes.POINTER(P)], st),
         "rl_loss_destroy": ([P], st),
         "rl_loss_forward_backward": ([P, ctypes.POINTER(rl_loss_inputs), ctypes.POINTER(rl_loss_outputs), P], st),
+        "rl_loss_forward_backward_from_host": ([P, ctypes.POINTER(rl_loss_inputs), ctypes.POINTER(rl_loss_inputs),
+                                                ctypes.POINTER(rl_loss_outputs), ctypes.c_int32, P], st),
         "rl_loss_get_device_status": ([P, P, ctypes.POINTER(ctypes.c_uint32)], st),
         "rl_loss_status_string": ([st], ctypes.c_char_p),
         "rl_loss_profile_start": ([P, ctypes.c_int32], st),
@@ -148,6 +150,12 @@ def rl_loss_destroy(handle) -> None:
 def rl_loss_forward_backward(handle, inputs: rl_loss_inputs, outputs: rl_loss_outputs, stream: int) -> int:
     return load().rl_loss_forward_backward(handle, ctypes.byref(inputs), ctypes.byref(outputs),
                                            ctypes.c_void_p(stream))
+
+
+def rl_loss_forward_backward_from_host(handle, host: rl_loss_inputs, device: rl_loss_inputs,
+                                       outputs: rl_loss_outputs, num_chunks: int, stream: int) -> int:
+    return load().rl_loss_forward_backward_from_host(handle, ctypes.byref(host), ctypes.byref(device),
+                                                     ctypes.byref(outputs), num_chunks, ctypes.c_void_p(stream))
 
 
 def rl_loss_get_device_status(handle, stream: int) -> int:
@@ -333,6 +341,29 @@ class RlLoss:
             raise RlLossError(code, "rl_loss_forward_backward (%s)" % rl_loss_last_cuda_error(self.handle))
         _check(code, "rl_loss_forward_backward")
 
+    def forward_backward_from_host(self, host: dict, device: dict, *, loss, dlogits, num_chunks: int = 8,
+                                   loss_f64=None, logp=None, entropy=None, flags=None, seq_adv=None, counts=None,
+                                   mean_entropy=None, stream=None) -> None:
+        """Enqueue one forward+backward whose inputs start in host memory: ``host`` and ``device``
+        map the input names (logits, targets, logp_old, logp_infer, mask, cu_seqlens,
+        rewards_or_adv) to pinned CPU tensors and to CUDA tensors of the same shapes that receive
+        them. The logits go over in ``num_chunks`` row blocks, each computed as soon as it lands."""
+        import torch
+
+        def inputs(d):
+            lg = d["logits"]
+            return rl_loss_inputs(int(d["targets"].shape[0]), int(d["cu_seqlens"].shape[0]) - 1,
+                                  int(lg.stride(0)) if lg.dim() == 2 else 0, _ptr(lg), _ptr(d["targets"]),
+                                  _ptr(d["logp_old"]), _ptr(d["logp_infer"]), _ptr(d["mask"]), _ptr(d["cu_seqlens"]),
+                                  _ptr(d["rewards_or_adv"]))
+        out = rl_loss_outputs(_ptr(loss), _ptr(loss_f64), _ptr(dlogits),
+                              int(dlogits.stride(0)) if dlogits.dim() == 2 else 0, _ptr(logp), _ptr(entropy),
+                              _ptr(flags), _ptr(seq_adv), _ptr(counts), _ptr(mean_entropy))
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        self._raise(rl_loss_forward_backward_from_host(self.handle, inputs(host), inputs(device), out, num_chunks,
+                                                       stream), "rl_loss_forward_backward_from_host")
+
     def _raise(self, code: int, what: str):
         if code == CODES["RL_ERR_CUDA"]:
             raise RlLossError(code, "%s (%s)" % (what, rl_loss_last_cuda_error(self.handle)))
@@ -423,6 +454,22 @@ def run_batch(rl: RlLoss, batch, outputs: dict, stream=None) -> dict:
     adv = batch.token_adv if (batch.adv_mode >= RL_ADV_PER_TOKEN) else batch.rewards_or_adv
     rl.forward_backward(batch.logits, batch.targets, batch.logp_old, batch.logp_infer, batch.mask,
                         batch.cu_seqlens, adv, stream=stream, **outputs)
+    return outputs
+
+
+INPUT_NAMES = ("logits", "targets", "logp_old", "logp_infer", "mask", "cu_seqlens", "rewards_or_adv")
+
+
+def batch_inputs(batch) -> dict:
+    """The input tensors of ``batch`` by name (the advantage array the batch's mode reads)."""
+    adv = batch.token_adv if (batch.adv_mode >= RL_ADV_PER_TOKEN) else batch.rewards_or_adv
+    return {n: (adv if n == "rewards_or_adv" else getattr(batch, n)) for n in INPUT_NAMES}
+
+
+def run_batch_from_host(rl: RlLoss, host: dict, device: dict, outputs: dict, num_chunks: int = 8,
+                        stream=None) -> dict:
+    """One forward+backward from pinned host inputs ``host`` into the device buffers ``device``."""
+    rl.forward_backward_from_host(host, device, num_chunks=num_chunks, stream=stream, **outputs)
     return outputs
 
 

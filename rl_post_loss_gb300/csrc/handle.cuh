@@ -21,7 +21,8 @@ enum RlKernelClass {
 };
 static const char *const kKernelNames[kNumKernels] = {"seg_prep",     "token_prep", "row_loss",  "seg_reduce",
                                                       "final_reduce", "proj_gemm",  "proj_rows", "cublas_gemm"};
-constexpr size_t kProfSlotsPerCall = 160;  // enough for a projection call of 32 chunks
+constexpr size_t kProfSlotsPerCall = 160;  // enough for a projection call of 32 chunks (or a host call of 64 blocks)
+constexpr int kMaxCopyChunks = 64;         // logits blocks of rl_loss_forward_backward_from_host
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -84,4 +85,37 @@ struct rl_loss_handle_s {
         if (slot >= 0) cudaEventRecord(prof_events[2 * (size_t)slot + 1], stream);
     }
     void proj_release();  // defined with the projection path
+
+    // host-input path (rl_loss_forward_backward_from_host): a copy stream and its events, made on first use
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t copy_entry = nullptr;
+    cudaEvent_t copy_done[kMaxCopyChunks] = {};
+
+    cudaError_t copy_setup() {
+        if (copy_stream) return cudaSuccess;
+        cudaStream_t st = nullptr;
+        cudaError_t e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+        if (e != cudaSuccess) return e;
+        cudaEvent_t ev[kMaxCopyChunks + 1] = {};
+        int made = 0;
+        for (; made < kMaxCopyChunks + 1 && e == cudaSuccess; ++made)
+            e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            for (int i = 0; i < made; ++i)
+                if (ev[i]) cudaEventDestroy(ev[i]);
+            cudaStreamDestroy(st);
+            return e;
+        }
+        copy_entry = ev[0];
+        for (int i = 0; i < kMaxCopyChunks; ++i) copy_done[i] = ev[i + 1];
+        copy_stream = st;
+        return cudaSuccess;
+    }
+    void copy_release() {
+        if (!copy_stream) return;
+        cudaEventDestroy(copy_entry);
+        for (cudaEvent_t e : copy_done) cudaEventDestroy(e);
+        cudaStreamDestroy(copy_stream);
+        copy_stream = nullptr;
+    }
 };

@@ -1,6 +1,7 @@
 // C ABI of the fused GRPO + IcePop loss (declared in include/rl_loss.h):
 // handle life cycle, host-side validation, workspace layout, launches,
 // device status and event-based kernel timing.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -85,6 +86,194 @@ static rlk::LossConsts loss_consts(const rl_loss_config &c) {
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The parameters of one loss call's kernels.
+struct LossLaunch {
+    rlk::SeqPrepParams sp;
+    rlk::TokenPrepParams tp;
+    rlk::RowParams rp;
+    rlk::ReduceParams rd;
+    int T;
+    int es;
+};
+
+// Checks what rl_loss_forward_backward requires of the handle, `in` and `out`, and fills the
+// parameters of its kernels.
+static rl_status prepare_call(rl_loss_handle_s *h, const rl_loss_inputs *in, const rl_loss_outputs *out,
+                              LossLaunch &L) {
+    if (!h || !in || !out) return RL_ERR_INVALID_ARG;
+    int cur = -1;
+    if (cudaError_t e0 = cudaGetDevice(&cur); e0 != cudaSuccess) {
+        h->last_cuda_error = e0;
+        return RL_ERR_CUDA;
+    }
+    if (cur != h->device) return RL_ERR_DEVICE;
+    const rl_loss_config &c = h->cfg;
+    const int T = in->num_tokens, S = in->num_seqs, V = c.vocab_size;
+    const int es = elem_size(c.logits_dtype);
+    if (T < 0 || S < 1 || S % c.group_size != 0) return RL_ERR_SHAPE;
+    if (T > c.max_tokens || S > c.max_seqs) return RL_ERR_CAPACITY;
+    if (!in->cu_seqlens || !in->rewards_or_adv || !out->loss) return RL_ERR_INVALID_ARG;
+    if (T > 0) {
+        if (!in->logits || !in->targets || !in->logp_old || !in->logp_infer || !in->mask || !out->dlogits)
+            return RL_ERR_INVALID_ARG;
+        if (in->ld_logits < V || out->ld_dlogits < V) return RL_ERR_SHAPE;
+        if (!aligned16(in->logits) || !aligned16(out->dlogits) || (in->ld_logits * es) % 16 != 0 ||
+            (out->ld_dlogits * es) % 16 != 0)
+            return RL_ERR_ALIGNMENT;
+        if (in->logits == out->dlogits && in->ld_logits != out->ld_dlogits) return RL_ERR_INVALID_ARG;
+    }
+    L.T = T;
+    L.es = es;
+
+    rlk::SeqPrepParams &sp = L.sp;
+    sp = rlk::SeqPrepParams{};
+    sp.cu_seqlens = in->cu_seqlens;
+    sp.mask = in->mask;
+    sp.rewards_or_adv = in->rewards_or_adv;
+    sp.num_seqs = S;
+    sp.num_tokens = T;
+    sp.group_size = c.group_size;
+    sp.adv_mode = c.adv_mode;
+    sp.std_unbiased = c.std_unbiased;
+    sp.loss_norm = c.loss_norm;
+    sp.adv_eps = c.adv_eps;
+    sp.seq_adv = h->seq_adv;
+    sp.seq_w = h->seq_w;
+    sp.seq_w64 = h->seq_w64;
+    sp.seq_n = h->seq_n;
+    sp.seq_adv_out = out->seq_adv;
+    sp.status = h->status;
+
+    rlk::TokenPrepParams &tp = L.tp;
+    tp = rlk::TokenPrepParams{};
+    tp.logits = in->logits;
+    tp.ld_logits = in->ld_logits;
+    tp.row0 = 0;
+    tp.rows = T;
+    tp.logits_dtype = c.logits_dtype;
+    tp.targets = in->targets;
+    tp.logp_old = in->logp_old;
+    tp.logp_infer = in->logp_infer;
+    tp.mask = in->mask;
+    tp.cu_seqlens = in->cu_seqlens;
+    tp.num_seqs = S;
+    tp.num_tokens = T;
+    tp.vocab = V;
+    tp.seq_adv = h->seq_adv;
+    tp.seq_w = h->seq_w;
+    tp.token_adv = c.adv_mode == RL_ADV_PER_TOKEN ? in->rewards_or_adv : nullptr;
+    tp.c = h->consts;
+    tp.rec = h->tok_rec;
+    tp.meta = h->tok_meta;
+    tp.status = h->status;
+
+    rlk::RowParams &rp = L.rp;
+    rp = rlk::RowParams{};
+    rp.logits = in->logits;
+    rp.ld_logits = in->ld_logits;
+    rp.dlogits = out->dlogits;
+    rp.ld_dlogits = out->ld_dlogits;
+    rp.rec = h->tok_rec;
+    rp.meta = h->tok_meta;
+    rp.teacher = c.adv_mode == RL_ADV_TEACHER_LOGP ? in->rewards_or_adv : nullptr;
+    rp.num_tokens = T;
+    rp.vocab = V;
+    rp.c = h->consts;
+    rp.logp_out = out->logp;
+    rp.entropy_out = out->entropy ? out->entropy : h->tok_ent;
+    rp.flags_out = out->flags ? out->flags : h->tok_flags;
+    rp.tok_obj = h->tok_obj;
+    rp.status = h->status;
+
+    rlk::ReduceParams &rd = L.rd;
+    rd = rlk::ReduceParams{};
+    rd.cu_seqlens = in->cu_seqlens;
+    rd.num_seqs = S;
+    rd.num_tokens = T;
+    rd.tok_obj = h->tok_obj;
+    rd.entropy = rp.entropy_out;
+    rd.flags = rp.flags_out;
+    rd.seq_w64 = h->seq_w64;
+    rd.seq_n = h->seq_n;
+    rd.seq_obj = h->seq_obj;
+    rd.seq_ent = h->seq_ent;
+    rd.seq_cnt = h->seq_cnt;
+    rd.loss = out->loss;
+    rd.loss_f64 = out->loss_f64;
+    rd.counts = out->counts;
+    rd.mean_entropy = out->mean_entropy;
+    rd.status = h->status;
+    return RL_OK;
+}
+
+// The token preparation and row kernel parameters restricted to tokens [r0, r1).
+static void restrict_rows(LossLaunch &B, const LossLaunch &L, int r0, int r1) {
+    B = L;
+    const size_t es = (size_t)L.es;
+    B.tp.logits = static_cast<const char *>(L.tp.logits) + (size_t)r0 * (size_t)L.tp.ld_logits * es;
+    B.tp.row0 = r0;
+    B.tp.rows = r1 - r0;
+    rlk::RowParams &rp = B.rp;
+    rp.logits = static_cast<const char *>(L.rp.logits) + (size_t)r0 * (size_t)L.rp.ld_logits * es;
+    rp.dlogits = static_cast<char *>(L.rp.dlogits) + (size_t)r0 * (size_t)L.rp.ld_dlogits * es;
+    rp.rec = L.rp.rec + r0;
+    rp.meta = L.rp.meta + r0;
+    if (L.rp.teacher) rp.teacher = L.rp.teacher + r0;
+    if (L.rp.logp_out) rp.logp_out = L.rp.logp_out + r0;
+    rp.entropy_out = L.rp.entropy_out + r0;
+    rp.flags_out = L.rp.flags_out + r0;
+    rp.tok_obj = L.rp.tok_obj + r0;
+    rp.num_tokens = r1 - r0;
+}
+
+// Enqueues one loss call on `stream`. With nb > 0 blocks (rows[b] .. rows[b + 1]), the token
+// preparation and row kernel of block b wait for h->copy_done[b] first.
+static rl_status launch_loss(rl_loss_handle_s *h, const LossLaunch &L, const int *rows, int nb, cudaStream_t stream) {
+    const rl_loss_config &c = h->cfg;
+    cudaError_t err;
+    auto failed = [&](cudaError_t e) {
+        h->last_cuda_error = e;
+        return RL_ERR_CUDA;
+    };
+    int slot = h->prof_begin(kSegPrep, stream);
+    err = rlk::launch_seg_prep(L.sp, stream);
+    if (err == cudaSuccess && c.loss_norm == RL_NORM_PER_TOKEN) err = rlk::launch_seg_token_norm(L.sp, stream);
+    h->prof_end(slot, stream);
+    if (err != cudaSuccess) return failed(err);
+    int64_t row_launches = 0;
+    const int blocks = nb > 0 ? nb : 1;
+    for (int b = 0; b < blocks; ++b) {
+        LossLaunch B;
+        if (nb > 0) {
+            restrict_rows(B, L, rows[b], rows[b + 1]);
+            err = cudaStreamWaitEvent(stream, h->copy_done[b], 0);
+            if (err != cudaSuccess) return failed(err);
+        } else {
+            B = L;
+        }
+        if (B.tp.rows <= 0) continue;
+        slot = h->prof_begin(kTokenPrep, stream);
+        err = rlk::launch_token_prep(B.tp, stream);
+        h->prof_end(slot, stream);
+        if (err != cudaSuccess) return failed(err);
+        slot = h->prof_begin(kRowLoss, stream);
+        err = rlk::launch_row_loss(B.rp, c.logits_dtype, stream);
+        h->prof_end(slot, stream);
+        if (err != cudaSuccess) return failed(err);
+        row_launches += 2;
+    }
+    slot = h->prof_begin(kSegReduce, stream);
+    err = rlk::launch_seg_reduce(L.rd, stream);
+    h->prof_end(slot, stream);
+    if (err != cudaSuccess) return failed(err);
+    slot = h->prof_begin(kFinalReduce, stream);
+    err = rlk::launch_final_reduce(L.rd, stream);
+    h->prof_end(slot, stream);
+    if (err != cudaSuccess) return failed(err);
+    h->launches += 3 + row_launches + (c.loss_norm == RL_NORM_PER_TOKEN ? 1 : 0);
+    return RL_OK;
+}
+
 extern "C" {
 
 RL_LOSS_API int32_t rl_loss_version(void) { return 100; }
@@ -160,6 +349,7 @@ RL_LOSS_API rl_status rl_loss_destroy(rl_loss_t h) {
     cudaDeviceSynchronize();
     for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
     h->proj_release();
+    h->copy_release();
     cudaError_t err = cudaFree(h->ws);
     if (cur != h->device && cur >= 0) cudaSetDevice(cur);
     delete h;
@@ -168,133 +358,85 @@ RL_LOSS_API rl_status rl_loss_destroy(rl_loss_t h) {
 
 RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t h, const rl_loss_inputs *in, const rl_loss_outputs *out,
                                                void *stream_ptr) {
-    if (!h || !in || !out) return RL_ERR_INVALID_ARG;
-    int cur = -1;
-    if (cudaError_t e0 = cudaGetDevice(&cur); e0 != cudaSuccess) {
-        h->last_cuda_error = e0;
-        return RL_ERR_CUDA;
-    }
-    if (cur != h->device) return RL_ERR_DEVICE;
+    LossLaunch L;
+    const rl_status st = prepare_call(h, in, out, L);
+    if (st != RL_OK) return st;
+    return launch_loss(h, L, nullptr, 0, reinterpret_cast<cudaStream_t>(stream_ptr));
+}
+
+RL_LOSS_API rl_status rl_loss_forward_backward_from_host(rl_loss_t h, const rl_loss_inputs *host,
+                                                         const rl_loss_inputs *dev, const rl_loss_outputs *out,
+                                                         int32_t num_chunks, void *stream_ptr) {
+    if (!h || !host || !dev || !out) return RL_ERR_INVALID_ARG;
+    if (num_chunks < 1 || num_chunks > kMaxCopyChunks) return RL_ERR_INVALID_ARG;
     const rl_loss_config &c = h->cfg;
-    const int T = in->num_tokens, S = in->num_seqs, V = c.vocab_size;
+    const int T = host->num_tokens, S = host->num_seqs, V = c.vocab_size;
     const int es = elem_size(c.logits_dtype);
-    if (T < 0 || S < 1 || S % c.group_size != 0) return RL_ERR_SHAPE;
-    if (T > c.max_tokens || S > c.max_seqs) return RL_ERR_CAPACITY;
-    if (!in->cu_seqlens || !in->rewards_or_adv || !out->loss) return RL_ERR_INVALID_ARG;
+    // the device side must pass every check of rl_loss_forward_backward, with the host's sizes
+    rl_loss_inputs d = *dev;
+    d.num_tokens = T;
+    d.num_seqs = S;
+    LossLaunch L;
+    rl_status st = prepare_call(h, &d, out, L);
+    if (st != RL_OK) return st;
+    if (!host->cu_seqlens || !host->rewards_or_adv) return RL_ERR_INVALID_ARG;
     if (T > 0) {
-        if (!in->logits || !in->targets || !in->logp_old || !in->logp_infer || !in->mask || !out->dlogits)
+        if (!host->logits || !host->targets || !host->logp_old || !host->logp_infer || !host->mask)
             return RL_ERR_INVALID_ARG;
-        if (in->ld_logits < V || out->ld_dlogits < V) return RL_ERR_SHAPE;
-        if (!aligned16(in->logits) || !aligned16(out->dlogits) || (in->ld_logits * es) % 16 != 0 ||
-            (out->ld_dlogits * es) % 16 != 0)
-            return RL_ERR_ALIGNMENT;
-        if (in->logits == out->dlogits && in->ld_logits != out->ld_dlogits) return RL_ERR_INVALID_ARG;
+        if (host->ld_logits < V) return RL_ERR_SHAPE;
     }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
-
-    rlk::SeqPrepParams sp{};
-    sp.cu_seqlens = in->cu_seqlens;
-    sp.mask = in->mask;
-    sp.rewards_or_adv = in->rewards_or_adv;
-    sp.num_seqs = S;
-    sp.num_tokens = T;
-    sp.group_size = c.group_size;
-    sp.adv_mode = c.adv_mode;
-    sp.std_unbiased = c.std_unbiased;
-    sp.loss_norm = c.loss_norm;
-    sp.adv_eps = c.adv_eps;
-    sp.seq_adv = h->seq_adv;
-    sp.seq_w = h->seq_w;
-    sp.seq_w64 = h->seq_w64;
-    sp.seq_n = h->seq_n;
-    sp.seq_adv_out = out->seq_adv;
-    sp.status = h->status;
-
-    rlk::TokenPrepParams tp{};
-    tp.logits = in->logits;
-    tp.ld_logits = in->ld_logits;
-    tp.row0 = 0;
-    tp.rows = T;
-    tp.logits_dtype = c.logits_dtype;
-    tp.targets = in->targets;
-    tp.logp_old = in->logp_old;
-    tp.logp_infer = in->logp_infer;
-    tp.mask = in->mask;
-    tp.cu_seqlens = in->cu_seqlens;
-    tp.num_seqs = S;
-    tp.num_tokens = T;
-    tp.vocab = V;
-    tp.seq_adv = h->seq_adv;
-    tp.seq_w = h->seq_w;
-    tp.token_adv = c.adv_mode == RL_ADV_PER_TOKEN ? in->rewards_or_adv : nullptr;
-    tp.c = h->consts;
-    tp.rec = h->tok_rec;
-    tp.meta = h->tok_meta;
-    tp.status = h->status;
-
-    rlk::RowParams rp{};
-    rp.logits = in->logits;
-    rp.ld_logits = in->ld_logits;
-    rp.dlogits = out->dlogits;
-    rp.ld_dlogits = out->ld_dlogits;
-    rp.rec = h->tok_rec;
-    rp.meta = h->tok_meta;
-    rp.teacher = c.adv_mode == RL_ADV_TEACHER_LOGP ? in->rewards_or_adv : nullptr;
-    rp.num_tokens = T;
-    rp.vocab = V;
-    rp.c = h->consts;
-    rp.logp_out = out->logp;
-    rp.entropy_out = out->entropy ? out->entropy : h->tok_ent;
-    rp.flags_out = out->flags ? out->flags : h->tok_flags;
-    rp.tok_obj = h->tok_obj;
-    rp.status = h->status;
-
-    rlk::ReduceParams rd{};
-    rd.cu_seqlens = in->cu_seqlens;
-    rd.num_seqs = S;
-    rd.num_tokens = T;
-    rd.tok_obj = h->tok_obj;
-    rd.entropy = rp.entropy_out;
-    rd.flags = rp.flags_out;
-    rd.seq_w64 = h->seq_w64;
-    rd.seq_n = h->seq_n;
-    rd.seq_obj = h->seq_obj;
-    rd.seq_ent = h->seq_ent;
-    rd.seq_cnt = h->seq_cnt;
-    rd.loss = out->loss;
-    rd.loss_f64 = out->loss_f64;
-    rd.counts = out->counts;
-    rd.mean_entropy = out->mean_entropy;
-    rd.status = h->status;
-
-    cudaError_t err;
     auto failed = [&](cudaError_t e) {
         h->last_cuda_error = e;
         return RL_ERR_CUDA;
     };
-    int slot = h->prof_begin(kSegPrep, stream);
-    err = rlk::launch_seg_prep(sp, stream);
-    if (err == cudaSuccess && c.loss_norm == RL_NORM_PER_TOKEN) err = rlk::launch_seg_token_norm(sp, stream);
-    h->prof_end(slot, stream);
+    cudaError_t err = h->copy_setup();
     if (err != cudaSuccess) return failed(err);
-    slot = h->prof_begin(kTokenPrep, stream);
-    err = rlk::launch_token_prep(tp, stream);
-    h->prof_end(slot, stream);
-    if (err != cudaSuccess) return failed(err);
-    slot = h->prof_begin(kRowLoss, stream);
-    err = rlk::launch_row_loss(rp, c.logits_dtype, stream);
-    h->prof_end(slot, stream);
-    if (err != cudaSuccess) return failed(err);
-    slot = h->prof_begin(kSegReduce, stream);
-    err = rlk::launch_seg_reduce(rd, stream);
-    h->prof_end(slot, stream);
-    if (err != cudaSuccess) return failed(err);
-    slot = h->prof_begin(kFinalReduce, stream);
-    err = rlk::launch_final_reduce(rd, stream);
-    h->prof_end(slot, stream);
-    if (err != cudaSuccess) return failed(err);
-    h->launches += ((T > 0) ? 5 : 3) + (c.loss_norm == RL_NORM_PER_TOKEN ? 1 : 0);
-    return RL_OK;
+
+    // the logits blocks start once the work enqueued before this call (which may still read the
+    // device buffers) is done
+    const int nb = T > 0 ? std::min(num_chunks, T) : 0;
+    if (nb > 0) {
+        err = cudaEventRecord(h->copy_entry, stream);
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(h->copy_stream, h->copy_entry, 0);
+        if (err != cudaSuccess) return failed(err);
+    }
+    // the small arrays, on the caller's stream
+    const bool adv_per_token = c.adv_mode == RL_ADV_PER_TOKEN || c.adv_mode == RL_ADV_TEACHER_LOGP;
+    const size_t tok = (size_t)T;
+    struct Part {
+        void *dst;
+        const void *src;
+        size_t bytes;
+    } parts[] = {
+        {const_cast<int32_t *>(d.cu_seqlens), host->cu_seqlens, ((size_t)S + 1) * sizeof(int32_t)},
+        {const_cast<float *>(d.rewards_or_adv), host->rewards_or_adv, (adv_per_token ? tok : (size_t)S) * sizeof(float)},
+        {const_cast<int32_t *>(d.targets), host->targets, tok * sizeof(int32_t)},
+        {const_cast<float *>(d.logp_old), host->logp_old, tok * sizeof(float)},
+        {const_cast<float *>(d.logp_infer), host->logp_infer, tok * sizeof(float)},
+        {const_cast<uint8_t *>(d.mask), host->mask, tok * sizeof(uint8_t)},
+    };
+    for (const Part &q : parts) {
+        if (q.bytes == 0 || !q.dst) continue;
+        err = cudaMemcpyAsync(q.dst, q.src, q.bytes, cudaMemcpyHostToDevice, stream);
+        if (err != cudaSuccess) return failed(err);
+    }
+    // the logits, block by block, on the copy stream
+    int rows[kMaxCopyChunks + 1];
+    for (int b = 0; b <= nb; ++b) rows[b] = (int)((int64_t)T * b / std::max(nb, 1));
+    for (int b = 0; b < nb; ++b) {
+        const int r0 = rows[b], n = rows[b + 1] - r0;
+        char *dst = const_cast<char *>(static_cast<const char *>(d.logits)) + (size_t)r0 * d.ld_logits * es;
+        const char *src = static_cast<const char *>(host->logits) + (size_t)r0 * host->ld_logits * es;
+        if (host->ld_logits == d.ld_logits)
+            err = cudaMemcpyAsync(dst, src, (size_t)n * d.ld_logits * es, cudaMemcpyHostToDevice, h->copy_stream);
+        else
+            err = cudaMemcpy2DAsync(dst, (size_t)d.ld_logits * es, src, (size_t)host->ld_logits * es, (size_t)V * es,
+                                    (size_t)n, cudaMemcpyHostToDevice, h->copy_stream);
+        if (err == cudaSuccess) err = cudaEventRecord(h->copy_done[b], h->copy_stream);
+        if (err != cudaSuccess) return failed(err);
+    }
+    return launch_loss(h, L, rows, nb, stream);
 }
 
 RL_LOSS_API rl_status rl_loss_get_device_status(rl_loss_t h, void *stream_ptr, uint32_t *bits) {

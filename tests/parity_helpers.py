@@ -1,7 +1,8 @@
 """Comparison of the CUDA path's outputs with the fp64 oracle on the same inputs.
 
 Tolerances (stated for this workload): per-token log-prob and entropy abs 1e-4
-with fp32 logits, 2e-3 with bf16 logits; scalar loss rel 1e-4; dL/dlogits
+with fp32 logits, 2e-3 with bf16 logits; scalar loss rel 1e-4 (plus, for the distillation advantage, the
+first-order effect of the log-prob error on the loss: see distillation_loss_slack); dL/dlogits
 abs 1e-6 + rel 8e-3; pop flags bit-exact; clip flags bit-exact against the
 clip rule applied to the kernel's own fp32 log-prob, and equal to the
 oracle's own decision wherever the oracle's log-prob is not within the
@@ -142,12 +143,37 @@ def check_tokens(batch, run: OracleRun, out: dict, report: dict | None = None):
     return near
 
 
+def distillation_loss_slack(run: OracleRun, out: dict) -> float:
+    """With the distillation advantage A_t = teacher_t - logp_t, every token term
+    depends on the kernel's fp32 log-prob (through r and through A): a log-prob off by
+    d_t moves the term m pop min(r A, clip(r) A) by at most pop max(r, 1 + eps_high)
+    (|A_t| + 1) |d_t| to first order. The loss, which is near zero when A is centred,
+    therefore carries the log-prob error (its own tolerance is absolute) on top of the
+    relative loss tolerance. Returns twice that first-order sum over the tokens, with
+    the measured per-token log-prob differences."""
+    a = run.np
+    T = run.batch.num_tokens
+    if run.p.adv_mode != 3 or T == 0:
+        return 0.0
+    lp = run.tok["logp"]
+    ok = np.isfinite(lp)
+    d = np.where(ok, np.abs(out["logp"].cpu().numpy().astype(np.float64) - np.where(ok, lp, 0.0)), 0.0)
+    lo = a["logp_old"].astype(np.float64)
+    rho = np.exp(lo - a["logp_infer"].astype(np.float64))
+    pop = np.where((run.tok["flags"] & 1) != 0, 1.0 if run.p.pop_indicator else rho, 0.0) * (a["mask"] != 0)
+    r = np.exp(np.where(ok, lp, lo) - lo)
+    A = run.token_adv.astype(np.float64) - np.where(ok, lp, 0.0)
+    w = np.repeat(np.asarray(run.w, np.float64), np.diff(a["cu_seqlens"]))
+    return 2.0 * float(np.sum(w * pop * np.maximum(r, 1.0 + run.p.eps_high) * (np.abs(A) + 1.0) * d))
+
+
 def check_loss(batch, run: OracleRun, out: dict, report: dict | None = None):
     L = float(out["loss_f64"].cpu()[0])
     L32 = float(out["loss"].cpu()[0])
     ref = run.loss
-    assert abs(L - ref) <= TOL_LOSS_REL * abs(ref) + 1e-12, f"loss {L} vs oracle {ref}"
-    assert abs(L32 - ref) <= TOL_LOSS_REL * abs(ref) + 1e-12, f"loss f32 {L32} vs oracle {ref}"
+    tol = TOL_LOSS_REL * abs(ref) + distillation_loss_slack(run, out) + 1e-12
+    assert abs(L - ref) <= tol, f"loss {L} vs oracle {ref}"
+    assert abs(L32 - ref) <= tol, f"loss f32 {L32} vs oracle {ref}"
     if report is not None:
         report.update(loss=L, loss_oracle=ref, loss_rel_err=abs(L - ref) / max(abs(ref), 1e-300))
 
