@@ -208,8 +208,12 @@ RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t handle, const rl_loss_i
  * The first call on a handle creates its copy stream and events (kept until
  * rl_loss_destroy); nothing is allocated on the device. Returns without
  * synchronising: the host buffers must stay unchanged until `stream` has
- * passed the call. Not for use inside a CUDA graph capture. Errors as for
- * rl_loss_forward_backward, checked before anything is enqueued. */
+ * passed the call. Not for use inside a CUDA graph capture. Argument errors
+ * (those of rl_loss_forward_backward for `device` and `outputs`, a NULL host
+ * array, host->ld_logits < V: RL_ERR_SHAPE, num_chunks outside [1, 64]:
+ * RL_ERR_INVALID_ARG) return before anything is enqueued; a copy or launch the
+ * runtime refuses (e.g. a host pointer that is not host memory) returns
+ * RL_ERR_CUDA, possibly after part of the work was enqueued. */
 RL_LOSS_API rl_status rl_loss_forward_backward_from_host(rl_loss_t handle, const rl_loss_inputs *host,
                                                          const rl_loss_inputs *device, const rl_loss_outputs *outputs,
                                                          int32_t num_chunks, void *stream);
