@@ -30,8 +30,10 @@
  *
  * Conventions shared by every entry point:
  *  - Pointers inside rl_loss_inputs / rl_loss_outputs are DEVICE pointers on
- *    the handle's device; the caller owns them. The handle owns only its
- *    workspace, allocated once by rl_loss_create and freed by rl_loss_destroy.
+ *    the handle's device (except the `host` inputs of
+ *    rl_loss_forward_backward_from_host); the caller owns them. The handle owns
+ *    only its workspace, allocated once by rl_loss_create and freed by
+ *    rl_loss_destroy.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream). Work is enqueued asynchronously; no call below synchronises
  *    except rl_loss_get_device_status and rl_loss_profile_read. One handle must
