@@ -93,11 +93,11 @@ struct TopkSmem {
     int broken;     // an internal check failed (the row's result is invalid; no access left its array)
 };
 
-// hist[digit] += 1 for every lane with `valid`, one atomic per distinct digit of the warp (the
-// scores tie often, so many lanes share a digit). All 32 lanes must call it.
-__device__ __forceinline__ void hist_add_warp(uint32_t *hist, uint32_t digit, bool valid) {
-    const unsigned peers = __match_any_sync(kFull, valid ? digit : 0xffffffffu);
-    if (valid && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+// hist[digit] += 1 when `valid`: one plain shared atomic per lane. Gathering the lanes of a warp
+// that share a digit first (__match_any_sync, one atomic per distinct digit) measured slower on
+// this kernel, although the scores tie often.
+__device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t digit, bool valid) {
+    if (valid) atomicAdd(&hist[digit], 1u);
 }
 
 // Finds, over hist[0..kBins), the bin b at which the running count (from the top bin down when
@@ -206,11 +206,11 @@ __device__ Descent radix_descent(TopkSmem &s, const uint32_t *keys, int cnt, int
         const int sh = shift - w;
         for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0u;
         __syncthreads();
-        for (int i0 = tid & ~31; i0 < cnt; i0 += kThreads) {  // warp-uniform trip count
+        for (int i0 = tid & ~31; i0 < cnt; i0 += kThreads) {
             const int i = i0 + (tid & 31);
             const uint32_t k = i < cnt ? keys[i] : 0u;
             const bool in = i < cnt && (shift >= 32 || (k >> shift) == prefix);
-            hist_add_warp(s.hist, (k >> sh) & ((1u << w) - 1u), in);
+            hist_add(s.hist, (k >> sh) & ((1u << w) - 1u), in);
         }
         __syncthreads();
         find_bin(s, (uint32_t)(target - above), true);
@@ -265,7 +265,7 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
                     s.found_before = -1;  // stays -1 only if the invariant broke
                 }
                 __syncthreads();
-                for (int i0 = tid & ~31; i0 < cnt; i0 += kThreads) {  // warp-uniform trip count
+                for (int i0 = tid & ~31; i0 < cnt; i0 += kThreads) {  // warp-uniform trip count: the ballot
                     const int i = i0 + lane;
                     const bool eq = i < cnt && s.cb.key[i] == key_star;
                     const unsigned m = __ballot_sync(kFull, eq);
@@ -302,7 +302,7 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
                     const bool eq = i < cnt && s.cb.key[i] == key_star;
                     const uint32_t ix = eq ? s.cb.idx[i] : 0u;
                     const bool in = eq && (ishift >= 32 || (ix >> ishift) == ipre);
-                    hist_add_warp(s.hist, (ix >> sh) & ((1u << w) - 1u), in);
+                    hist_add(s.hist, (ix >> sh) & ((1u << w) - 1u), in);
                 }
                 __syncthreads();
                 find_bin(s, (uint32_t)(need - ibelow), false);
@@ -547,7 +547,7 @@ __device__ bool bucket_sort(TopkSmem &s, int n, bool by_score) {
     for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0u;
     __syncthreads();
 #pragma unroll
-    for (int j = 0; j < kSortPer; ++j) hist_add_warp(s.hist, digit(c[j]), j * kThreads + tid < n);
+    for (int j = 0; j < kSortPer; ++j) hist_add(s.hist, digit(c[j]), j * kThreads + tid < n);
     __syncthreads();
 
     // bucket starts from the top bin down, and the cost (sum of squared sizes)
@@ -587,17 +587,13 @@ __device__ bool bucket_sort(TopkSmem &s, int n, bool by_score) {
     __syncthreads();
     if (!ok) return false;
 
-    // scatter by bucket: one shared atomic per distinct digit of a warp
+    // scatter by bucket: each entry takes the next slot of its bucket (the order within a bucket is
+    // free, since the ranking below compares the entries)
 #pragma unroll
     for (int j = 0; j < kSortPer; ++j) {
         const bool valid = j * kThreads + tid < n;
         const uint32_t d = digit(c[j]);
-        const unsigned peers = __match_any_sync(kFull, valid ? d : 0xffffffffu);
-        const int leader = __ffs(peers) - 1;
-        uint32_t b0 = 0u;
-        if (valid && lane == leader) b0 = atomicAdd(&s.hist[d], (uint32_t)__popc(peers));
-        b0 = __shfl_sync(kFull, b0, leader);
-        if (valid) s.packed[b0 + __popc(peers & ((1u << lane) - 1u))] = c[j];
+        if (valid) s.packed[atomicAdd(&s.hist[d], 1u)] = c[j];
     }
     __syncthreads();
     // hist[d] is now the end of bucket d, and hist[d + 1] its start (buckets run from the top bin down)
@@ -677,7 +673,8 @@ __device__ bool select_sort_by_score(TopkSmem &s, int kk, int32_t *oi, float *ov
     if (tid == 0) s.found_bin = -1;
     __syncthreads();
 #pragma unroll
-    for (int j = 0; j < kPerT; ++j) hist_add_warp(s.hist, digit(c[j]), j * kThreads + tid < cnt);
+    for (int j = 0; j < kPerT; ++j)
+        if (j * kThreads + tid < cnt) atomicAdd(&s.hist[digit(c[j])], 1u);
     __syncthreads();
 
     // bucket starts from the top bin down, the cost (sum of squared sizes), and the bucket holding
@@ -731,12 +728,7 @@ __device__ bool select_sort_by_score(TopkSmem &s, int kk, int32_t *oi, float *ov
     for (int j = 0; j < kPerT; ++j) {
         const uint32_t d = digit(c[j]);
         const bool valid = j * kThreads + tid < cnt && d >= (uint32_t)cut;
-        const unsigned peers = __match_any_sync(kFull, valid ? d : 0xffffffffu);
-        const int leader = __ffs(peers) - 1;
-        uint32_t b0 = 0u;
-        if (valid && lane == leader) b0 = atomicAdd(&s.hist[d], (uint32_t)__popc(peers));
-        b0 = __shfl_sync(kFull, b0, leader);
-        if (valid) s.packed[b0 + __popc(peers & ((1u << lane) - 1u))] = c[j];
+        if (valid) s.packed[atomicAdd(&s.hist[d], 1u)] = c[j];  // the order within a bucket is free, as above
     }
     __syncthreads();
     // hist[d] is now the end of bucket d and hist[d + 1] its start; the cut bucket ends the scatter
@@ -994,9 +986,9 @@ __device__ uint64_t sampled_bound(TopkSmem &s, const float *x, int n, int r) {
     __syncthreads();
     for (int w = 0; w < kThreads / 32; ++w) kmax = max(kmax, s.warp_tot[w]);
     const uint32_t wlo = kmax >= (1u << kWinBits) ? kmax - ((1u << kWinBits) - 1u) : 0u;
-    for (int i0 = tid & ~31; i0 < kSample; i0 += kThreads) {  // warp-uniform trip count
+    for (int i0 = tid & ~31; i0 < kSample; i0 += kThreads) {
         const uint32_t key = s.sample[i0 + lane];
-        hist_add_warp(s.hist, (key - wlo) >> kBinBits, key >= wlo);
+        hist_add(s.hist, (key - wlo) >> kBinBits, key >= wlo);
     }
     __syncthreads();  // also: every thread has read warp_tot (find_bin rewrites it)
     find_bin(s, (uint32_t)r, true);
