@@ -41,9 +41,9 @@ def parse_args():
                          "GAE; topk: deterministic top-k")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--e2e-chunks", type=int, default=8,
-                    help="loss cases 0-3: logits row blocks of the host-input call timed as e2e (each computed as "
-                         "soon as it lands); 0 = copy every input first, then the device call")
+    ap.add_argument("--e2e-chunks", type=int, default=0,
+                    help="loss cases 0-3: 0 = copy every input first, then the device call (the e2e default); N > 0 "
+                         "= the host-input call with N logits row blocks, each computed as soon as it lands")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prompts", type=int, default=0,
@@ -380,8 +380,9 @@ def main():
     traffic = kernel_traffic("row_loss", args.case)
 
     # end to end through the public API: pinned host inputs -> device, call, loss -> host. With
-    # --e2e-chunks N > 0 the host-input entry point copies the logits in N row blocks and computes
-    # each block as soon as it lands; with 0, every input is copied first and the device call follows.
+    # --e2e-chunks 0 (the default) every input is copied first and the device call follows; with
+    # N > 0 the host-input entry point copies the logits in N row blocks and computes each block as
+    # soon as it lands.
     dev_in = capi.batch_inputs(batch)
     host = {k: t.cpu().pin_memory() for k, t in dev_in.items()}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
