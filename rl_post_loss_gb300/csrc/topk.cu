@@ -827,14 +827,14 @@ __device__ __forceinline__ int filter_append(TopkSmem &s, const float (&vals)[kP
     }
     if (slice >= 0)  // slice j: threads [128 (j % 4), +128), first (j < 4) or second float4
         keepm &= ((int)threadIdx.x >> 7) == (slice & 3) ? (0x0fu << (4 * (slice >> 2))) : 0u;
-    if (!__any_sync(kFull, keepm != 0u)) {
+    const unsigned m = __ballot_sync(kFull, keepm != 0u);  // the lanes that keep something
+    if (m == 0u) {
         if (lane == 0) s.warp_base[threadIdx.x >> 5] = INT_MAX;
         return 0;
     }
     const int c = __popc(keepm);
     if (!__any_sync(kFull, c > 1)) {
-        // the common case: every lane keeps at most one score, so one ballot gives the positions
-        const unsigned m = __ballot_sync(kFull, c != 0);
+        // the common case: every lane keeps at most one score, so the ballot gives the positions
         const int total = __popc(m);
         int base = 0;
         if (lane == 0) base = atomicAdd(&s.count, total);
