@@ -81,6 +81,10 @@ def test_null_arguments_are_rejected_without_a_device(lib):
     # these return before touching CUDA
     assert lib.rl_loss_create(None, None) == capi.CODES["RL_ERR_INVALID_ARG"]
     assert lib.rl_loss_forward_backward(None, None, None, None) == capi.CODES["RL_ERR_INVALID_ARG"]
+    inp, out = capi.rl_loss_inputs(), capi.rl_loss_outputs()
+    for args in ((None, None, None, None, 8, None),
+                 (None, ctypes.byref(inp), ctypes.byref(inp), ctypes.byref(out), 8, None)):
+        assert lib.rl_loss_forward_backward_from_host(*args) == capi.CODES["RL_ERR_INVALID_ARG"]
     assert lib.rl_loss_destroy(None) == 0
     bad = capi.rl_loss_config(0, 1, 1, 1, 0.2, 0.28, 2.0, 1e-6, 0, 0, 0, 1)
     h = ctypes.c_void_p()
