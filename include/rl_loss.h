@@ -72,7 +72,7 @@ typedef enum rl_status {
     RL_ERR_NONFINITE = 8,     /* device bit: a logits row holds NaN or +inf, or the loss is not finite */
     RL_ERR_EMPTY_SEQ = 9,     /* device bit (warning): a response has no mask=1 token; it adds 0 */
     RL_ERR_TIMEOUT = 10,      /* device bit: a bounded wait ran out */
-    RL_ERR_UNSUPPORTED = 11,  /* valid request this build does not implement */
+    RL_ERR_UNSUPPORTED = 11,  /* valid request the library does not implement */
     RL_ERR_SEQLENS = 12,      /* device bit: cu_seqlens not monotone or not ending at num_tokens */
     RL_ERR_DEVICE = 13,       /* called with another CUDA device current than the handle's */
     RL_ERR_INTERNAL = 14      /* device bit: an internal consistency check failed; that result is invalid */
@@ -333,7 +333,7 @@ typedef struct rl_topk_config {
     int32_t order;  /* rl_topk_order */
 } rl_topk_config;
 
-/* Largest k this build supports (4096). */
+/* Largest k the library supports (4096). */
 RL_LOSS_API int32_t rl_topk_max_k(void);
 
 /* Device pointers: scores [rows x ld] fp32, row-major, 16-byte aligned with
