@@ -597,6 +597,26 @@ def test_gae_special_cases():
             assert abs(a0[t] - (float(r[t]) + 0.9 * v_next - float(v[t]))) < 1e-12
 
 
+def test_gae_general_case_is_the_discounted_sum_of_td_errors():
+    # the definition written out: over the action tokens t_0 < t_1 < ... of a response,
+    # delta_j = r_{t_j} + gamma V_{t_{j+1}} - V_{t_j} (V after the last action token = 0) and
+    # A_{t_j} = sum_{l >= 0} (gamma lambda)^l delta_{j+l}; observation tokens get 0
+    rng = np.random.default_rng(33)
+    cu, r, v, m = _gae_case(rng, [11, 1, 17, 6])
+    gamma, lam = 0.93, 0.71
+    a = oracle.gae(cu, r, v, m, gamma, lam)
+    for i in range(len(cu) - 1):
+        acts = [t for t in range(cu[i], cu[i + 1]) if m[t]]
+        vals = [float(v[t]) for t in acts] + [0.0]
+        delta = [float(r[t]) + gamma * vals[j + 1] - vals[j] for j, t in enumerate(acts)]
+        for j, t in enumerate(acts):
+            want = sum((gamma * lam) ** l * delta[j + l] for l in range(len(acts) - j))
+            assert abs(a[t] - want) < 1e-12
+        for t in range(cu[i], cu[i + 1]):
+            if not m[t]:
+                assert a[t] == 0.0
+
+
 def test_gae_skip_observations_equals_gae_on_the_action_tokens_alone():
     rng = np.random.default_rng(31)
     cu, r, v, m = _gae_case(rng, [15, 9, 20])
