@@ -36,14 +36,15 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--case", default="1", choices=["0", "1", "2", "3", "4", "gae", "topk"],
+    ap.add_argument("--case", default="3", choices=["0", "1", "2", "3", "4", "gae", "topk"],
                     help="0-3: the fused loss over logits; 4: the fused projection + loss; gae: skip-observation "
                          "GAE; topk: deterministic top-k")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--e2e-chunks", type=int, default=0,
-                    help="loss cases 0-3: 0 = copy every input first, then the device call (the e2e default); N > 0 "
-                         "= the host-input call with N logits row blocks, each computed as soon as it lands")
+    ap.add_argument("--e2e-chunks", type=int, default=16,
+                    help="loss cases 0-3: N > 0 = the host-input call rl_loss_forward_backward_from_host with N "
+                         "logits row blocks, each computed as soon as it lands (the e2e default, 16); 0 = copy "
+                         "every input first, then the device call")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prompts", type=int, default=0,
@@ -79,6 +80,7 @@ def measured_peaks(key: str = "hbm_gbs"):
 KERNEL_SOURCES = {
     "row_loss": ["row_loss.cu", "common.cuh"],
     "proj_gemm": ["proj_gemm.cu", "proj.cuh", "ptx.cuh", "common.cuh"],
+    "proj_bwd": ["proj_gemm.cu", "proj.cuh", "ptx.cuh", "common.cuh"],
     "gae": ["gae.cu", "scan_select.cuh", "common.cuh"],
     "topk": ["topk.cu", "scan_select.cuh", "ptx.cuh", "common.cuh"],
 }
@@ -380,14 +382,25 @@ def main():
     traffic = kernel_traffic("row_loss", args.case)
 
     # end to end through the public API: pinned host inputs -> device, call, loss -> host. With
-    # --e2e-chunks 0 (the default) every input is copied first and the device call follows; with
-    # N > 0 the host-input entry point copies the logits in N row blocks and computes each block as
-    # soon as it lands.
+    # --e2e-chunks N > 0 (the default) the host-input entry point copies the logits in N row blocks
+    # and computes each block as soon as it lands; with 0 every input is copied first and the device
+    # call follows.
     dev_in = capi.batch_inputs(batch)
-    host = {k: t.cpu().pin_memory() for k, t in dev_in.items()}
+    host = {}
+    for k, t in dev_in.items():
+        host[k] = torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, pin_memory=True)
+        host[k].copy_(t)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     loss_host = torch.empty(1, dtype=torch.float64).pin_memory()
     e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the host link as this run sees it: the same copies alone, just before the timed steps
+    torch.cuda.synchronize()
+    e_start.record(stream)
+    for name, t in host.items():
+        dev_in[name].copy_(t, non_blocking=True)
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    copy_ms = e_start.elapsed_time(e_stop)
     for k in range(args.e2e_steps + 1):
         if k == 1:
             torch.cuda.synchronize()
@@ -427,6 +440,10 @@ def main():
                 "clocks": clocks.summary(),
                 "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": 8, "ms_per_step": e2e_ms,
+                        "h2d_gbs_in_step": h2d / (e2e_ms / 1e3) / 1e9,
+                        "copy_alone_ms": copy_ms, "h2d_gbs_copy_alone": h2d / (copy_ms / 1e3) / 1e9,
+                        "outputs": "the loss (8 B) comes back to the host; dlogits stays on the device for "
+                                   "the caller's backward",
                         "call": ("rl_loss_forward_backward_from_host, %d logits blocks" % args.e2e_chunks
                                  if args.e2e_chunks > 0 else "copies, then rl_loss_forward_backward")},
                 "gpu_launches": launches, "device_status": capi.status_bits_to_names(bits),
@@ -528,6 +545,9 @@ def main_projection(args):
     gemm_flops = 2.0 * T * V * H / max(1, g_n // args.steps)  # per launch (one chunk)
     peak, peak_kind = measured_peaks("bf16_tflops_sustained")
     achieved = gemm_flops / (g_ms / max(1, g_n) / 1e3) / 1e12
+    b_n, b_ms = prof["proj_bwd"]
+    bwd_flops = 4.0 * T * V * H / max(1, b_n // args.steps)  # dL/dh and dL/dW of one chunk per launch
+    bwd_achieved = bwd_flops / (b_ms / max(1, b_n) / 1e3) / 1e12
     step_tflops = flops_alg / (ms / args.steps / 1e3) / 1e12
 
     host = {"hidden": pb.hidden.cpu().pin_memory(), "w": pb.w.cpu().pin_memory()}
@@ -566,10 +586,14 @@ def main_projection(args):
                            "mask1_tokens": int(b.mask.sum().item()), "parallelism": "replicas",
                            "l2": "no flush: each step streams W (1.9 GB) once per chunk and writes 3.7 GB of fp32 "
                                  "logits per chunk, far larger than the 129 MB L2"},
-                "roofline": {"bound": "tensor", "kernel": "proj_gemm", "achieved": achieved, "peak": peak,
+                "roofline": {"bound": "tensor", "kernel": "proj_bwd", "achieved": bwd_achieved, "peak": peak,
                              "peak_kind": f"{peak_kind} sustained cuBLAS bf16 TFLOP/s", "unit": "TFLOP/s",
-                             "frac": achieved / peak, "traffic": kernel_traffic("proj_gemm", 4),
-                             "algorithmic_flops_per_launch": gemm_flops, "avg_launch_ms": g_ms / max(1, g_n)},
+                             "frac": bwd_achieved / peak, "traffic": kernel_traffic("proj_bwd", 4),
+                             "algorithmic_flops_per_launch": bwd_flops, "avg_launch_ms": b_ms / max(1, b_n)},
+                "roofline_forward": {"bound": "tensor", "kernel": "proj_gemm", "achieved": achieved, "peak": peak,
+                                     "unit": "TFLOP/s", "frac": achieved / peak,
+                                     "traffic": kernel_traffic("proj_gemm", 4),
+                                     "algorithmic_flops_per_launch": gemm_flops, "avg_launch_ms": g_ms / max(1, g_n)},
                 "step_tensor": {"algorithmic_tflops": step_tflops, "frac": step_tflops / peak,
                                 "executed_flops_per_step": flops_alg, "note": "6 N V H per step"},
                 "kernel_ms": {k: v[1] / args.steps for k, v in prof.items() if v[0]},

@@ -226,16 +226,18 @@ RL_LOSS_API rl_status rl_loss_forward_backward_from_host(rl_loss_t handle, const
  * infrastructure item 5): the hidden states are split into chunks of rows; per
  * chunk the output projection z = h W^T, the loss above and their backward run
  * to completion before the next chunk reuses the buffers, so the logits of the
- * whole sequence never exist at once. The projection runs on the tensor cores
- * (tcgen05, bf16 inputs, fp32 accumulation) fused with the per-row softmax
- * statistics; dZ is formed once per chunk in bf16; dH = dZ W and dW += dZ^T H
- * are plain GEMMs computed with cuBLAS. */
+ * whole sequence never exist at once. All three products run on the tensor
+ * cores (tcgen05, pairs of CTAs on 256 x 256 tiles, bf16 inputs, fp32
+ * accumulation in a fixed order): the projection fused with the per-row
+ * softmax statistics; dZ is formed once per chunk in bf16; dH = dZ W and
+ * dW += dZ^T H share one launch per chunk, dW accumulated in fp32 chunk after
+ * chunk in chunk order, so every output repeats bit for bit. */
 
 /* Allocates the fused projection path's buffers for hidden size `hidden_dim`
  * (a multiple of 8) and chunks of `chunk_tokens` rows: a chunk_tokens x V fp32
- * logits buffer, a chunk_tokens x V bf16 dL/dlogits buffer, the per-row
- * statistics, and a cuBLAS handle with its own 64 MiB workspace. Requires a
- * handle with logits_dtype RL_BF16 (else RL_ERR_UNSUPPORTED). Calling it again
+ * logits buffer, a chunk_tokens x V bf16 dL/dlogits buffer and the per-row
+ * statistics. Requires a handle with logits_dtype RL_BF16 (else
+ * RL_ERR_UNSUPPORTED). Calling it again
  * replaces the buffers. Synchronises the device. */
 RL_LOSS_API rl_status rl_loss_projection_setup(rl_loss_t handle, int32_t hidden_dim, int32_t chunk_tokens);
 
@@ -377,10 +379,10 @@ RL_LOSS_API const char *rl_loss_last_cuda_error(rl_loss_t handle);
 RL_LOSS_API rl_status rl_loss_launch_count(rl_loss_t handle, int64_t *count);
 
 /* Allocation-free variant of rl_loss_forward_backward, for callers that cannot
- * call cudaMalloc when they need the loss: code running while a CUDA graph is
- * captured, inside a framework whose caching allocator owns all device memory,
- * or in a serving process with a fixed memory budget. (The pages describe no
- * such entry point; it has no counterpart there.)
+ * call cudaMalloc when they need the loss: code inside a framework whose
+ * caching allocator owns all device memory, or a serving process with a fixed
+ * memory budget, where an allocation could fail or synchronise the device.
+ * (The pages describe no such entry point; it has no counterpart there.)
  *
  * It needs no handle and allocates nothing: its workspace is one static
  * 16 MiB device array of this library, which every GPU that loads the library

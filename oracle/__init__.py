@@ -244,6 +244,49 @@ def projection_rows(row_ids, hidden_bits, w_bits, targets, logp_old, logp_infer,
     return out
 
 
+def projection_forward_stats(hidden_bits, w_bits, batch: dict, p: LossParams, row_block: int = 1024) -> dict:
+    """The forward of the fused path over every row, streamed in blocks of
+    ``row_block`` rows so that no [T, V] array is held: per token the log-prob,
+    entropy, flags, objective term and dL/dlogp (``g``), and the exact loss of
+    Eq. (1) ("GLM-5: from Vibe Coding to Agentic Engineering", section 3.2) on
+    the projected logits z = h W^T (section 2.4.1). No dL/dz is formed."""
+    cu = batch["cu_seqlens"]
+    T = int(cu[-1])
+    n, adv, w = seq_prep(cu, batch["mask"], batch["rewards_or_adv"], p)
+    W = bf16_bits_to_f64(w_bits)
+    keys = ("logp", "entropy", "flags", "tok_obj", "g")
+    parts = {k: [] for k in keys}
+    for r0 in range(0, T, row_block):
+        ids = np.arange(r0, min(T, r0 + row_block), dtype=np.int64)
+        z = np.ascontiguousarray(bf16_bits_to_f64(hidden_bits[r0:r0 + len(ids)]) @ W.T)
+        o = rows(ids, z, F64, W.shape[0], batch["targets"], batch["logp_old"], batch["logp_infer"], batch["mask"],
+                 cu, adv, w, p)
+        for k in keys:
+            parts[k].append(o[k])
+    out = {k: (np.concatenate(v) if v else np.zeros(0)) for k, v in parts.items()}
+    out["loss"] = loss(cu, w, out["tok_obj"]) if T else loss(cu, w, np.zeros(0))
+    out["n_tokens"], out["adv"], out["w"] = n, adv, w
+    return out
+
+
+def projection_dw_rows(vocab_ids, h: np.ndarray, W: np.ndarray, targets, logp, g) -> np.ndarray:
+    """Rows ``vocab_ids`` of dL/dW = (dL/dz)^T h for the fused path, from the
+    per-token log-probs and dL/dlogp of the forward (``logp``, ``g``) on float64
+    h [T, H] and W [V, H]: dL/dz_{t,v} = g_t (1[v = y_t] - exp(z_{t,v} - logZ_t))
+    with logZ_t = z_{t,y_t} - logp_t (the chain rule through Eq. (1)'s log-prob,
+    section 3.2). Rows with g_t = 0 contribute nothing."""
+    ids = np.asarray(vocab_ids, np.int64)
+    g = np.asarray(g, np.float64)
+    live = np.nonzero(g != 0.0)[0]
+    hl = h[live]
+    y = np.asarray(targets, np.int64)[live]
+    zy = np.einsum("th,th->t", hl, W[y])
+    logz = zy - np.asarray(logp, np.float64)[live]
+    zv = hl @ W[ids].T
+    dz = g[live][:, None] * ((y[:, None] == ids[None, :]).astype(np.float64) - np.exp(zv - logz[:, None]))
+    return dz.T @ hl
+
+
 def projection_forward_backward_f64(h: np.ndarray, W: np.ndarray, batch: dict, p: LossParams) -> dict:
     """Whole-batch oracle of the fused path on float64 hidden states h [T, H]
     and LM head W [V, H]: z = h W^T, the loss of Eq. (1) on z, dL/dz, and by the

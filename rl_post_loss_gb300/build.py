@@ -73,9 +73,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
         raise RuntimeError("nvcc failed:\n" + "\n".join(f"--- {s}\n{o}" for s, o in failed))
     if force or procs or _stale(LIB_PATH, objs):
         tmp = LIB_PATH + ".tmp%d" % os.getpid()
-        cudalib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc_path()))), "lib64")
-        cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + [
-            "-lcublas", "-Xlinker", "-rpath=" + cudalib]
+        cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
         subprocess.check_call(cmd)
         os.replace(tmp, LIB_PATH)
     return LIB_PATH

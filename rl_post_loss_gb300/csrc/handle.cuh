@@ -16,11 +16,11 @@ enum RlKernelClass {
     kFinalReduce,
     kProjGemm,
     kProjRows,
-    kLibGemm,  // the two cuBLAS GEMMs of the projection backward
+    kProjBwd,  // both products of the projection backward (one tcgen05 launch per chunk)
     kNumKernels
 };
 static const char *const kKernelNames[kNumKernels] = {"seg_prep",     "token_prep", "row_loss",  "seg_reduce",
-                                                      "final_reduce", "proj_gemm",  "proj_rows", "cublas_gemm"};
+                                                      "final_reduce", "proj_gemm",  "proj_rows", "proj_bwd"};
 constexpr size_t kProfSlotsPerCall = 160;  // enough for a projection call of 32 chunks (or a host call of 64 blocks)
 constexpr int kMaxCopyChunks = 64;         // logits blocks of rl_loss_forward_backward_from_host
 
@@ -58,9 +58,6 @@ struct rl_loss_handle_s {
     float *proj_z = nullptr;
     void *proj_dz = nullptr;
     float4 *proj_stats = nullptr;
-    void *cublas = nullptr;     // cublasHandle_t
-    void *cublas_ws = nullptr;  // its workspace
-    size_t cublas_ws_bytes = 0;
 
     bool prof_reset(size_t slots) {
         for (cudaEvent_t e : prof_events) cudaEventDestroy(e);

@@ -25,6 +25,35 @@ int proj_gemm_tile_cols();
 cudaError_t launch_proj_gemm(const void *A, int64_t lda, const void *B, int64_t ldb, const ProjGemmParams &p,
                              cudaStream_t stream);
 
+// One bf16 operand of a GEMM problem, row-major with row stride `ld`
+// elements (16-byte aligned base, ld * 2 a multiple of 16). K-major: the
+// operand's M (or N) index is the row and K the column; MN-major: K is the row
+// and M (or N) the column.
+struct GemmOperand {
+    const void *base;
+    int64_t ld;
+    int mn_major;
+};
+
+// D [M x N] = A [M x K] B [K x N] (fp32 accumulation over K in a fixed order).
+struct GemmProblem {
+    enum Epi { kZStats = 0, kBf16 = 1, kF32 = 2 };
+    int M, N, K;
+    GemmOperand a, b;
+    int epi;         // kZStats: fp32 D (optional) + per-row, per-256-column softmax statistics;
+                     // kBf16: D rounded to bf16; kF32: D in fp32
+    int accumulate;  // kF32: D += A B instead of D = A B
+    int n_fastest;   // tile order of the problem (consecutive tiles of a CTA pair walk N, else M)
+    void *d;
+    int64_t ldd;     // elements
+    float4 *stats;   // kZStats: [M x ceil(N / 256)]
+};
+
+// One launch over one or two problems. With two, the tiles of the first are
+// strided over the CTA pairs and those of the second are split into
+// contiguous ranges that balance the pairs' k-blocks.
+cudaError_t launch_gemm_problems(const GemmProblem *probs, int nprob, uint32_t *status, cudaStream_t stream);
+
 struct ProjRowParams {
     const float *z;      // [rows x ldz] fp32 logits of the chunk
     int64_t ldz;

@@ -9,22 +9,17 @@
 //   proj_gemm   Z_c = H_c W^T (tcgen05, fp32) + per-row, per-256-column softmax statistics
 //   token_prep  per-token records (z_y read from Z_c)
 //   proj_rows   statistics merged per row in tile order, token objective, dZ_c (bf16)
-//   cuBLAS      dH_c = dZ_c W (bf16 out)        -- plain GEMMs: library routines
-//               dW  (+)= dZ_c^T H_c (fp32; overwritten by chunk 0, accumulated after)
+//   proj_bwd    one tcgen05 launch over both backward products:
+//               dH_c = dZ_c W (bf16 out) and
+//               dW  (+)= dZ_c^T H_c (fp32; stored by chunk 0, added into by the later chunks)
 // then the fixed-order per-response and batch reductions give the loss.
-#include <cublas_v2.h>
-
 #include <cmath>
 
 #include "handle.cuh"
 #include "proj.cuh"
 
 void rl_loss_handle_s::proj_release() {
-    if (cublas) cublasDestroy(reinterpret_cast<cublasHandle_t>(cublas));
-    if (cublas_ws) cudaFree(cublas_ws);
     if (proj_ws) cudaFree(proj_ws);
-    cublas = nullptr;
-    cublas_ws = nullptr;
     proj_ws = nullptr;
     proj_z = nullptr;
     proj_dz = nullptr;
@@ -70,21 +65,6 @@ RL_LOSS_API rl_status rl_loss_projection_setup(rl_loss_t h, int32_t hidden_dim, 
     h->proj_z = reinterpret_cast<float *>(ws);
     h->proj_dz = reinterpret_cast<char *>(ws) + z_bytes;
     h->proj_stats = reinterpret_cast<float4 *>(reinterpret_cast<char *>(ws) + z_bytes + dz_bytes);
-    cublasHandle_t cb = nullptr;
-    if (cublasCreate(&cb) != CUBLAS_STATUS_SUCCESS) {
-        h->proj_release();
-        return RL_ERR_CUDA;
-    }
-    h->cublas = cb;
-    // a workspace of its own, so that later calls allocate nothing
-    h->cublas_ws_bytes = size_t(64) << 20;
-    e = cudaMalloc(&h->cublas_ws, h->cublas_ws_bytes);
-    if (e != cudaSuccess || cublasSetWorkspace(cb, h->cublas_ws, h->cublas_ws_bytes) != CUBLAS_STATUS_SUCCESS ||
-        cublasSetMathMode(cb, CUBLAS_DEFAULT_MATH) != CUBLAS_STATUS_SUCCESS) {
-        cudaGetLastError();
-        h->proj_release();
-        return RL_ERR_CUDA;
-    }
     h->proj_hidden = hidden_dim;
     h->proj_chunk = chunk_tokens;
     h->proj_n_tiles = n_tiles;
@@ -143,8 +123,6 @@ RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(
             return RL_ERR_ALIGNMENT;
     }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
-    cublasHandle_t cb = reinterpret_cast<cublasHandle_t>(h->cublas);
-    if (cublasSetStream(cb, stream) != CUBLAS_STATUS_SUCCESS) return RL_ERR_CUDA;
 
     rlk::SeqPrepParams sp{};
     sp.cu_seqlens = in->cu_seqlens;
@@ -172,7 +150,6 @@ RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(
 
     float *entropy = out->entropy ? out->entropy : h->tok_ent;
     uint8_t *flags = out->flags ? out->flags : h->tok_flags;
-    const float one = 1.f, zero = 0.f;
     for (int r0 = 0, ci = 0; r0 < T; r0 += h->proj_chunk, ++ci) {
         const int m = T - r0 < h->proj_chunk ? T - r0 : h->proj_chunk;
         const char *hc = reinterpret_cast<const char *>(hidden) + (size_t)r0 * ld_hidden * 2;
@@ -241,20 +218,33 @@ RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(
         if (e != cudaSuccess) return cuda_fail(h, e);
         launches += 3;
 
-        // dH_c [m x H] = dZ_c [m x V] W [V x H]; column-major view: dH^T = W^T dZ^T
-        char *dhc = reinterpret_cast<char *>(dhidden) + (size_t)r0 * ld_dhidden * 2;
-        slot = h->prof_begin(kLibGemm, stream);
-        cublasStatus_t cs =
-            cublasGemmEx(cb, CUBLAS_OP_N, CUBLAS_OP_N, H, m, V, &one, w_lm, CUDA_R_16BF, (int)ld_w, h->proj_dz,
-                         CUDA_R_16BF, (int)h->proj_lddz, &zero, dhc, CUDA_R_16BF, (int)ld_dhidden, CUBLAS_COMPUTE_32F,
-                         CUBLAS_GEMM_DEFAULT);
-        // dW [V x H] (+)= dZ_c^T [V x m] H_c [m x H]; column-major view: dW^T = H_c^T dZ_c
-        if (cs == CUBLAS_STATUS_SUCCESS)
-            cs = cublasGemmEx(cb, CUBLAS_OP_N, CUBLAS_OP_T, H, V, m, &one, hc, CUDA_R_16BF, (int)ld_hidden,
-                              h->proj_dz, CUDA_R_16BF, (int)h->proj_lddz, ci == 0 ? &zero : &one, dw_lm, CUDA_R_32F,
-                              (int)ld_dw, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+        // dH_c [m x H] = dZ_c [m x V] W [V x H]: dZ_c is K-major, W MN-major (H contiguous)
+        // dW [V x H] (+)= dZ_c^T [V x m] H_c [m x H]: dZ_c and H_c both MN-major
+        rlk::GemmProblem bw[2] = {};
+        bw[0].M = m;
+        bw[0].N = H;
+        bw[0].K = V;
+        bw[0].a = rlk::GemmOperand{h->proj_dz, h->proj_lddz, 0};
+        bw[0].b = rlk::GemmOperand{w_lm, ld_w, 1};
+        bw[0].epi = rlk::GemmProblem::kBf16;
+        bw[0].n_fastest = 0;  // pairs running at once share W's column blocks through L2
+        bw[0].d = reinterpret_cast<char *>(dhidden) + (size_t)r0 * ld_dhidden * 2;
+        bw[0].ldd = ld_dhidden;
+        bw[1].M = V;
+        bw[1].N = H;
+        bw[1].K = m;
+        bw[1].a = rlk::GemmOperand{h->proj_dz, h->proj_lddz, 1};
+        bw[1].b = rlk::GemmOperand{hc, ld_hidden, 1};
+        bw[1].epi = rlk::GemmProblem::kF32;
+        bw[1].accumulate = ci > 0;
+        bw[1].n_fastest = 1;  // a pair's consecutive tiles reuse one block of dZ_c from L2
+        bw[1].d = dw_lm;
+        bw[1].ldd = ld_dw;
+        slot = h->prof_begin(kProjBwd, stream);
+        e = rlk::launch_gemm_problems(bw, 2, h->status, stream);
         h->prof_end(slot, stream);
-        if (cs != CUBLAS_STATUS_SUCCESS) return RL_ERR_CUDA;
+        if (e != cudaSuccess) return cuda_fail(h, e);
+        launches += 1;
     }
 
     if (T == 0 && dw_lm) {  // no chunk ran: the weight gradient is zero

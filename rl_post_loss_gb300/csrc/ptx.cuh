@@ -138,6 +138,104 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ---------------------------------------------------------------- clusters and CTA pairs
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// The shared::cluster address of the same shared-memory offset in CTA `rank`
+// of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Every thread of every CTA of the cluster arrives, then waits for all of
+// them (release / acquire: shared-memory writes before it are visible after).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Arrive on an mbarrier of (possibly) another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+// 2-D tiled bulk tensor load into this CTA's shared memory whose completion is
+// counted on an mbarrier of either CTA of the pair (`bar_cluster`, a
+// shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap, int x, int y, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+
+// The same load written into this CTA and the others in `cta_mask` (same
+// shared-memory offset); in each destination the completion is counted on the
+// mbarrier at `bar_cluster`'s offset in the even CTA of that destination's pair.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void *tmap, int x, int y, uint32_t bar_cluster,
+                                                    uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::"
+        "cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster), "h"(cta_mask)
+        : "memory");
+}
+
+// TMEM allocation, MMA and commit of a CTA pair (cta_group::2): the
+// allocation is made collectively by one warp of each CTA of the pair; the MMA
+// and its commits are issued by one thread of the even CTA, which reads A and
+// B from both CTAs' shared memory (same offsets) and writes D into both CTAs'
+// TMEM (rows 0..127 in the even CTA, 128..255 in the odd one).
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the mbarrier at shared-memory offset `bar` of every CTA in
+// `cta_mask` when all tcgen05 operations issued so far by this thread complete.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a bf16 tile in the 128-byte-swizzled
+// layout written by a TMA copy with SWIZZLE_128B, with explicit leading- and
+// stride-dimension byte offsets. K-major tiles (rows of 64 K-elements, 8-row
+// atoms stacked along M/N): lbo unused (16), sbo = 1024. MN-major tiles (rows
+// of 64 M/N-elements, one row per k, 8-k atoms of 1024 bytes): lbo = the byte
+// distance between 64-element blocks along M/N, sbo = 1024 between 8-k atoms.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
 // Shared-memory matrix descriptor of a K-major bf16 tile stored in the
 // 128-byte-swizzled layout a TMA copy with SWIZZLE_128B produces: rows of 128
 // bytes (64 elements), 8-row (1024-byte) swizzle atoms stacked along M/N.
@@ -161,6 +259,11 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
 // M >> 4 [24,29).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// The same with the operand majorness bits: A MN-major [15], B MN-major [16].
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_major(int M, int N, int a_mn, int b_mn) {
+    return idesc_bf16_f32(M, N) | ((uint32_t)(a_mn ? 1 : 0) << 15) | ((uint32_t)(b_mn ? 1 : 0) << 16);
 }
 
 }  // namespace ptx

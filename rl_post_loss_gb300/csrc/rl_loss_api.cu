@@ -428,8 +428,10 @@ RL_LOSS_API rl_status rl_loss_forward_backward_from_host(rl_loss_t h, const rl_l
         const int r0 = rows[b], n = rows[b + 1] - r0;
         char *dst = const_cast<char *>(static_cast<const char *>(d.logits)) + (size_t)r0 * d.ld_logits * es;
         const char *src = static_cast<const char *>(host->logits) + (size_t)r0 * host->ld_logits * es;
-        if (host->ld_logits == d.ld_logits)
-            err = cudaMemcpyAsync(dst, src, (size_t)n * d.ld_logits * es, cudaMemcpyHostToDevice, h->copy_stream);
+        // one flat copy only when rows are packed on both sides: with ld > V it would touch the
+        // padding columns and read past the end of a host buffer of (T - 1) * ld + V elements
+        if (host->ld_logits == V && d.ld_logits == V)
+            err = cudaMemcpyAsync(dst, src, (size_t)n * V * es, cudaMemcpyHostToDevice, h->copy_stream);
         else
             err = cudaMemcpy2DAsync(dst, (size_t)d.ld_logits * es, src, (size_t)host->ld_logits * es, (size_t)V * es,
                                     (size_t)n, cudaMemcpyHostToDevice, h->copy_stream);
@@ -493,10 +495,9 @@ RL_LOSS_API rl_status rl_loss_launch_count(rl_loss_t h, int64_t *count) {
 // ---------------------------------------------------------------- allocation-free entry point
 //
 // Some callers cannot call cudaMalloc at the moment they need the loss: code
-// that runs while a CUDA graph is being captured, inside a framework whose
-// caching allocator owns all device memory, or in a serving process with a
-// fixed memory budget where an allocation could fail or synchronise the
-// device. rl_loss_forward_backward_noalloc serves them without a handle: its
+// inside a framework whose caching allocator owns all device memory, or a
+// serving process with a fixed memory budget where an allocation could fail or
+// synchronise the device. rl_loss_forward_backward_noalloc serves them without a handle: its
 // workspace is one statically sized device array of this library, which every
 // GPU that loads the library holds until the process exits.
 namespace {

@@ -108,6 +108,34 @@ def test_device_row_stride_differs_from_the_host_one():
     assert bool((dev["logits"][:, b.vocab:] == 7.0).all())  # columns past V are not written
 
 
+def test_equal_padded_strides_touch_neither_padding_nor_past_the_last_row():
+    """Host and device rows both padded (ld > V, same stride): the padding
+    columns of the device buffer keep their sentinels, and a host buffer that
+    ends right after the last row's V-th element is enough."""
+    b = synthetic.make_batch(1, "cuda", lengths=_lengths(8, 10, 80, 8), vocab=1001)
+    T, V, ld = b.num_tokens, b.vocab, 1024 + 8
+    rl = capi.handle_for_batch(b)
+    ref = capi.alloc_outputs(b)
+    capi.run_batch(rl, b, ref)
+    torch.cuda.synchronize()
+    ref_bits = rl.device_status()
+    src = capi.batch_inputs(b)
+    host = _host_copy(src)
+    flat = torch.empty((T - 1) * ld + V, dtype=src["logits"].dtype).pin_memory()
+    hl = flat.as_strided((T, V), (ld, 1))
+    hl.copy_(src["logits"][:, :V].cpu())
+    host["logits"] = hl
+    dev = _device_like(src, ld)
+    out = capi.alloc_outputs(b)
+    capi.run_batch_from_host(rl, host, dev, out, num_chunks=4)
+    torch.cuda.synchronize()
+    assert rl.device_status() == ref_bits
+    _equal_outputs(b, out, ref)
+    assert dev["logits"].stride(0) == ld
+    assert _same(dev["logits"][:, :V], src["logits"][:, :V])
+    assert bool((dev["logits"][:, V:] == 7.0).all())  # padding columns are not written
+
+
 @pytest.mark.parametrize("over", [
     dict(token_adv="normal"),
     dict(token_adv="teacher", group=1, prompts=16),

@@ -419,6 +419,93 @@ def test_projection_gradients_match_finite_differences():
         np.testing.assert_allclose(grad, fd, rtol=1e-5, atol=1e-8 * np.abs(grad).max(), err_msg=name)
 
 
+def _bf16_bits(x):
+    """Round-to-nearest-even bf16 bit patterns of float values."""
+    u = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _projection_case(seed, T=40, H=24, V=37):
+    rng = np.random.default_rng(seed)
+    hb = _bf16_bits(rng.normal(0, 1, (T, H)))
+    wb = _bf16_bits(rng.normal(0, 0.4, (V, H)))
+    cu = np.array([0, 9, 17, 30, 40], np.int32)
+    tg = rng.integers(0, V, T).astype(np.int32)
+    b = _batch(np.zeros((T, V)), tg, np.zeros(T), np.zeros(T), (rng.random(T) > 0.2).astype(np.uint8), cu,
+               [1.0, 0.0, 0.0, 1.0])
+    p = LossParams(group_size=2)
+    lp = oracle.projection_forward_backward(hb, wb, b, p)["logp"]
+    b["logp_old"] = (lp - rng.normal(0, 0.15, T)).astype(np.float32)
+    b["logp_infer"] = (b["logp_old"].astype(np.float64) - rng.normal(0, 0.3, T)).astype(np.float32)
+    return hb, wb, b, p
+
+
+def test_projection_rows_equal_the_whole_batch_oracle():
+    """The row-subset oracle of the fused path (used at sizes where the whole
+    batch cannot be formed) gives, on any subset of rows, the log-prob,
+    entropy, flags, dL/dlogp and dL/dh of the whole-batch oracle, whose
+    gradients are pinned by finite differences above. H != V, so a transposed
+    W or a wrong row gather fails here."""
+    hb, wb, b, p = _projection_case(31)
+    full = oracle.projection_forward_backward(hb, wb, b, p)
+    n, adv, w = oracle.seq_prep(b["cu_seqlens"], b["mask"], b["rewards_or_adv"], p)
+    ids = np.array([3, 0, 39, 17, 22, 8, 30])
+    sub = oracle.projection_rows(ids, hb, wb, b["targets"], b["logp_old"], b["logp_infer"], b["mask"],
+                                 b["cu_seqlens"], adv, w, p, want_dh=True)
+    for k in ("logp", "entropy", "g", "tok_obj"):
+        np.testing.assert_allclose(sub[k], full[k][ids], rtol=1e-12, atol=1e-14, err_msg=k)
+    assert np.array_equal(sub["flags"], full["flags"][ids])
+    np.testing.assert_allclose(sub["dh"], full["dh"][ids], rtol=1e-12, atol=1e-14)
+    assert np.abs(full["g"][ids]).min() >= 0 and np.count_nonzero(full["g"][ids]) >= 3
+
+
+def test_projection_streamed_forward_and_dw_rows_equal_the_whole_batch_oracle():
+    """The streamed forward (exact loss over every row without a [T, V] array)
+    and the sampled dL/dW rows computed from its log-probs and dL/dlogp equal
+    the whole-batch oracle, whose dL/dW is pinned by finite differences."""
+    hb, wb, b, p = _projection_case(32)
+    full = oracle.projection_forward_backward(hb, wb, b, p)
+    st = oracle.projection_forward_stats(hb, wb, b, p, row_block=7)
+    for k in ("logp", "entropy", "g", "tok_obj"):
+        np.testing.assert_allclose(st[k], full[k], rtol=1e-12, atol=1e-14, err_msg=k)
+    assert np.array_equal(st["flags"], full["flags"])
+    assert abs(st["loss"] - full["loss"]) <= 1e-13 * abs(full["loss"])
+    ids = np.array([0, 36, 5, 11, 20])
+    h64, W64 = oracle.bf16_bits_to_f64(hb), oracle.bf16_bits_to_f64(wb)
+    dw = oracle.projection_dw_rows(ids, h64, W64, b["targets"], st["logp"], st["g"])
+    np.testing.assert_allclose(dw, full["dW"][ids], rtol=1e-10, atol=1e-14 * np.abs(full["dW"]).max())
+
+
+def test_clip_active_vec_matches_the_scalar_rule_at_threshold_neighbours():
+    """The vector clip decision (the checker of every clip bit) equals the
+    scalar rule token by token, and both follow the strict one-sided
+    inequalities at the fp32 thresholds and their fp32 neighbours."""
+    eps_low, eps_high = 0.2, 0.28
+    _, hi, lo = oracle.thresholds_f32(2.0, eps_low, eps_high)
+    hi, lo = np.float32(hi), np.float32(lo)
+    cases = []  # (logp, logp_old = 0 so that fl32(logp - logp_old) = logp exactly, adv)
+    for thr in (hi, lo):
+        for e in (thr, np.nextafter(thr, np.float32(np.inf)), np.nextafter(thr, np.float32(-np.inf))):
+            for adv in (0.7, -0.7, 0.0):
+                cases.append((np.float32(e), np.float32(0.0), adv))
+    rng = np.random.default_rng(40)
+    for _ in range(200):
+        lo_ = np.float32(rng.normal(-2, 1))
+        lp = np.float32(lo_ + np.float32(rng.normal(0, 0.4)))
+        cases.append((lp, lo_, float(rng.choice([-1.3, 0.0, 0.4]))))
+    lp = np.array([c[0] for c in cases], np.float32)
+    lo_ = np.array([c[1] for c in cases], np.float32)
+    adv = np.array([c[2] for c in cases], np.float64)
+    vec = oracle.clip_active_vec(lp, lo_, adv, eps_low, eps_high)
+    for k, (a, o, A) in enumerate(cases):
+        assert int(vec[k]) == int(oracle.clip_active(float(a), float(o), A, eps_low, eps_high)), k
+    assert vec[:18].reshape(2, 3, 3).tolist() == [
+        # ln r at fl32(ln(1 + eps_high)), one ulp above, one ulp below; A = +0.7, -0.7, 0
+        [[0, 0, 0], [1, 0, 0], [0, 0, 0]],
+        # ln r at fl32(ln(1 - eps_low)), one ulp above, one ulp below
+        [[0, 0, 0], [0, 0, 0], [0, 1, 0]]]
+
+
 # ----------------------------------------------------------------------------- DIS, OPD, per-token advantages
 
 def _tok_batch(rng, lengths, V, token_adv=None):

@@ -1,9 +1,9 @@
 """The allocation-free entry point ``rl_loss_forward_backward_noalloc``.
 
 Callers that cannot allocate device memory when they need the loss (code
-running under CUDA graph capture, inside a framework whose caching allocator
-owns the device memory, or in a process with a fixed memory budget) use this
-entry point: it takes no handle and keeps its workspace in a static device
+inside a framework whose caching allocator owns the device memory, or a
+process with a fixed memory budget, where an allocation could fail or
+synchronise the device) use this entry point: it takes no handle and keeps its workspace in a static device
 array of the library. These tests call it through the C ABI and check that two
 calls in a row give the same results as the handle-based entry point, within
 the parity tolerances used everywhere else, and that the static workspace does
