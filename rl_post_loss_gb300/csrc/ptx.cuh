@@ -90,6 +90,40 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// 2-D tiled bulk tensor store shared -> global, or element-wise reduce-add
+// into global (the L2 adds each element once: the result is old + value,
+// rounded once). Boxes that reach past the tensor's edge are clipped.
+// Completion is tracked by bulk groups (commit_group / wait_group).
+__device__ __forceinline__ void tma_store_2d(const void *tmap, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const void *tmap, int x, int y, uint32_t src) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     tmap),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N committed bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until at most N committed bulk groups of this thread are incomplete.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// Makes this thread's shared-memory writes visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05 / TMEM
 
 // Allocate `ncols` TMEM columns (power of two >= 32) for this CTA; the base
@@ -173,18 +207,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
         "%3}], [%4];" ::"r"(dst),
         "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster)
-        : "memory");
-}
-
-// The same load written into this CTA and the others in `cta_mask` (same
-// shared-memory offset); in each destination the completion is counted on the
-// mbarrier at `bar_cluster`'s offset in the even CTA of that destination's pair.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void *tmap, int x, int y, uint32_t bar_cluster,
-                                                    uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::"
-        "cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster), "h"(cta_mask)
         : "memory");
 }
 
