@@ -314,6 +314,24 @@ RL_LOSS_API rl_status rl_gae_advantages(const rl_gae_config *config, int32_t num
                                         float *returns, void *workspace, size_t workspace_bytes,
                                         uint32_t *device_status, void *stream);
 
+/* Failure injection for tests of the failure detection above (the pages have
+ * no counterpart): rl_gae_advantages with the map of chunk `withhold_chunk`
+ * (8192-token chunks, counted from token 0) never published, and each wait
+ * for a neighbouring chunk's map bounded by `wait_limit_s` seconds
+ * (0 < wait_limit_s <= 1; rl_gae_advantages uses 1 s). The chunks whose
+ * look-back needs the withheld map wait that long, raise RL_ERR_TIMEOUT in
+ * `device_status` and treat the chunk as a response end, so their advantages
+ * are wrong but the launch always completes and the GPU stays usable. No
+ * fault, trap or unbounded wait is involved. RL_ERR_INVALID_ARG for
+ * withhold_chunk < 0 or wait_limit_s outside (0, 1]; otherwise as
+ * rl_gae_advantages. */
+RL_LOSS_API rl_status rl_gae_advantages_withheld(const rl_gae_config *config, int32_t num_tokens, int32_t num_seqs,
+                                                 const float *rewards, const float *values, const uint8_t *mask,
+                                                 const int32_t *cu_seqlens, const int32_t *rollout_ids,
+                                                 float *advantages, float *returns, void *workspace,
+                                                 size_t workspace_bytes, uint32_t *device_status, void *stream,
+                                                 int32_t withhold_chunk, double wait_limit_s);
+
 /* ---- Deterministic top-k over DSA indexer scores ----------------------
  * "GLM-5: from Vibe Coding to Agentic Engineering", section 3.2 ("DSA RL
  * insights"): the DSA indexer keeps the k = 2048 best-scoring key positions of

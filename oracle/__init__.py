@@ -244,7 +244,8 @@ def projection_rows(row_ids, hidden_bits, w_bits, targets, logp_old, logp_infer,
     return out
 
 
-def projection_forward_stats(hidden_bits, w_bits, batch: dict, p: LossParams, row_block: int = 1024) -> dict:
+def projection_forward_stats(hidden_bits, w_bits, batch: dict, p: LossParams, row_block: int = 1024,
+                             w64: np.ndarray | None = None) -> dict:
     """The forward of the fused path over every row, streamed in blocks of
     ``row_block`` rows so that no [T, V] array is held: per token the log-prob,
     entropy, flags, objective term and dL/dlogp (``g``), and the exact loss of
@@ -253,7 +254,7 @@ def projection_forward_stats(hidden_bits, w_bits, batch: dict, p: LossParams, ro
     cu = batch["cu_seqlens"]
     T = int(cu[-1])
     n, adv, w = seq_prep(cu, batch["mask"], batch["rewards_or_adv"], p)
-    W = bf16_bits_to_f64(w_bits)
+    W = bf16_bits_to_f64(w_bits) if w64 is None else w64
     keys = ("logp", "entropy", "flags", "tok_obj", "g")
     parts = {k: [] for k in keys}
     for r0 in range(0, T, row_block):

@@ -232,7 +232,8 @@ int32_t oracle_rows(int64_t n_rows, const int64_t *row_ids, int64_t V, int64_t l
         double H = 0.0;
         for (int64_t v = 0; v < V; ++v) {
             double lp = logit_at(row, dtype, v) - logZ;
-            H -= exp(lp) * lp;
+            const double pv = exp(lp);
+            if (pv > 0.0) H -= pv * lp; /* p log p -> 0 as p -> 0: a -inf logit adds nothing */
         }
         entropy[k] = H;
 

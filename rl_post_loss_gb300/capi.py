@@ -106,6 +106,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "rl_loss_projection_setup": ([P, ctypes.c_int32, ctypes.c_int32], st),
         "rl_gae_advantages": ([ctypes.POINTER(rl_gae_config), ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P, P, P,
                                ctypes.c_size_t, P, P], st),
+        "rl_gae_advantages_withheld": ([ctypes.POINTER(rl_gae_config), ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P,
+                                        P, P, ctypes.c_size_t, P, P, ctypes.c_int32, ctypes.c_double], st),
         "rl_gae_workspace_bytes": ([ctypes.c_int32], ctypes.c_size_t),
         "rl_topk_max_k": ([], ctypes.c_int32),
         "rl_topk": ([ctypes.POINTER(rl_topk_config), ctypes.c_int32, P, ctypes.c_int64, P, P, P, ctypes.c_int64, P, P],
@@ -219,6 +221,14 @@ def rl_gae_advantages(config: rl_gae_config, num_tokens, num_seqs, rewards, valu
     return load().rl_gae_advantages(ctypes.byref(config), num_tokens, num_seqs, rewards, values, mask, cu_seqlens,
                                     rollout_ids, advantages, returns, workspace, workspace_bytes, device_status,
                                     ctypes.c_void_p(stream))
+
+
+def rl_gae_advantages_withheld(config: rl_gae_config, num_tokens, num_seqs, rewards, values, mask, cu_seqlens,
+                               rollout_ids, advantages, returns, workspace, workspace_bytes, device_status, stream,
+                               withhold_chunk, wait_limit_s) -> int:
+    return load().rl_gae_advantages_withheld(ctypes.byref(config), num_tokens, num_seqs, rewards, values, mask,
+                                             cu_seqlens, rollout_ids, advantages, returns, workspace, workspace_bytes,
+                                             device_status, ctypes.c_void_p(stream), withhold_chunk, wait_limit_s)
 
 
 def rl_gae_workspace_bytes(num_tokens: int) -> int:

@@ -29,8 +29,8 @@
 // decoupled look-back with inclusive values. It waits only for the chunks up
 // to those stopping points. Every floating-point result depends only on the
 // inputs, never on timing: bit-identical from run to run. Waits are bounded
-// (1 s of %globaltimer); one that runs out raises RL_ERR_TIMEOUT and treats
-// the chunk as a response end. The last block past its look-back clears the
+// (1 s of %globaltimer by default); one that runs out raises RL_ERR_TIMEOUT
+// and treats the chunk as a response end. The last block past its look-back clears the
 // flags and the ticket (records are only read under a flag set by the same
 // launch), so the workspace is ready for the next launch.
 #include <atomic>
@@ -47,7 +47,6 @@ constexpr int kTok = 32;                 // consecutive tokens per thread
 constexpr int kChunk = kThreads * kTok;  // tokens per chunk
 constexpr int kVec = kTok / 4;           // float4 groups per thread
 constexpr unsigned kFull = 0xffffffffu;
-constexpr unsigned long long kWaitNs = 1000000000ull;
 // Dynamic shared memory: rewards and values (one 128-byte row per thread,
 // its eight 16-byte groups XOR-swizzled by the row index so that the 16-byte
 // reads of a quarter warp hit distinct banks), then the mask bytes.
@@ -464,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p) {
         const GaeMap wi = warp_suffix<kCross>(lane < kThreads / 32 ? s_wtot[lane] : map_identity());
         agg = shfl_map<kCross>(wi, 0);
         if (warp == 1) {
-            if (lane == 0) {  // publish (the release fence stalls this warp, not the look-back)
+            if (lane == 0 && k != p.withhold_chunk) {  // publish (the release fence stalls this warp, not the look-back)
                 ChunkRecord *rec = recs + k;
                 *reinterpret_cast<float4 *>(rec) = make_float4(agg.p, agg.q, agg.c, agg.vf);
                 *(reinterpret_cast<int4 *>(rec) + 1) = make_int4((int)agg.bits, agg.n_resp, agg.n_roll, 0);
@@ -497,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p) {
                             ready = true;
                             m = load_record(recs + j);
                             if (kCross && f >= 2u) incl_roll = __ldcg(&recs[j].roll_incl);
-                        } else if (global_ns() - t_begin > kWaitNs) {
+                        } else if (global_ns() - t_begin > p.wait_ns) {
                             gae_raise(p.status, RL_ERR_TIMEOUT);
                             ready = true;  // treated as a response end
                         }
@@ -538,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p) {
     __syncthreads();
     if (warp == 1) {
         if (lane == 0) {
-            if (kCross) {
+            if (kCross && k != p.withhold_chunk) {
                 recs[k].roll_incl = agg.n_roll + ((agg.bits & kPassRoll) ? s_ER : 0);
                 st_release(&recs[k].flag, 2u);
             }

@@ -579,12 +579,12 @@ extern "C" RL_LOSS_API size_t rl_gae_workspace_bytes(int32_t num_tokens) {
     return rlk::gae_workspace_bytes(num_tokens < 0 ? 0 : num_tokens);
 }
 
-extern "C" RL_LOSS_API rl_status rl_gae_advantages(const rl_gae_config *config, int32_t num_tokens, int32_t num_seqs,
-                                                   const float *rewards, const float *values, const uint8_t *mask,
-                                                   const int32_t *cu_seqlens, const int32_t *rollout_ids,
-                                                   float *advantages, float *returns, void *workspace,
-                                                   size_t workspace_bytes, uint32_t *device_status,
-                                                   void *stream_ptr) {
+namespace {
+
+rl_status gae_call(const rl_gae_config *config, int32_t num_tokens, int32_t num_seqs, const float *rewards,
+                   const float *values, const uint8_t *mask, const int32_t *cu_seqlens, const int32_t *rollout_ids,
+                   float *advantages, float *returns, void *workspace, size_t workspace_bytes,
+                   uint32_t *device_status, void *stream_ptr, uint64_t wait_ns, int32_t withhold_chunk) {
     if (!config) return RL_ERR_INVALID_ARG;
     const rl_gae_config &c = *config;
     if (!(c.gamma >= 0.0 && c.gamma <= 1.0) || !(c.lambda >= 0.0 && c.lambda <= 1.0)) return RL_ERR_INVALID_ARG;
@@ -617,8 +617,36 @@ extern "C" RL_LOSS_API rl_status rl_gae_advantages(const rl_gae_config *config, 
     p.returns = returns;
     p.workspace = workspace;
     p.status = device_status;  // may be NULL: the bits are then not reported
+    p.wait_ns = wait_ns;
+    p.withhold_chunk = withhold_chunk;
     if (rlk::launch_gae(p, reinterpret_cast<cudaStream_t>(stream_ptr)) != cudaSuccess) return RL_ERR_CUDA;
     return RL_OK;
+}
+
+}  // namespace
+
+extern "C" RL_LOSS_API rl_status rl_gae_advantages(const rl_gae_config *config, int32_t num_tokens, int32_t num_seqs,
+                                                   const float *rewards, const float *values, const uint8_t *mask,
+                                                   const int32_t *cu_seqlens, const int32_t *rollout_ids,
+                                                   float *advantages, float *returns, void *workspace,
+                                                   size_t workspace_bytes, uint32_t *device_status,
+                                                   void *stream_ptr) {
+    return gae_call(config, num_tokens, num_seqs, rewards, values, mask, cu_seqlens, rollout_ids, advantages, returns,
+                    workspace, workspace_bytes, device_status, stream_ptr, 1000000000ull, -1);
+}
+
+extern "C" RL_LOSS_API rl_status rl_gae_advantages_withheld(const rl_gae_config *config, int32_t num_tokens,
+                                                            int32_t num_seqs, const float *rewards,
+                                                            const float *values, const uint8_t *mask,
+                                                            const int32_t *cu_seqlens, const int32_t *rollout_ids,
+                                                            float *advantages, float *returns, void *workspace,
+                                                            size_t workspace_bytes, uint32_t *device_status,
+                                                            void *stream_ptr, int32_t withhold_chunk,
+                                                            double wait_limit_s) {
+    if (withhold_chunk < 0 || !(wait_limit_s > 0.0 && wait_limit_s <= 1.0)) return RL_ERR_INVALID_ARG;
+    return gae_call(config, num_tokens, num_seqs, rewards, values, mask, cu_seqlens, rollout_ids, advantages, returns,
+                    workspace, workspace_bytes, device_status, stream_ptr, (uint64_t)(wait_limit_s * 1e9),
+                    withhold_chunk);
 }
 
 extern "C" RL_LOSS_API int32_t rl_topk_max_k(void) { return rlk::topk_max_k(); }

@@ -124,10 +124,11 @@ __device__ __forceinline__ void accumulate(RowStats2 &st, const float (&x)[N]) {
     }
 #pragma unroll
     for (int k = 0; k < N; ++k) {
+        // a -inf logit has probability 0 and adds nothing, also to the entropy sum (0 log 0 = 0)
         const float d2 = fmaf(x[k], kLog2e, -st.m2);
-        const float e = ex2_approx(d2);
+        const float e = x[k] == -INFINITY ? 0.f : ex2_approx(d2);
         st.s += e;
-        st.u2 = fmaf(e, d2, st.u2);
+        st.u2 = e > 0.f ? fmaf(e, d2, st.u2) : st.u2;
     }
 }
 

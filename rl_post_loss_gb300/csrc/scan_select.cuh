@@ -25,6 +25,8 @@ struct GaeParams {
     void *workspace;           // gae_workspace_bytes(T), zeroed before the first launch
     int32_t vec;               // set by launch_gae: every array 16-byte aligned
     uint32_t *status;
+    uint64_t wait_ns;          // bound on each wait for a neighbouring chunk's map (1 s)
+    int32_t withhold_chunk;    // failure injection: this chunk never publishes its map (-1: none)
 };
 
 // Row-wise deterministic top-k (see topk.cu).

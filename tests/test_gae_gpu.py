@@ -239,6 +239,49 @@ def test_gae_repeated_calls_are_bit_identical_and_leave_the_workspace_clear():
         assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
 
 
+def test_a_withheld_chunk_map_runs_the_bounded_wait_out():
+    """Failure detection without a fault: the map of chunk 20 of a 300,000-token response
+    (37 chunks) is never published, so the look-back of the chunks to its left waits for it
+    until the 20-ms bound runs out. The call must complete with RL_ERR_TIMEOUT raised; the
+    withheld chunk and those to its right (which never wait for it) must equal a normal call
+    bit for bit while the chunks to its left differ; the workspace must be clear again, and
+    the next normal call must repeat the first one bit for bit."""
+    import time
+    gb = synthetic.make_gae_batch("cuda", lengths=[300000, 3, 140000, 70000], segments=2)
+    T, S = gb.num_tokens, gb.cu_seqlens.numel() - 1
+    ref = capi.gae(gb.rewards, gb.values, gb.mask, gb.cu_seqlens, gb.gamma, gb.lam, True, rollout_ids=gb.rollout_ids)
+    torch.cuda.synchronize()
+    w = 20
+    adv = torch.full((T,), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = capi.gae_workspace(T, "cuda")
+    cfg = capi.rl_gae_config(gb.gamma, gb.lam, 1, 1)
+    p = capi._ptr
+    t0 = time.perf_counter()
+    rc = capi.rl_gae_advantages_withheld(cfg, T, S, p(gb.rewards), p(gb.values), p(gb.mask), p(gb.cu_seqlens),
+                                         p(gb.rollout_ids), p(adv), None, p(ws), ws.numel(), p(st),
+                                         torch.cuda.current_stream().cuda_stream, w, 0.02)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 10.0
+    assert capi.status_bits_to_names(int(st.item())) == ["RL_ERR_TIMEOUT"]
+    lo = w * 8192
+    assert torch.equal(adv[lo:].view(torch.int32), ref[lo:].view(torch.int32))
+    assert not torch.equal(adv[:lo], ref[:lo])
+    assert _workspace_is_clear(T)
+    st.zero_()
+    again = capi.gae(gb.rewards, gb.values, gb.mask, gb.cu_seqlens, gb.gamma, gb.lam, True,
+                     rollout_ids=gb.rollout_ids, device_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(again.view(torch.int32), ref.view(torch.int32))
+    # arguments the injection entry point refuses before launching anything
+    for bad_w, bad_s in ((-1, 0.02), (w, 0.0), (w, 2.0)):
+        assert capi.rl_gae_advantages_withheld(cfg, T, S, p(gb.rewards), p(gb.values), p(gb.mask),
+                                               p(gb.cu_seqlens), p(gb.rollout_ids), p(adv), None, p(ws),
+                                               ws.numel(), p(st), 0, bad_w, bad_s) == capi.CODES["RL_ERR_INVALID_ARG"]
+
+
 @pytest.mark.slow
 def test_gae_full_size_repeated_launches_are_bit_identical():
     """Ten launches on the full workload (2048 chunks, several waves): the tickets go to whichever

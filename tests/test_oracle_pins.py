@@ -86,6 +86,20 @@ def test_dominant_logit_and_entropy_bounds():
             assert np.all(o["entropy"] >= -1e-15) and np.all(o["entropy"] <= math.log(V) + 1e-12)
 
 
+def test_minus_infinity_logits_are_absent_entries():
+    """A -inf logit has probability 0: the log-probs and the entropy of the other entries
+    equal those of the row without it (0 log 0 = 0), and its own log-prob is -inf."""
+    z = np.array([1.0, -np.inf, 0.5, -np.inf, 2.0, -3.0])
+    keep = np.isfinite(z)
+    full = _row_logp(z)
+    part = _row_logp(z[keep])
+    np.testing.assert_allclose(full["logp"][keep], part["logp"], rtol=0, atol=1e-15)
+    assert np.all(full["logp"][~keep] == -np.inf)
+    np.testing.assert_allclose(full["entropy"], part["entropy"][0], rtol=0, atol=1e-15)
+    one = _row_logp(np.array([-np.inf, 4.0, -np.inf]))
+    assert one["logp"][1] == 0.0 and np.all(one["entropy"] == 0.0)
+
+
 def test_bf16_widening_is_exact():
     # bf16 bit patterns of 1.0, -2.5, 0.15625 and 3.0 (upper halves of binary32 words)
     bits = np.array([[0x3F80, 0xC020, 0x3E20, 0x4040]], np.uint16)

@@ -141,6 +141,28 @@ def test_bad_targets_are_flagged_and_excluded():
     check_all(b, out, dz_rows="all")
 
 
+def test_minus_infinity_logits_are_zero_probability():
+    """A -inf logit (a masked vocabulary entry) is valid: probability 0, no entropy term
+    (0 log 0 = 0), a zero gradient, no status bit; the short-row and the long-row kernel.
+    One row keeps only its target finite: log-prob 0 and entropy 0."""
+    for dtype, V in (("f32", 4096), ("bf16", 200003)):
+        b = synthetic.make_batch(0, "cuda", lengths=_lengths(0, 1, 10, 40), vocab=V,
+                                 case_overrides={"dtype": dtype})
+        g = torch.Generator(device="cuda").manual_seed(V)
+        hole = torch.rand((b.num_tokens, V), generator=g, device="cuda") < 0.1
+        hole[torch.arange(b.num_tokens, device="cuda"), b.targets.long()] = False
+        hole[3] = True
+        hole[3, b.targets[3].long()] = False
+        view = b.logits[:, :V]
+        view[hole] = float("-inf")
+        _, out, bits = _run(b)
+        assert bits == 0, capi.status_bits_to_names(bits)
+        assert bool(torch.isfinite(out["entropy"]).all()) and bool(torch.isfinite(out["loss_f64"]).all())
+        assert abs(out["logp"][3].item()) <= 1e-6 and abs(out["entropy"][3].item()) <= 1e-6
+        assert bool((out["dlogits"][:, :V][hole] == 0).all())
+        check_all(b, out, dz_rows="all" if dtype == "f32" else 16)
+
+
 def test_nonfinite_and_malformed_offsets_raise_device_bits():
     for dtype, V in (("f32", 4096), ("bf16", 200003)):  # the short-row and the long-row kernel
         for bad in (float("nan"), float("inf")):

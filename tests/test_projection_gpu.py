@@ -2,6 +2,8 @@
 the tcgen05 projection GEMM alone (ragged tiles, full width), the whole fused
 forward+backward on small cases spanning several chunks and tiles, its
 determinism, and the full-size case on sampled rows plus identities."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -112,6 +114,88 @@ def test_fused_projection_bit_identical_runs():
     for k in outs[0]:
         for o in outs[1:]:
             assert torch.equal(outs[0][k].view(torch.uint8), o[k].view(torch.uint8)), k
+
+
+def _rows_close(name, got, want):
+    """Per-row relative L2 <= 1e-2 and element-wise |got - want| <= 3e-2 |want| + 1e-2 rms(row);
+    rows whose exact gradient is zero must be exact zeros."""
+    nrm = np.linalg.norm(want, axis=1)
+    nz = nrm > 0
+    rn = np.linalg.norm(got - want, axis=1)[nz] / nrm[nz]
+    assert rn.size == 0 or rn.max() <= 1e-2, f"{name} row relative L2 {rn.max()}"
+    rms = np.sqrt((want ** 2).mean(axis=1, keepdims=True))
+    assert np.all(np.abs(got - want) <= 3e-2 * np.abs(want) + 1e-2 * rms), name
+    assert np.all(got[~nz] == 0.0), f"{name}: rows with zero gradient must be exact zeros"
+    return float(rn.max()) if rn.size else 0.0
+
+
+def _check_exact_forward_and_sampled_grads(pb, out, n_vocab_rows=256, n_token_rows=64, seed=5):
+    """The loss against the exact fp64 loss over every row (streamed forward), every
+    row's log-prob / entropy / flags, and sampled rows of dL/dW and dL/dh element by
+    element (dL/dW_v = sum_t dL/dz_tv h_t needs the forward of every row)."""
+    b = pb.batch
+    T, H, V = b.num_tokens, pb.hidden_dim, b.vocab
+    p = params_for(b)
+    npb = {k: getattr(b, k).cpu().numpy() for k in
+           ("targets", "logp_old", "logp_infer", "mask", "cu_seqlens", "rewards_or_adv")}
+    hb, wb = _bits(pb.hidden[:, :H]), _bits(pb.w[:, :H])
+    h64, W64 = oracle.bf16_bits_to_f64(hb), oracle.bf16_bits_to_f64(wb)
+    ref = oracle.projection_forward_stats(hb, None, npb, p, w64=W64)
+    L = out["loss_f64"].item()
+    assert abs(L - ref["loss"]) <= 1e-4 * abs(ref["loss"]) + 1e-12, (L, ref["loss"])
+    lp = out["logp"].cpu().numpy().astype(np.float64)
+    assert np.abs(lp - ref["logp"]).max() <= TOL_LOGP_STATED
+    assert np.abs(lp - ref["logp"]).max() <= TOL_LOGP_STRICT
+    assert np.abs(out["entropy"].cpu().numpy() - ref["entropy"]).max() <= TOL_LOGP_STRICT
+    f = out["flags"].cpu().numpy()
+    assert np.array_equal(f & 0xD, ref["flags"] & 0xD)
+    advt = np.repeat(ref["adv"], np.diff(npb["cu_seqlens"]))
+    rule = oracle.clip_active_vec(out["logp"].cpu().numpy(), npb["logp_old"], advt, p.eps_low, p.eps_high)
+    assert np.array_equal((f >> 1) & 1, rule)
+    rng = np.random.default_rng(seed)
+    # vocabulary rows: both ends, tile edges, the targets of a few tokens, and a random sample
+    vids = np.unique(np.concatenate([[0, V - 1, 255, 256, 511, 512], npb["targets"][rng.choice(T, 16)],
+                                     rng.choice(V, n_vocab_rows, replace=False)]))[:n_vocab_rows]
+    dw_ref = oracle.projection_dw_rows(vids, h64, W64, npb["targets"], ref["logp"], ref["g"])
+    dw = out["dw_lm"][torch.as_tensor(vids, device="cuda"), :H].double().cpu().numpy()
+    rep = {"dW_row_rel_l2_max": _rows_close("dW", dw, dw_ref)}
+    tids = np.unique(np.concatenate([[0, T - 1, min(4095, T - 1), min(4096, T - 1)],
+                                     rng.choice(T, n_token_rows, replace=False)]))
+    n, adv, w = oracle.seq_prep(npb["cu_seqlens"], npb["mask"], npb["rewards_or_adv"], p)
+    rows = oracle.projection_rows(tids, hb, None, npb["targets"], npb["logp_old"], npb["logp_infer"], npb["mask"],
+                                  npb["cu_seqlens"], adv, w, p, want_dh=True, w64=W64)
+    dh = out["dhidden"][torch.as_tensor(tids, device="cuda"), :H].double().cpu().numpy()
+    rep["dH_row_rel_l2_max"] = _rows_close("dhidden", dh, rows["dh"])
+    rep.update(loss=L, loss_oracle=ref["loss"], logp_max_err=float(np.abs(lp - ref["logp"]).max()))
+    return rep
+
+
+def test_fused_projection_mid_size_exact():
+    """8,192 tokens (two 4,096-row chunks) x V = 32,768 x H = 6,144: the exact loss,
+    every row's log-prob, and 256 dL/dW rows and 64 dL/dh rows element by element."""
+    pb = synthetic.make_projection_batch("cuda", prompts=8, vocab=32768)
+    rl = capi.projection_handle(pb)
+    out = capi.alloc_projection_outputs(pb)
+    capi.run_projection(rl, pb, out)
+    torch.cuda.synchronize()
+    assert rl.device_status() & ~(1 << capi.CODES["RL_ERR_EMPTY_SEQ"]) == 0
+    print(_check_exact_forward_and_sampled_grads(pb, out))
+
+
+@pytest.mark.slow
+@pytest.mark.skipif(os.environ.get("RL_LOSS_FULL_ORACLE") != "1",
+                    reason="the exact full-size oracle takes minutes of host time: set RL_LOSS_FULL_ORACLE=1")
+def test_fused_projection_full_size_exact_loss_and_dw_rows():
+    """The full case (65,536 tokens x V = 151,552 x H = 6,144): the loss against the
+    exact fp64 loss streamed over every row, and 256 dL/dW rows element by element."""
+    torch.cuda.empty_cache()
+    pb = synthetic.make_projection_batch("cuda")
+    rl = capi.projection_handle(pb)
+    out = capi.alloc_projection_outputs(pb)
+    capi.run_projection(rl, pb, out)
+    torch.cuda.synchronize()
+    assert rl.device_status() & ~(1 << capi.CODES["RL_ERR_EMPTY_SEQ"]) == 0
+    print(_check_exact_forward_and_sampled_grads(pb, out))
 
 
 @pytest.mark.slow
