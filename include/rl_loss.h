@@ -169,7 +169,7 @@ typedef struct rl_loss_outputs {
 } rl_loss_outputs;
 
 /* Kernel timing collected with CUDA events (see rl_loss_profile_start). */
-#define RL_PROFILE_MAX_KERNELS 8
+#define RL_PROFILE_MAX_KERNELS 12
 typedef struct rl_loss_profile {
     int32_t num_kernels;
     char names[RL_PROFILE_MAX_KERNELS][32];
@@ -185,9 +185,13 @@ RL_LOSS_API rl_status rl_loss_create(const rl_loss_config *config, rl_loss_t *ou
 /* Frees the workspace and the handle (synchronises the device first). NULL is a no-op. */
 RL_LOSS_API rl_status rl_loss_destroy(rl_loss_t handle);
 
-/* The fused forward + backward pass of Eq. (1) over one batch. Enqueues four
- * kernels on `stream` (per-response prep, the fused row kernel, two
- * fixed-order reductions) and returns without synchronising. */
+/* The fused forward + backward pass of Eq. (1) over one batch. Enqueues six
+ * kernels on `stream` (per-response prep, per-token prep, the fused row
+ * kernel, the entropy of the rows that hold -inf logits, two fixed-order
+ * reductions) and returns without synchronising. A -inf logit is a valid
+ * input (probability 0, e.g. a masked vocabulary entry): it adds nothing to
+ * the entropy (0 log 0 = 0) and gets a zero gradient; NaN and +inf logits are
+ * non-finite (RL_ERR_NONFINITE). */
 RL_LOSS_API rl_status rl_loss_forward_backward(rl_loss_t handle, const rl_loss_inputs *inputs,
                                                const rl_loss_outputs *outputs, void *stream);
 

@@ -71,8 +71,8 @@ RL_TOPK_BY_SCORE, RL_TOPK_BY_POSITION = 0, 1
 
 
 class rl_loss_profile(ctypes.Structure):
-    _fields_ = [("num_kernels", ctypes.c_int32), ("names", (ctypes.c_char * 32) * 8),
-                ("launches", ctypes.c_int64 * 8), ("total_ms", ctypes.c_double * 8)]
+    _fields_ = [("num_kernels", ctypes.c_int32), ("names", (ctypes.c_char * 32) * 12),
+                ("launches", ctypes.c_int64 * 12), ("total_ms", ctypes.c_double * 12)]
 
 
 _lib = None

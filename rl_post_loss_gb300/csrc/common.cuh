@@ -251,6 +251,7 @@ struct RowParams {
     uint8_t *flags_out;
     float *tok_obj;
     uint32_t *status;
+    uint8_t *fix_rows;   // workspace [T], zero: rows whose entropy the fix kernel redoes
 };
 
 struct ReduceParams {
@@ -280,5 +281,7 @@ cudaError_t launch_final_reduce(const ReduceParams &p, cudaStream_t stream);
 
 // The fused row kernel (one block per logits row).
 cudaError_t launch_row_loss(const RowParams &p, int dtype, cudaStream_t stream);
+// The entropy of the rows launch_row_loss marked in p.fix_rows (rows holding -inf logits).
+cudaError_t launch_entropy_fix(const RowParams &p, int dtype, cudaStream_t stream);
 
 }  // namespace rlk

@@ -16,11 +16,13 @@ enum RlKernelClass {
     kFinalReduce,
     kProjGemm,
     kProjRows,
-    kProjBwd,  // both products of the projection backward (one tcgen05 launch per chunk)
+    kProjBwd,     // both products of the projection backward (one tcgen05 launch per chunk)
+    kEntropyFix,  // the entropy of rows holding -inf logits
     kNumKernels
 };
-static const char *const kKernelNames[kNumKernels] = {"seg_prep",     "token_prep", "row_loss",  "seg_reduce",
-                                                      "final_reduce", "proj_gemm",  "proj_rows", "proj_bwd"};
+static const char *const kKernelNames[kNumKernels] = {"seg_prep",  "token_prep", "row_loss", "seg_reduce",
+                                                      "final_reduce", "proj_gemm", "proj_rows", "proj_bwd",
+                                                      "entropy_fix"};
 constexpr size_t kProfSlotsPerCall = 160;  // enough for a projection call of 32 chunks (or a host call of 64 blocks)
 constexpr int kMaxCopyChunks = 64;         // logits blocks of rl_loss_forward_backward_from_host
 
@@ -39,6 +41,7 @@ struct rl_loss_handle_s {
     int32_t *seq_n, *seq_cnt;
     float *tok_obj, *tok_ent;
     uint8_t *tok_flags;
+    uint8_t *tok_fix;  // rows whose entropy the fix kernel redoes (zero between calls)
     float4 *tok_rec;
     uint32_t *tok_meta;
     float *loss_scratch;

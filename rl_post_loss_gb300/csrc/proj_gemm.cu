@@ -239,14 +239,19 @@ __device__ __forceinline__ void epi_stats(const TcProblem &q, const void *dmap, 
             }
             st.m2 = mv2;
         }
+        if (st.m2 == -INFINITY) {  // every value so far is -inf (adds nothing) or NaN (must show)
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if (j < nvalid) {  // a -inf logit adds nothing (0 log 0 = 0)
-                const float zj = __uint_as_float(r[j]);
-                const float d2 = fmaf(zj, kLog2e, -st.m2);
-                const float e = zj == -INFINITY ? 0.f : ex2_approx(d2);
-                st.s += e;
-                st.u2 = e > 0.f ? fmaf(e, d2, st.u2) : st.u2;
+            for (int j = 0; j < 32; ++j)
+                if (j < nvalid && !(__uint_as_float(r[j]) == __uint_as_float(r[j]))) st.s = __uint_as_float(r[j]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (j < nvalid) {  // a -inf logit adds nothing (0 log 0 = 0): see the row kernel
+                    const float d2 = fmaf(__uint_as_float(r[j]), kLog2e, -st.m2);
+                    const float e = ex2_approx(d2);
+                    st.s += e;
+                    st.u2 = fmaf(e, fmaxf(d2, -256.f), st.u2);
+                }
             }
         }
         if (q.d) {

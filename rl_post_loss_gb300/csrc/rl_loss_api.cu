@@ -34,6 +34,7 @@ static size_t workspace_layout(const rl_loss_config &c, rl_loss_handle_s *h, cha
     char *tok_obj = carve(T * sizeof(float));
     char *tok_ent = carve(T * sizeof(float));
     char *tok_flags = carve(T * sizeof(uint8_t));
+    char *tok_fix = carve(T * sizeof(uint8_t));
     char *tok_rec = carve(T * sizeof(float4));
     char *tok_meta = carve(T * sizeof(uint32_t));
     char *loss_scratch = carve(4 * sizeof(float));
@@ -49,6 +50,7 @@ static size_t workspace_layout(const rl_loss_config &c, rl_loss_handle_s *h, cha
         h->tok_obj = reinterpret_cast<float *>(tok_obj);
         h->tok_ent = reinterpret_cast<float *>(tok_ent);
         h->tok_flags = reinterpret_cast<uint8_t *>(tok_flags);
+        h->tok_fix = reinterpret_cast<uint8_t *>(tok_fix);
         h->tok_rec = reinterpret_cast<float4 *>(tok_rec);
         h->tok_meta = reinterpret_cast<uint32_t *>(tok_meta);
         h->loss_scratch = reinterpret_cast<float *>(loss_scratch);
@@ -184,6 +186,7 @@ static rl_status prepare_call(rl_loss_handle_s *h, const rl_loss_inputs *in, con
     rp.flags_out = out->flags ? out->flags : h->tok_flags;
     rp.tok_obj = h->tok_obj;
     rp.status = h->status;
+    rp.fix_rows = h->tok_fix;
 
     rlk::ReduceParams &rd = L.rd;
     rd = rlk::ReduceParams{};
@@ -223,6 +226,7 @@ static void restrict_rows(LossLaunch &B, const LossLaunch &L, int r0, int r1) {
     rp.entropy_out = L.rp.entropy_out + r0;
     rp.flags_out = L.rp.flags_out + r0;
     rp.tok_obj = L.rp.tok_obj + r0;
+    rp.fix_rows = L.rp.fix_rows + r0;
     rp.num_tokens = r1 - r0;
 }
 
@@ -261,6 +265,13 @@ static rl_status launch_loss(rl_loss_handle_s *h, const LossLaunch &L, const int
         h->prof_end(slot, stream);
         if (err != cudaSuccess) return failed(err);
         row_launches += 2;
+    }
+    if (L.rp.num_tokens > 0) {  // after every row block: the entropy of rows holding -inf logits
+        slot = h->prof_begin(kEntropyFix, stream);
+        err = rlk::launch_entropy_fix(L.rp, c.logits_dtype, stream);
+        h->prof_end(slot, stream);
+        if (err != cudaSuccess) return failed(err);
+        row_launches += 1;
     }
     slot = h->prof_begin(kSegReduce, stream);
     err = rlk::launch_seg_reduce(L.rd, stream);
@@ -330,7 +341,8 @@ RL_LOSS_API rl_status rl_loss_create(const rl_loss_config *config, rl_loss_t *ou
         return RL_ERR_CUDA;
     }
     workspace_layout(c, h, reinterpret_cast<char *>(h->ws));
-    if (cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess) {
+    if (cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(h->tok_fix, 0, (size_t)c.max_tokens) != cudaSuccess) {
         cudaFree(h->ws);
         delete h;
         return RL_ERR_CUDA;

@@ -12,6 +12,7 @@
 // Rows with g == 0 (masked, popped, clipped, zero advantage) are written as
 // +0.0 without evaluating the softmax a second time.
 #include <algorithm>
+#include <cfloat>
 #include <mutex>
 
 #include "common.cuh"
@@ -124,13 +125,19 @@ __device__ __forceinline__ void accumulate(RowStats2 &st, const float (&x)[N]) {
     }
 #pragma unroll
     for (int k = 0; k < N; ++k) {
-        // a -inf logit has probability 0 and adds nothing, also to the entropy sum (0 log 0 = 0)
         const float d2 = fmaf(x[k], kLog2e, -st.m2);
-        const float e = x[k] == -INFINITY ? 0.f : ex2_approx(d2);
+        const float e = ex2_approx(d2);
         st.s += e;
-        st.u2 = e > 0.f ? fmaf(e, d2, st.u2) : st.u2;
+        st.u2 = fmaf(e, d2, st.u2);  // NaN for a -inf logit (0 * -inf): see kRowStart
     }
 }
+
+// Start of a thread's statistics: a finite reference point, so that a -inf logit gives e = 0
+// (it adds nothing to s) even before the thread has seen a finite one. Only u2 then turns NaN
+// (0 * -inf): a row whose s is finite but whose u2 is NaN holds -inf logits and no NaN or +inf,
+// and its entropy is redone by entropy_fix_kernel. Merging a start that saw nothing scales it
+// by 2^(-FLT_MAX - M) = 0: bit for bit the same as merging an empty part.
+constexpr RowStats2 kRowStart{-FLT_MAX, 0.f, 0.f};
 
 // kStage: the first stage_vecs 16-byte groups of the row are kept in shared memory between the
 // passes (each thread re-reads only the groups it wrote).
@@ -153,7 +160,7 @@ __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twop
     const float4 rec = __ldg(p.rec + row);
     const uint32_t meta = __ldg(p.meta + row);
 
-    RowStats2 st = empty_stats();
+    RowStats2 st = kRowStart;
 #pragma unroll kUnroll
     for (int k = threadIdx.x; k < nvec; k += kRowThreads) {
         float x[VEC];
@@ -180,6 +187,8 @@ __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twop
         if (lane == 0) {
             const RowOut o = finish_row(w, rec, meta, p.c, p.teacher ? __ldg(p.teacher + row) : 0.f);
             if (!isfinite(o.logZ2)) raise_status(p.status, RL_ERR_NONFINITE);  // NaN or +inf logit in the row
+            // -inf logits (kRowStart): the entropy is redone by entropy_fix_kernel
+            if (isfinite(w.s) && isnan(w.u2)) p.fix_rows[row] = 1;
             if (p.logp_out) p.logp_out[row] = o.logp;
             p.entropy_out[row] = o.H;
             p.flags_out[row] = static_cast<uint8_t>(o.flags);
@@ -226,6 +235,77 @@ __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twop
     }
 }
 
+// The entropy of the rows the row kernel marked (rows that hold -inf logits): one pass over
+// the row with every term of probability 0 left out (0 log 0 = 0), per-thread strided order
+// and a fixed block tree; the mark is cleared. The blocks scan contiguous ranges of marks.
+template <typename T>
+__global__ void __launch_bounds__(256) entropy_fix_kernel(RowParams p) {
+    using VT = VecTraits<T>;
+    constexpr int VEC = VT::kElems;
+    __shared__ uint8_t s_mark[256];
+    __shared__ RowStats2 s_warp[8];
+    const int T_ = p.num_tokens, V = p.vocab, nvec = V / VEC, tail0 = nvec * VEC;
+    const int per = (T_ + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int r_begin = (int)blockIdx.x * per, r_end = min(T_, r_begin + per);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int base = r_begin; base < r_end; base += 256) {
+        const int r = base + (int)threadIdx.x;
+        const uint8_t m = r < r_end ? p.fix_rows[r] : 0;
+        s_mark[threadIdx.x] = m;
+        if (!__syncthreads_or(m)) continue;
+        for (int i = 0; i < 256 && base + i < r_end; ++i) {
+            if (!s_mark[i]) continue;  // block-uniform
+            const int row = base + i;
+            const char *z = reinterpret_cast<const char *>(p.logits) + (size_t)row * p.ld_logits * sizeof(T);
+            RowStats2 st = empty_stats();
+            auto add = [&](float x) {
+                if (x == -INFINITY) return;
+                const float x2 = x * kLog2e;
+                if (x2 > st.m2) {
+                    if (st.m2 != -INFINITY) {
+                        const float dm = st.m2 - x2;
+                        const float f = ex2_approx(dm);
+                        st.u2 = f * fmaf(dm, st.s, st.u2);
+                        st.s = f * st.s;
+                    }
+                    st.m2 = x2;
+                }
+                const float d2 = fmaf(x, kLog2e, -st.m2);
+                const float e = ex2_approx(d2);
+                st.s += e;
+                if (e > 0.f) st.u2 = fmaf(e, d2, st.u2);
+            };
+            for (int k = threadIdx.x; k < nvec; k += 256) {
+                float x[VEC];
+                VT::load(z + (size_t)k * 16, x);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) add(x[j]);
+            }
+            if (tail0 + (int)threadIdx.x < V) add(VT::load1(z, tail0 + threadIdx.x));
+            st = warp_merge_stats2(st);
+            if (lane == 0) s_warp[warp] = st;
+            __syncthreads();
+            if (warp == 0) {
+                RowStats2 w = lane < 8 ? s_warp[lane] : empty_stats();
+                w = warp_merge_stats2(w);
+                if (lane == 0) {
+                    p.entropy_out[row] = (log2f(w.s) - w.u2 / w.s) * kLn2;
+                    p.fix_rows[row] = 0;
+                }
+            }
+            __syncthreads();
+        }
+        __syncthreads();
+    }
+}
+
+template <typename T>
+cudaError_t launch_fix_for(const RowParams &p, cudaStream_t stream) {
+    const int grid = p.num_tokens < 608 ? p.num_tokens : 608;
+    entropy_fix_kernel<T><<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_for(const RowParams &p, cudaStream_t stream) {
     if ((size_t)p.vocab * sizeof(T) <= kShortRowBytes) {
@@ -259,6 +339,11 @@ cudaError_t launch_for(const RowParams &p, cudaStream_t stream) {
 cudaError_t launch_row_loss(const RowParams &p, int dtype, cudaStream_t stream) {
     if (p.num_tokens == 0) return cudaSuccess;
     return dtype == RL_F32 ? launch_for<float>(p, stream) : launch_for<__nv_bfloat16>(p, stream);
+}
+
+cudaError_t launch_entropy_fix(const RowParams &p, int dtype, cudaStream_t stream) {
+    if (p.num_tokens == 0) return cudaSuccess;
+    return dtype == RL_F32 ? launch_fix_for<float>(p, stream) : launch_fix_for<__nv_bfloat16>(p, stream);
 }
 
 }  // namespace rlk

@@ -229,11 +229,11 @@ def test_profile_and_launch_count():
     for _ in range(3):
         capi.run_batch(rl, b, out)
     prof = rl.profile_read()
-    used = {"seg_prep", "token_prep", "row_loss", "seg_reduce", "final_reduce"}
+    used = {"seg_prep", "token_prep", "row_loss", "entropy_fix", "seg_reduce", "final_reduce"}
     assert used <= set(prof)
     assert all(prof[k][0] == 3 and prof[k][1] > 0 for k in used)
     assert all(n == 0 for k, (n, _) in prof.items() if k not in used)
-    assert rl.launch_count() == 15
+    assert rl.launch_count() == 18
 
 
 def test_alternating_vocab_sizes_on_one_kernel_configuration():
