@@ -393,14 +393,17 @@ def main():
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     loss_host = torch.empty(1, dtype=torch.float64).pin_memory()
     e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # the host link as this run sees it: the same copies alone, just before the timed steps
-    torch.cuda.synchronize()
-    e_start.record(stream)
-    for name, t in host.items():
-        dev_in[name].copy_(t, non_blocking=True)
+    # the host link as this run sees it: the same copies alone, as many times as the e2e steps
+    # (one untimed first), just before them
+    for k in range(args.e2e_steps + 1):
+        if k == 1:
+            torch.cuda.synchronize()
+            e_start.record(stream)
+        for name, t in host.items():
+            dev_in[name].copy_(t, non_blocking=True)
     e_stop.record(stream)
     torch.cuda.synchronize()
-    copy_ms = e_start.elapsed_time(e_stop)
+    copy_ms = e_start.elapsed_time(e_stop) / args.e2e_steps
     for k in range(args.e2e_steps + 1):
         if k == 1:
             torch.cuda.synchronize()
