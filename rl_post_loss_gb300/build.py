@@ -17,6 +17,11 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "librl_loss.so")
+# The debug build: every kernel also checks its index invariants and raises RL_ERR_INTERNAL
+# (skipping the access) where one fails. Built on request, next to the normal library.
+DEBUG_BUILD_DIR = os.path.join(HERE, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(HERE, "librl_loss_debug.so")
+DEBUG_FLAGS = ["-DRL_LOSS_DEBUG_CHECKS"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -47,15 +52,18 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None, debug: bool = False) -> str:
+    build_dir, lib_path = (DEBUG_BUILD_DIR, DEBUG_LIB_PATH) if debug else (BUILD_DIR, LIB_PATH)
+    if debug:
+        extra_flags = DEBUG_FLAGS + (extra_flags or [])
+    os.makedirs(build_dir, exist_ok=True)
     headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
     srcs = sources()
     objs = []
     procs = []
     flags = NVCC_FLAGS + (extra_flags or [])
     for src in srcs:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
             cmd = [nvcc()] + ARCH + flags + ["-c", src, "-o", obj]
@@ -71,13 +79,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
             print(out.decode(errors="replace"), file=sys.stderr)
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(f"--- {s}\n{o}" for s, o in failed))
-    if force or procs or _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + ".tmp%d" % os.getpid()
+    if force or procs or _stale(lib_path, objs):
+        tmp = lib_path + ".tmp%d" % os.getpid()
         cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
         subprocess.check_call(cmd)
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv))

@@ -78,11 +78,13 @@ class rl_loss_profile(ctypes.Structure):
 _lib = None
 
 
-def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load the CUDA library (raises if it has not been built)."""
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built). RL_LOSS_LIB in the
+    environment names another build of it, such as the debug build."""
     global _lib
     if _lib is not None:
         return _lib
+    path = path or os.environ.get("RL_LOSS_LIB") or LIB_PATH
     if not os.path.exists(path):
         raise RuntimeError(f"CUDA library {path} is missing; build it with __graft_entry__.build()")
     lib = ctypes.CDLL(path)

@@ -200,6 +200,19 @@ __device__ __forceinline__ void raise_status(uint32_t *status, rl_status code) {
     atomicOr(status, 1u << static_cast<int>(code));
 }
 
+// Invariant checks of the debug build (RL_LOSS_DEBUG_CHECKS, see build.py): a failed check
+// raises RL_ERR_INTERNAL and the guarded access is skipped. In the normal build the check is
+// `true` and compiles away.
+#ifdef RL_LOSS_DEBUG_CHECKS
+__device__ __forceinline__ bool debug_check_failed(uint32_t *status) {
+    if (status) raise_status(status, RL_ERR_INTERNAL);  // the status word is optional for some entry points
+    return false;
+}
+#define RLK_CHECK(status, cond) ((cond) ? true : ::rlk::debug_check_failed(status))
+#else
+#define RLK_CHECK(status, cond) true
+#endif
+
 // ---------------------------------------------------------------- kernel parameters
 
 struct SeqPrepParams {

@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p) {
     }
     __syncthreads();
     const int k = s_k;
+    if (!RLK_CHECK(p.status, k < nchunks)) return;
     if (k < 0) {  // a ticket counter left dirty (the workspace was not zeroed): flag and stop
         if (tid == 0) gae_raise(p.status, RL_ERR_INVALID_ARG);
         return;

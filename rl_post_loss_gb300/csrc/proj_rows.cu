@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(kThreads) proj_rows_kernel(ProjRowParams p) {
     __shared__ uint32_t s_y;
     const int r = blockIdx.x;
     const int t = p.row0 + r;
+    if (!RLK_CHECK(p.status, r < p.rows)) return;
     const float4 *st_row = p.stats + (size_t)r * p.n_tiles;
 
     RowStats2 st = empty_stats();

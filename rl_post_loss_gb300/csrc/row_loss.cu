@@ -200,6 +200,7 @@ __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twop
     }
     __syncthreads();
     const float g = s_g;
+    if (!RLK_CHECK(p.status, row < p.num_tokens && (g == 0.f || s_y < (uint32_t)V))) return;
     if (g == 0.f) {
         float zero[VEC];
 #pragma unroll

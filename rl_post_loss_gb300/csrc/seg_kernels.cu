@@ -88,8 +88,12 @@ __global__ void __launch_bounds__(kTokenThreads) token_prep_kernel(TokenPrepPara
     const int i_row = blockIdx.x * kTokenThreads + threadIdx.x;
     if (i_row >= p.rows) return;
     const int t = p.row0 + i_row;
+    if (!RLK_CHECK(p.status, t < p.num_tokens)) return;
     const int i = find_seq(p.cu_seqlens, p.num_seqs, t);
     if (i < 0) raise_status(p.status, RL_ERR_SEQLENS);
+    if (!RLK_CHECK(p.status, i < 0 || (i < p.num_seqs && __ldg(p.cu_seqlens + i) <= t &&
+                                        t < __ldg(p.cu_seqlens + i + 1))))
+        return;
     const float A = p.token_adv ? __ldg(p.token_adv + t) : (i >= 0 ? p.seq_adv[i] : 0.f);
     const float w = i >= 0 ? p.seq_w[i] : 0.f;
     const int y = __ldg(p.targets + t);
