@@ -47,6 +47,9 @@ def parse_args():
                          "every input first, then the device call")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-also", action="store_true",
+                    help="the default loss line leaves out its `also` object (short runs of the fused projection, "
+                         "GAE and top-k)")
     ap.add_argument("--prompts", type=int, default=0,
                     help="use only the first P prompts' responses (small profiling runs); 0 = the whole case")
     ap.add_argument("--max-len", type=int, default=0, help="cap every response length (small profiling runs)")
@@ -56,6 +59,38 @@ def parse_args():
                     help="loss cases 0-3: capture one step in a CUDA graph and time its replays (the per-kernel "
                          "profile is then not taken; the roofline uses the whole step)")
     return ap.parse_args()
+
+
+def emit(line: dict, args) -> None:
+    """Print the bench line, or hand it to the caller that runs this workload as a secondary one."""
+    sink = getattr(args, "collect", None)
+    if sink is not None:
+        sink.append(line)
+    else:
+        print(json.dumps(line), flush=True)
+
+
+def secondary_lines(args) -> dict:
+    """Short runs of the other workloads on the hot path (the fused projection, GAE and top-k), for the
+    `also` object of the default line: each one's time, rate, roofline fraction and clocks."""
+    import copy
+    import torch
+    runs = {"case4_fused_projection": ("4", 3, 2), "gae": ("gae", 50, 3), "topk": ("topk", 20, 3)}
+    also = {}
+    for name, (case, steps, warmup) in runs.items():
+        a = copy.copy(args)
+        a.case, a.steps, a.warmup, a.e2e_steps, a.no_cpu_baseline, a.collect = case, steps, warmup, 1, True, []
+        a.prompts = a.max_len = a.vocab = a.rows = 0
+        {"4": main_projection, "gae": main_gae, "topk": main_topk}[case](a)
+        torch.cuda.empty_cache()
+        if not a.collect:
+            continue
+        ln = a.collect[0]
+        keep = {k: ln[k] for k in ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "roofline", "clocks",
+                                   "step_tensor", "roofline_forward", "gpu_launches", "device_status") if k in ln}
+        keep["workload"] = ln["config"]["workload"]
+        also[name] = keep
+    return also
 
 
 def dist_env():
@@ -451,6 +486,12 @@ def main():
                                  if args.e2e_chunks > 0 else "copies, then rl_loss_forward_backward")},
                 "gpu_launches": launches, "device_status": capi.status_bits_to_names(bits),
                 "cpu_baseline": cpu}
+    if world == 1 and not args.no_also and not args.graph and not (args.prompts or args.max_len or args.vocab):
+        # the other workloads of the hot path, measured in the same run (after this workload's buffers go)
+        del batch, out, host, dev_in, rl
+        torch.cuda.empty_cache()
+        line["also"] = secondary_lines(args)
+    if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -604,7 +645,7 @@ def main_projection(args):
                 "e2e": {"value": replica_throughput(T, 1, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": 8, "ms_per_step": e2e_ms},
                 "gpu_launches": launches, "device_status": capi.status_bits_to_names(bits), "cpu_baseline": cpu}
-        print(json.dumps(line), flush=True)
+        emit(line, args)
     if world > 1:
         dist.destroy_process_group()
     return 0
@@ -730,7 +771,7 @@ def main_gae(args):
                         "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
                         "d2h_bytes_per_step": T * 4, "ms_per_step": e2e_ms},
                 "gpu_launches": args.steps, "cpu_baseline": cpu}
-        print(json.dumps(line), flush=True)
+        emit(line, args)
     return 0
 
 
@@ -841,7 +882,7 @@ def main_topk(args):
                         "h2d_bytes_per_step": host.numel() * 4, "d2h_bytes_per_step": b.rows * b.k * 4,
                         "ms_per_step": e2e_ms},
                 "gpu_launches": args.steps, "cpu_baseline": cpu}
-        print(json.dumps(line), flush=True)
+        emit(line, args)
     return 0
 
 
