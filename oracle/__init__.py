@@ -270,12 +270,14 @@ def projection_forward_stats(hidden_bits, w_bits, batch: dict, p: LossParams, ro
     return out
 
 
-def projection_dw_rows(vocab_ids, h: np.ndarray, W: np.ndarray, targets, logp, g) -> np.ndarray:
+def projection_dw_rows(vocab_ids, h: np.ndarray, W: np.ndarray, targets, logp, g, magnitudes: bool = False):
     """Rows ``vocab_ids`` of dL/dW = (dL/dz)^T h for the fused path, from the
     per-token log-probs and dL/dlogp of the forward (``logp``, ``g``) on float64
     h [T, H] and W [V, H]: dL/dz_{t,v} = g_t (1[v = y_t] - exp(z_{t,v} - logZ_t))
     with logZ_t = z_{t,y_t} - logp_t (the chain rule through Eq. (1)'s log-prob,
-    section 3.2). Rows with g_t = 0 contribute nothing."""
+    section 3.2). Rows with g_t = 0 contribute nothing. With ``magnitudes`` also
+    |dL/dz|^T |h| and sqrt((dL/dz)^2^T h^2), the sizes of the product's terms
+    (for error bounds)."""
     ids = np.asarray(vocab_ids, np.int64)
     g = np.asarray(g, np.float64)
     live = np.nonzero(g != 0.0)[0]
@@ -285,6 +287,8 @@ def projection_dw_rows(vocab_ids, h: np.ndarray, W: np.ndarray, targets, logp, g
     logz = zy - np.asarray(logp, np.float64)[live]
     zv = hl @ W[ids].T
     dz = g[live][:, None] * ((y[:, None] == ids[None, :]).astype(np.float64) - np.exp(zv - logz[:, None]))
+    if magnitudes:
+        return dz.T @ hl, np.abs(dz).T @ np.abs(hl), np.sqrt((dz * dz).T @ (hl * hl))
     return dz.T @ hl
 
 
