@@ -231,16 +231,20 @@ RL_LOSS_API rl_status rl_loss_forward_backward_from_host(rl_loss_t handle, const
  * chunk the output projection z = h W^T, the loss above and their backward run
  * to completion before the next chunk reuses the buffers, so the logits of the
  * whole sequence never exist at once. All three products run on the tensor
- * cores (tcgen05, pairs of CTAs on 256 x 256 tiles, bf16 inputs, fp32
+ * cores (tcgen05, pairs of CTAs on 256 x 512 tiles, bf16 inputs, fp32
  * accumulation in a fixed order): the projection fused with the per-row
- * softmax statistics; dZ is formed once per chunk in bf16; dH = dZ W and
- * dW += dZ^T H share one launch per chunk, dW accumulated in fp32 chunk after
- * chunk in chunk order, so every output repeats bit for bit. */
+ * softmax statistics, its output kept as bf16 scaled probabilities
+ * 2^{z log2e - m} (m a per-row reference of each 64-column block; the target's
+ * logit kept in fp32); dZ is formed once per chunk in bf16 over them, in
+ * place; dH = dZ W and dW += dZ^T H share one launch per chunk, dW
+ * accumulated in fp32 chunk after chunk in chunk order, so every output
+ * repeats bit for bit. */
 
 /* Allocates the fused projection path's buffers for hidden size `hidden_dim`
- * (a multiple of 8) and chunks of `chunk_tokens` rows: a chunk_tokens x V fp32
- * logits buffer, a chunk_tokens x V bf16 dL/dlogits buffer and the per-row
- * statistics. Requires a handle with logits_dtype RL_BF16 (else
+ * (a multiple of 8) and chunks of `chunk_tokens` rows: one chunk_tokens x V
+ * bf16 buffer (the scaled probabilities, then dL/dlogits), the per-row
+ * statistics and block references (32 bytes per row per 256 columns) and the
+ * target logits. Requires a handle with logits_dtype RL_BF16 (else
  * RL_ERR_UNSUPPORTED). Calling it again
  * replaces the buffers. Synchronises the device. */
 RL_LOSS_API rl_status rl_loss_projection_setup(rl_loss_t handle, int32_t hidden_dim, int32_t chunk_tokens);

@@ -232,6 +232,7 @@ struct SeqPrepParams {
 struct TokenPrepParams {
     const void *logits;  // row i holds token row0 + i
     int64_t ld_logits;
+    const float *target_logit;  // [rows] z_y of row i, read instead of the logits (the projection path), else null
     int32_t row0, rows;  // tokens [row0, row0 + rows) are prepared
     int32_t logits_dtype;
     const int32_t *targets;

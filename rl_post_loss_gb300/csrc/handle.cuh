@@ -56,11 +56,12 @@ struct rl_loss_handle_s {
 
     // fused projection path (rl_loss_projection_setup)
     int32_t proj_hidden = 0, proj_chunk = 0, proj_n_tiles = 0;
-    int64_t proj_ldz = 0, proj_lddz = 0;
-    void *proj_ws = nullptr;  // one cudaMalloc: logits chunk, dZ chunk, statistics
-    float *proj_z = nullptr;
-    void *proj_dz = nullptr;
+    int64_t proj_ldp = 0;
+    void *proj_ws = nullptr;  // one cudaMalloc: the bf16 chunk, statistics, block references, target logits
+    void *proj_p = nullptr;   // [chunk x ldp] bf16: scaled probabilities, then dZ in place
     float4 *proj_stats = nullptr;
+    float4 *proj_refs = nullptr;
+    float *proj_zy = nullptr;
 
     bool prof_reset(size_t slots) {
         for (cudaEvent_t e : prof_events) cudaEventDestroy(e);

@@ -37,30 +37,34 @@ struct GemmOperand {
 
 // D [M x N] = A [M x K] B [K x N] (fp32 accumulation over K in a fixed order).
 struct GemmProblem {
-    enum Epi { kZStats = 0, kBf16 = 1, kF32 = 2 };
+    enum Epi { kZStats = 0, kBf16 = 1, kF32 = 2, kProbStats = 3 };
     int M, N, K;
     GemmOperand a, b;
     int epi;         // kZStats: fp32 D (optional) + per-row, per-256-column softmax statistics;
+                     // kProbStats: bf16 scaled probabilities 2^{z log2e - m} in D, the statistics,
+                     //   each 64-column block's reference m and the target logits;
                      // kBf16: D rounded to bf16; kF32: D in fp32
     int accumulate;  // kF32: D += A B instead of D = A B
     int n_fastest;   // tile order of the problem (consecutive tiles of a CTA pair walk N, else M)
     void *d;
     int64_t ldd;     // elements
-    float4 *stats;   // kZStats: [M x ceil(N / 256)]
+    float4 *stats;   // kZStats, kProbStats: [M x ceil(N / 256)]
+    float4 *refs;    // kProbStats: [M x ceil(N / 256)], the references of a tile's four 64-column blocks
+    const int32_t *targets;  // kProbStats: [M] target column per row
+    float *target_logit;     // kProbStats: [M] written for rows whose target is in [0, N)
 };
 
 // One launch over one or two problems. With two, the tiles of the first are
-// strided over the CTA pairs and those of the second are split into
-// contiguous ranges that balance the pairs' k-blocks.
+// strided over the CTA pairs and those of the second follow in strided rounds
+// that the pairs with one more tile of the first join later.
 cudaError_t launch_gemm_problems(const GemmProblem *probs, int nprob, uint32_t *status, cudaStream_t stream);
 
 struct ProjRowParams {
-    const float *z;      // [rows x ldz] fp32 logits of the chunk
-    int64_t ldz;
-    const float4 *stats; // [rows x n_tiles]
+    void *probs;          // [rows x ldp] bf16: in, the scaled probabilities of the chunk; out, dZ (in place)
+    int64_t ldp;
+    const float4 *stats;  // [rows x n_tiles]
+    const float4 *refs;   // [rows x n_tiles]: base-2 reference of each 64-column block
     int32_t n_tiles;
-    void *dz;            // [rows x lddz] bf16 dL/dlogits of the chunk
-    int64_t lddz;
     int32_t row0;        // token index of the chunk's first row
     int32_t rows, vocab;
     const float4 *rec;   // per-token records (indexed by token)

@@ -6,9 +6,13 @@
 // chunk's buffers reused, so logits for the whole sequence never exist.
 //
 // Per chunk c of rows [r0, r0 + m):
-//   proj_gemm   Z_c = H_c W^T (tcgen05, fp32) + per-row, per-256-column softmax statistics
-//   token_prep  per-token records (z_y read from Z_c)
-//   proj_rows   statistics merged per row in tile order, token objective, dZ_c (bf16)
+//   proj_gemm   Z_c = H_c W^T (tcgen05, fp32 accumulators), stored as bf16 scaled
+//               probabilities 2^{z log2e - m} (m a per-row, per-64-column reference),
+//               with per-row, per-256-column softmax statistics and the exact
+//               target logits
+//   token_prep  per-token records (z_y from the target logits)
+//   proj_rows   statistics merged per row in tile order, token objective, dZ_c (bf16,
+//               over the scaled probabilities, in place)
 //   proj_bwd    one tcgen05 launch over both backward products:
 //               dH_c = dZ_c W (bf16 out) and
 //               dW  (+)= dZ_c^T H_c (fp32; stored by chunk 0, added into by the later chunks)
@@ -21,9 +25,10 @@
 void rl_loss_handle_s::proj_release() {
     if (proj_ws) cudaFree(proj_ws);
     proj_ws = nullptr;
-    proj_z = nullptr;
-    proj_dz = nullptr;
+    proj_p = nullptr;
     proj_stats = nullptr;
+    proj_refs = nullptr;
+    proj_zy = nullptr;
     proj_hidden = proj_chunk = proj_n_tiles = 0;
 }
 
@@ -51,25 +56,26 @@ RL_LOSS_API rl_status rl_loss_projection_setup(rl_loss_t h, int32_t hidden_dim, 
     const int64_t V = h->cfg.vocab_size;
     const int tile = rlk::proj_gemm_tile_cols();
     const int n_tiles = (int)((V + tile - 1) / tile);
-    const int64_t ldz = (V + 3) / 4 * 4, lddz = (V + 7) / 8 * 8;
-    const size_t z_bytes = align_up((size_t)chunk_tokens * ldz * 4, 256);
-    const size_t dz_bytes = align_up((size_t)chunk_tokens * lddz * 2, 256);
+    const int64_t ldp = (V + 7) / 8 * 8;
+    const size_t p_bytes = align_up((size_t)chunk_tokens * ldp * 2, 256);
     const size_t st_bytes = align_up((size_t)chunk_tokens * n_tiles * sizeof(float4), 256);
+    const size_t zy_bytes = align_up((size_t)chunk_tokens * sizeof(float), 256);
     void *ws = nullptr;
-    cudaError_t e = cudaMalloc(&ws, z_bytes + dz_bytes + st_bytes);
+    cudaError_t e = cudaMalloc(&ws, p_bytes + 2 * st_bytes + zy_bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return cuda_fail(h, e);
     }
+    char *b = reinterpret_cast<char *>(ws);
     h->proj_ws = ws;
-    h->proj_z = reinterpret_cast<float *>(ws);
-    h->proj_dz = reinterpret_cast<char *>(ws) + z_bytes;
-    h->proj_stats = reinterpret_cast<float4 *>(reinterpret_cast<char *>(ws) + z_bytes + dz_bytes);
+    h->proj_p = b;
+    h->proj_stats = reinterpret_cast<float4 *>(b + p_bytes);
+    h->proj_refs = reinterpret_cast<float4 *>(b + p_bytes + st_bytes);
+    h->proj_zy = reinterpret_cast<float *>(b + p_bytes + 2 * st_bytes);
     h->proj_hidden = hidden_dim;
     h->proj_chunk = chunk_tokens;
     h->proj_n_tiles = n_tiles;
-    h->proj_ldz = ldz;
-    h->proj_lddz = lddz;
+    h->proj_ldp = ldp;
     return RL_OK;
 }
 
@@ -154,22 +160,27 @@ RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(
         const int m = T - r0 < h->proj_chunk ? T - r0 : h->proj_chunk;
         const char *hc = reinterpret_cast<const char *>(hidden) + (size_t)r0 * ld_hidden * 2;
 
-        rlk::ProjGemmParams gp{};
-        gp.M = m;
-        gp.N = V;
-        gp.K = H;
-        gp.z = h->proj_z;
-        gp.ldz = h->proj_ldz;
-        gp.stats = h->proj_stats;
-        gp.status = h->status;
+        rlk::GemmProblem fw{};
+        fw.M = m;
+        fw.N = V;
+        fw.K = H;
+        fw.a = rlk::GemmOperand{hc, ld_hidden, 0};
+        fw.b = rlk::GemmOperand{w_lm, ld_w, 0};
+        fw.epi = rlk::GemmProblem::kProbStats;
+        fw.n_fastest = 0;  // pairs running at once share the LM-head tiles through L2
+        fw.d = h->proj_p;
+        fw.ldd = h->proj_ldp;
+        fw.stats = h->proj_stats;
+        fw.refs = h->proj_refs;
+        fw.targets = in->targets + r0;
+        fw.target_logit = h->proj_zy;
         slot = h->prof_begin(kProjGemm, stream);
-        e = rlk::launch_proj_gemm(hc, ld_hidden, w_lm, ld_w, gp, stream);
+        e = rlk::launch_gemm_problems(&fw, 1, h->status, stream);
         h->prof_end(slot, stream);
         if (e != cudaSuccess) return cuda_fail(h, e);
 
         rlk::TokenPrepParams tp{};
-        tp.logits = h->proj_z;
-        tp.ld_logits = h->proj_ldz;
+        tp.target_logit = h->proj_zy;
         tp.row0 = r0;
         tp.rows = m;
         tp.logits_dtype = RL_F32;
@@ -194,12 +205,11 @@ RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(
         if (e != cudaSuccess) return cuda_fail(h, e);
 
         rlk::ProjRowParams rp{};
-        rp.z = h->proj_z;
-        rp.ldz = h->proj_ldz;
+        rp.probs = h->proj_p;
+        rp.ldp = h->proj_ldp;
         rp.stats = h->proj_stats;
+        rp.refs = h->proj_refs;
         rp.n_tiles = h->proj_n_tiles;
-        rp.dz = h->proj_dz;
-        rp.lddz = h->proj_lddz;
         rp.row0 = r0;
         rp.rows = m;
         rp.vocab = V;
@@ -224,7 +234,7 @@ RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(
         bw[0].M = m;
         bw[0].N = H;
         bw[0].K = V;
-        bw[0].a = rlk::GemmOperand{h->proj_dz, h->proj_lddz, 0};
+        bw[0].a = rlk::GemmOperand{h->proj_p, h->proj_ldp, 0};
         bw[0].b = rlk::GemmOperand{w_lm, ld_w, 1};
         bw[0].epi = rlk::GemmProblem::kBf16;
         bw[0].n_fastest = 0;  // pairs running at once share W's column blocks through L2
@@ -233,7 +243,7 @@ RL_LOSS_API rl_status rl_loss_fused_projection_forward_backward(
         bw[1].M = V;
         bw[1].N = H;
         bw[1].K = m;
-        bw[1].a = rlk::GemmOperand{h->proj_dz, h->proj_lddz, 1};
+        bw[1].a = rlk::GemmOperand{h->proj_p, h->proj_ldp, 1};
         bw[1].b = rlk::GemmOperand{hc, ld_hidden, 1};
         bw[1].epi = rlk::GemmProblem::kF32;
         bw[1].accumulate = ci > 0;

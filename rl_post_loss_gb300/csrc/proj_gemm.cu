@@ -88,19 +88,22 @@ struct Cfg {
     static constexpr uint32_t total = tmem_off + 16;
 };
 
-enum { kEpiStats = 0, kEpiBf16 = 1, kEpiF32 = 2 };
+enum { kEpiStats = 0, kEpiBf16 = 1, kEpiF32 = 2, kEpiProbs = 3 };
 
 struct TcProblem {
     int M, N, K;
     int a_mn, b_mn;     // operand stored MN-major (else K-major)
-    int epi;            // kEpiStats / kEpiBf16 / kEpiF32
+    int epi;            // kEpiStats / kEpiBf16 / kEpiF32 / kEpiProbs
     int accumulate;     // kEpiF32: D += A B (else D = A B)
     int n_fastest;      // tile order: consecutive tiles walk N (else M)
     int tiles_m, tiles_n, k_blocks;  // tiles_n counts 256-column tiles
     int tiles_np, tiles;             // pair tiles: tiles_m x tiles_np, each kTileM x (NH x kTileN)
     void *d;            // output, row stride ldd elements (fp32 or bf16 by epi)
     int64_t ldd;
-    float4 *stats;      // kEpiStats: [M x tiles_n] partial row statistics (optional)
+    float4 *stats;      // kEpiStats, kEpiProbs: [M x tiles_n] partial row statistics (optional for kEpiStats)
+    float4 *refs;       // kEpiProbs: [M x tiles_n] base-2 reference of each 64-column block
+    const int32_t *targets;  // kEpiProbs: [M] target column of each row (any value: only in-range ones are kept)
+    float *target_logit;     // kEpiProbs: [M] the target's logit, fp32, for rows whose target is in [0, N)
 };
 
 struct TcParams {
@@ -261,6 +264,85 @@ __device__ __forceinline__ void epi_stats(const TcProblem &q, const void *dmap, 
         }
     }
     if (q.stats && row < q.M) q.stats[(size_t)row * q.tiles_n + nt] = make_float4(st.m2, st.s, st.u2, 0.f);
+}
+
+// Scaled probabilities + per-row softmax statistics of the 256 columns at n0
+// (the fused loss path). Each 64-column block is stored in bf16 as
+// e_v = 2^{z_v log2e - m}, m the row's running base-2 maximum after the block,
+// and m is kept per block in `refs`: every stored value is in [0, 1] and keeps
+// bf16's relative precision whatever its size, so p_v = e_v 2^{m - logZ2}
+// once the row's logZ is known. The target's own logit is kept exactly
+// (fp32) for the log-probability.
+__device__ __forceinline__ void epi_probs(const TcProblem &q, const void *dmap, EpiStage &es, int lane,
+                                          uint32_t tbase, int row, int wrow0, int n0, int nt, int y) {
+    RowStats2 st = empty_stats();
+    float4 ref = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+#pragma unroll 1
+    for (int c = 0; c < kTileN / 64; ++c) {
+        uint32_t r[2][32];
+        ptx::tmem_ld_32x32b_x32(tbase + c * 64, r[0]);
+        ptx::tmem_ld_32x32b_x32(tbase + c * 64 + 32, r[1]);
+        ptx::tmem_ld_wait();
+        const int col0 = n0 + c * 64;
+        const int nvalid = min(64, q.N - col0);
+        if (nvalid <= 0) break;
+        float mv = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+            if (j < nvalid) mv = fmaxf(mv, __uint_as_float(r[j >> 5][j & 31]));
+        const float mv2 = mv * kLog2e;
+        if (mv2 > st.m2) {
+            if (st.m2 != -INFINITY) {
+                const float dm = st.m2 - mv2;
+                const float f = ex2_approx(dm);
+                st.u2 = f * fmaf(dm, st.s, st.u2);
+                st.s = f * st.s;
+            }
+            st.m2 = mv2;
+        }
+        float e[64];
+        if (st.m2 == -INFINITY) {  // every value so far is -inf (probability 0) or NaN (must show)
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const float x = __uint_as_float(r[j >> 5][j & 31]);
+                const bool nan = j < nvalid && !(x == x);
+                if (nan) st.s = x;
+                e[j] = nan ? x : 0.f;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const float d2 = fmaf(__uint_as_float(r[j >> 5][j & 31]), kLog2e, -st.m2);
+                const float ej = ex2_approx(d2);
+                if (j < nvalid) {  // a -inf logit adds nothing (0 log 0 = 0): see the row kernel
+                    st.s += ej;
+                    st.u2 = fmaf(ej, fmaxf(d2, -256.f), st.u2);
+                }
+                e[j] = j < nvalid ? ej : 0.f;
+            }
+        }
+        if ((unsigned)(y - col0) < (unsigned)nvalid) {  // this row's target: its logit exactly
+            float zy = 0.f;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) zy = (j == y - col0) ? __uint_as_float(r[j >> 5][j & 31]) : zy;
+            q.target_logit[row] = zy;
+        }
+        ref.x = c == 0 ? st.m2 : ref.x;
+        ref.y = c == 1 ? st.m2 : ref.y;
+        ref.z = c == 2 ? st.m2 : ref.z;
+        ref.w = c == 3 ? st.m2 : ref.w;
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(e[2 * j], e[2 * j + 1]);
+        const uint32_t buf = stage_acquire(es, lane);
+        stage_row(buf, lane, pk);
+        stage_issue(es, lane, dmap, col0, wrow0, buf, false);
+    }
+    if (row < q.M) {
+        const size_t i = (size_t)row * q.tiles_n + nt;
+        q.stats[i] = make_float4(st.m2, st.s, st.u2, 0.f);
+        q.refs[i] = ref;
+    }
 }
 
 // bf16 output of the 256 columns at n0, 64 columns per staged block.
@@ -451,6 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int wrow0 = m0 + (int)rank * kRowsCta + qd * 32;  // this warp's first row
             const int row = wrow0 + lane;
             const uint32_t acc = (uint32_t)i % C::NACC, aph = ((uint32_t)i / C::NACC) & 1u;
+            const int y = (q.epi == kEpiProbs && row < q.M) ? __ldg(q.targets + row) : -1;
             if (!timed_out && !ptx::mbar_wait(accf0 + 8 * acc, aph)) timed_out = true;
             ptx::tc_fence_after();
 #pragma unroll 1
@@ -459,6 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t tbase = tmem_base + ((uint32_t)(qd * 32) << 16) + (acc * NH + h) * kTileN;
                 if (n0h >= q.N || wrow0 >= q.M) {
                     // past the last column (an odd count of 256-column tiles) or below the last row
+                } else if (q.epi == kEpiProbs) {
+                    epi_probs(q, dmap, es, lane, tbase, row, wrow0, n0h, nt + h, y);
                 } else if (q.epi == kEpiStats) {
                     epi_stats(q, dmap, es, lane, tbase, row, wrow0, n0h, nt + h);
                 } else if (q.epi == kEpiBf16) {
@@ -578,8 +663,10 @@ cudaError_t launch(const GemmProblem *probs, int nprob, uint32_t *status, cudaSt
         if (!operand_map(&maps.a[i], g.a, g.M, g.K, kRowsCta) || !operand_map(&maps.b[i], g.b, g.N, g.K, kBnCta))
             return cudaErrorInvalidValue;
         if (!g.d && g.epi != GemmProblem::kZStats) return cudaErrorInvalidValue;
+        if (g.epi == GemmProblem::kProbStats && (!g.stats || !g.refs || !g.targets || !g.target_logit))
+            return cudaErrorInvalidValue;
         if (g.d) {  // the output, written in staged 32-row blocks of 128 bytes per row
-            const bool f32 = g.epi != GemmProblem::kBf16;
+            const bool f32 = g.epi == GemmProblem::kZStats || g.epi == GemmProblem::kF32;
             const uint32_t es = f32 ? 4 : 2;
             if (!aligned16(g.d) || g.ldd < g.N || (g.ldd * es) % 16 != 0 ||
                 !make_tmap(&maps.d[i], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, es,
@@ -592,7 +679,10 @@ cudaError_t launch(const GemmProblem *probs, int nprob, uint32_t *status, cudaSt
         q.K = g.K;
         q.a_mn = g.a.mn_major;
         q.b_mn = g.b.mn_major;
-        q.epi = g.epi == GemmProblem::kZStats ? kEpiStats : (g.epi == GemmProblem::kBf16 ? kEpiBf16 : kEpiF32);
+        q.epi = g.epi == GemmProblem::kZStats      ? kEpiStats
+                : g.epi == GemmProblem::kProbStats ? kEpiProbs
+                : g.epi == GemmProblem::kBf16      ? kEpiBf16
+                                                   : kEpiF32;
         q.accumulate = g.accumulate;
         q.n_fastest = g.n_fastest;
         q.tiles_m = (g.M + kTileM - 1) / kTileM;
@@ -603,6 +693,9 @@ cudaError_t launch(const GemmProblem *probs, int nprob, uint32_t *status, cudaSt
         q.d = g.d;
         q.ldd = g.ldd;
         q.stats = g.stats;
+        q.refs = g.refs;
+        q.targets = g.targets;
+        q.target_logit = g.target_logit;
     }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

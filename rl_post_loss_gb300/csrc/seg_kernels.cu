@@ -104,7 +104,9 @@ __global__ void __launch_bounds__(kTokenThreads) token_prep_kernel(TokenPrepPara
     const float d = __fsub_rn(lo, __ldg(p.logp_infer + t));  // ln rho, one fp32 subtraction
     const bool in_bounds = (-p.c.ln_beta <= d) && (d <= p.c.ln_beta);
     float zy = 0.f;
-    if (ok) {
+    if (ok && p.target_logit) {
+        zy = __ldg(p.target_logit + i_row);
+    } else if (ok) {
         const size_t off = (size_t)i_row * (size_t)p.ld_logits + (size_t)y;
         if (p.logits_dtype == RL_F32) {
             zy = __ldg(reinterpret_cast<const float *>(p.logits) + off);
