@@ -628,8 +628,8 @@ def main_projection(args):
                 "config": {"workload": f"case 4: {c['name']}", "tokens": T, "responses": b.num_seqs,
                            "group": b.group, "vocab": V, "hidden": H, "chunk_tokens": pb.chunk,
                            "mask1_tokens": int(b.mask.sum().item()), "parallelism": "replicas",
-                           "l2": "no flush: each step streams W (1.9 GB) once per chunk and writes 3.7 GB of fp32 "
-                                 "logits per chunk, far larger than the 129 MB L2"},
+                           "l2": "no flush: each step streams W (1.9 GB) once per chunk and writes a 1.24-GB bf16 "
+                                 "chunk twice per chunk, far larger than the 129 MB L2"},
                 "roofline": {"bound": "tensor", "kernel": "proj_bwd", "achieved": bwd_achieved, "peak": peak,
                              "peak_kind": f"{peak_kind} sustained cuBLAS bf16 TFLOP/s", "unit": "TFLOP/s",
                              "frac": bwd_achieved / peak, "traffic": kernel_traffic("proj_bwd", 4),
