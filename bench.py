@@ -113,10 +113,10 @@ def measured_peaks(key: str = "hbm_gbs"):
 
 # the source files each profiled kernel is compiled from
 KERNEL_SOURCES = {
-    "row_loss": ["row_loss.cu", "common.cuh"],
-    "proj_gemm": ["proj_gemm.cu", "proj.cuh", "ptx.cuh", "common.cuh"],
-    "proj_bwd": ["proj_gemm.cu", "proj.cuh", "ptx.cuh", "common.cuh"],
-    "gae": ["gae.cu", "scan_select.cuh", "common.cuh"],
+    "row_loss": ["row_loss.cu", "ptx.cuh", "common.cuh"],
+    "proj_gemm": ["proj_gemm.cu", "proj.cuh", "ptx.cuh", "tmap.cuh", "common.cuh"],
+    "proj_bwd": ["proj_gemm.cu", "proj.cuh", "ptx.cuh", "tmap.cuh", "common.cuh"],
+    "gae": ["gae.cu", "scan_select.cuh", "ptx.cuh", "tmap.cuh", "common.cuh"],
     "topk": ["topk.cu", "scan_select.cuh", "ptx.cuh", "common.cuh"],
 }
 

@@ -19,9 +19,12 @@
 // and a response end resets the state to zero; with the cross-trajectory
 // discount two integer counts ride along (mask=1 tokens to the right within
 // the response and within the rollout), whose difference is N_{>s}. Such maps
-// compose associatively. A block stages its chunk in shared memory with
-// coalesced 16-byte asynchronous copies, folds 32 tokens per thread into a map
-// (fp32), scans the 256 maps with a fixed tree and publishes the chunk's map.
+// compose associatively. A block stages its chunk in shared memory (two
+// tensor copies of the rewards and values as [256 x 32] tiles with the
+// 128-byte swizzle and one bulk copy of the mask bytes, issued by one thread;
+// coalesced 16-byte asynchronous copies for a partial chunk or unaligned
+// arrays), folds 32 tokens per thread into a map (fp32), scans the 256 maps
+// with a fixed tree and publishes the chunk's map.
 // Warp 0 then looks back: it composes the published maps of the chunks to its
 // right, in a fixed order and tree, up to and including the first one that
 // holds a response end (the state further right cannot reach it); the rollout
@@ -30,13 +33,19 @@
 // to those stopping points. Every floating-point result depends only on the
 // inputs, never on timing: bit-identical from run to run. Waits are bounded
 // (1 s of %globaltimer by default); one that runs out raises RL_ERR_TIMEOUT
-// and treats the chunk as a response end. The last block past its look-back clears the
-// flags and the ticket (records are only read under a flag set by the same
-// launch), so the workspace is ready for the next launch.
+// and treats the chunk as a response end. The advantages are written in place
+// of the staged rewards and leave by tensor stores (one thread) when the whole
+// chunk lies inside the covered range. The last block past its look-back
+// clears the flags and the ticket (records are only read under a flag set by
+// the same launch), so the workspace is ready for the next launch.
+#include <cuda.h>
+
 #include <atomic>
 
 #include "common.cuh"
+#include "ptx.cuh"
 #include "scan_select.cuh"
+#include "tmap.cuh"
 
 namespace rlk {
 
@@ -80,6 +89,27 @@ struct ChunkRecord {
 };
 static_assert(sizeof(ChunkRecord) == 48, "record size");
 constexpr int kWsHeader = 256;
+
+// Tensor maps of the token arrays viewed as [T / 32 rows x 32 floats] (one 128-byte row per
+// thread's 32 tokens), boxes of 256 rows (a chunk) with the 128-byte swizzle: the same XOR layout
+// as tile_off, so the fold and the re-walk read the staged rows unchanged.
+struct GaeMaps {
+    CUtensorMap r, v, adv, ret;
+    int32_t ok;  // 1: the maps are valid (every array 16-byte aligned, T >= one chunk)
+};
+
+struct GaeSmall {
+    uint64_t bar;
+    uint32_t last[kThreads];  // bit i of word w: token 32 w + i is the last of its response
+    uint32_t cont[kThreads];  // ... and its rollout continues into the next response
+    GaeMap wtot[kThreads / 32];
+    GaeMap after[kThreads / 32];
+    int k, sa, sb, lo, hi;
+    float EA, EV;
+    int EP, ER;
+    float pw[kTok + 1], qpw[kTok + 1];  // gl^k and gamma gl^(k-1), by repeated products
+};
+constexpr int kSmemTotal = kSmemBytes + (int)sizeof(GaeSmall);
 
 struct WsHeader {
     uint32_t ticket, done;
@@ -262,19 +292,23 @@ __device__ __noinline__ Scale cross_scale(int n, ScaleArgs p) {
 __device__ __forceinline__ float apply_scale(float a, const Scale &s) { return ((a * s.m) * s.s1) * s.s2 * s.s3; }
 
 template <bool kCross>
-__global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p) {
-    extern __shared__ __align__(16) unsigned char smem[];
+__global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p, const __grid_constant__ GaeMaps maps) {
+    // All shared memory is dynamic, carved below: the staged rows first (1024-byte aligned for the
+    // tensor copies' swizzle when the block's window allows it), then the small per-block state.
+    extern __shared__ __align__(1024) unsigned char smem[];
     float *s_r = reinterpret_cast<float *>(smem + kSmemR);
     float *s_v = reinterpret_cast<float *>(smem + kSmemV);
     uint8_t *s_m = smem + kSmemM;
-    __shared__ uint32_t s_last[kThreads];  // bit i of word w: token 32 w + i is the last of its response
-    __shared__ uint32_t s_cont[kThreads];  // ... and its rollout continues into the next response
-    __shared__ GaeMap s_wtot[kThreads / 32];
-    __shared__ GaeMap s_after[kThreads / 32];
-    __shared__ int s_k, s_sa, s_sb, s_lo, s_hi;
-    __shared__ float s_EA, s_EV;
-    __shared__ int s_EP, s_ER;
-    __shared__ float s_pow[kTok + 1], s_qpow[kTok + 1];  // gl^k and gamma gl^(k-1), by repeated products
+    GaeSmall &sm = *reinterpret_cast<GaeSmall *>(smem + kSmemBytes);
+    uint32_t *s_last = sm.last;
+    uint32_t *s_cont = sm.cont;
+    GaeMap *s_wtot = sm.wtot;
+    GaeMap *s_after = sm.after;
+    int &s_k = sm.k, &s_sa = sm.sa, &s_sb = sm.sb, &s_lo = sm.lo, &s_hi = sm.hi;
+    float &s_EA = sm.EA, &s_EV = sm.EV;
+    int &s_EP = sm.EP, &s_ER = sm.ER;
+    float *s_pow = sm.pw, *s_qpow = sm.qpw;
+    uint64_t &s_bar = sm.bar;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = p.num_tokens, S = p.num_seqs;
@@ -308,9 +342,21 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p) {
     }
     const int cs = k * kChunk, ce = min(T, cs + kChunk);
     const int t0 = cs + tid * kTok;
+    const bool tma = maps.ok && ce - cs == kChunk && (ptx::smem_u32(smem) & 1023u) == 0u;
+    const uint32_t bar = ptx::smem_u32(&s_bar);
 
-    // stage the chunk: coalesced 16-byte copies straight into shared memory
-    if (p.vec && ce - cs == kChunk) {
+    // stage the chunk: tensor copies (128-byte swizzle) and one bulk copy of the mask bytes,
+    // issued by one thread; else coalesced 16-byte copies
+    if (tma) {
+        if (tid == 0) {
+            ptx::mbar_init(bar, 1);
+            ptx::fence_mbar_init();
+            ptx::mbar_arrive_expect_tx(bar, 2u * kChunk * 4u + kChunk);
+            ptx::tma_load_2d(ptx::smem_u32(s_r), &maps.r, 0, k * kThreads, bar);
+            ptx::tma_load_2d(ptx::smem_u32(s_v), &maps.v, 0, k * kThreads, bar);
+            ptx::bulk_g2s(ptx::smem_u32(s_m), p.mask + cs, kChunk, bar);
+        }
+    } else if (p.vec && ce - cs == kChunk) {
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
             const int f = j * kThreads + tid;  // float4 index within the chunk
@@ -379,7 +425,16 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p) {
             }
         }
     }
-    cp_async_wait_all();
+    if (tma) {
+        // bounded: on a timeout the chunk's values are not valid (flagged), and the copies get one
+        // more bounded wait so that none is in flight when the block exits
+        if (!ptx::mbar_wait(bar, 0u)) {
+            gae_raise(p.status, RL_ERR_TIMEOUT);
+            if (tid == 0) ptx::mbar_wait(bar, 0u, 100000000ull);
+        }
+    } else {
+        cp_async_wait_all();
+    }
     __syncthreads();
 
     const uint32_t last = s_last[tid];
@@ -634,9 +689,21 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p) {
         }
     }
 
-    // store: coalesced 16-byte stores of the rows inside [lo, hi), token by token elsewhere
-    __syncthreads();
+    // store: tensor stores of a chunk that lies inside [lo, hi), issued by one thread; else
+    // coalesced 16-byte stores of the rows inside [lo, hi), token by token elsewhere
     const int a_in = min(max(s_lo - cs, 0), kChunk), b_in = min(max(min(s_hi, ce) - cs, 0), kChunk);
+    if (tma && a_in == 0 && b_in == kChunk) {
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            ptx::tma_store_2d(&maps.adv, 0, k * kThreads, ptx::smem_u32(s_r));
+            if (want_ret) ptx::tma_store_2d(&maps.ret, 0, k * kThreads, ptx::smem_u32(s_v));
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_read<0>();  // shared memory is read before the block exits
+        }
+        return;
+    }
+    __syncthreads();
     if (p.vec) {
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
@@ -667,6 +734,11 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p) {
     }
 }
 
+// [rows x 32] fp32 view of a token array, boxes of kThreads rows, 128-byte swizzle.
+bool token_map(CUtensorMap *m, const float *base, int64_t rows) {
+    return make_tmap_sw128(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, rows, kTok, kTok, kTok, kThreads);
+}
+
 template <bool kCross>
 cudaError_t launch_chunks(const GaeParams &p, unsigned nchunks, cudaStream_t stream) {
     static std::atomic<uint64_t> configured{0};  // one bit per device
@@ -675,11 +747,19 @@ cudaError_t launch_chunks(const GaeParams &p, unsigned nchunks, cudaStream_t str
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(gae_chunk_kernel<kCross>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(gae_chunk_kernel<kCross>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemTotal);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    gae_chunk_kernel<kCross><<<nchunks, kThreads, kSmemBytes, stream>>>(p);
+    GaeMaps maps{};
+    const int64_t rows = p.num_tokens / kTok;
+    if (p.vec && rows >= kThreads) {
+        maps.ok = token_map(&maps.r, p.rewards, rows) && token_map(&maps.v, p.values, rows) &&
+                  token_map(&maps.adv, p.adv, rows) && (!p.returns || token_map(&maps.ret, p.returns, rows));
+        if (!p.returns) maps.ret = maps.adv;
+    }
+    gae_chunk_kernel<kCross><<<nchunks, kThreads, kSmemTotal, stream>>>(p, maps);
     return cudaGetLastError();
 }
 
@@ -702,3 +782,4 @@ cudaError_t launch_gae(GaeParams p, cudaStream_t stream) {
 }
 
 }  // namespace rlk
+

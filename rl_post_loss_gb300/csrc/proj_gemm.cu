@@ -50,6 +50,7 @@
 #include "common.cuh"
 #include "proj.cuh"
 #include "ptx.cuh"
+#include "tmap.cuh"
 
 namespace rlk {
 
@@ -574,44 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static std::once_flag once;
-    static EncodeTiledFn fn = nullptr;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-        cudaGetLastError();
-    });
-    return fn;
-}
-
-// 2-D tensor map over a row-major [rows x cols] matrix with row stride `ld`
-// elements: boxes of box_rows x box_cols with the 128-byte swizzle (box_cols
-// x element size = 128 bytes). Out-of-range parts of a box read as zero and
-// are not written.
-bool make_tmap(CUtensorMap *m, CUtensorMapDataType type, uint32_t esize, const void *base, int64_t rows,
-               int64_t cols, int64_t ld, uint32_t box_cols, uint32_t box_rows) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)ld * esize};
-    const cuuint32_t box[2] = {box_cols, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, type, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool make_tmap_bf16(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows) {
-    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rows, cols, ld, BK, box_rows);
+    return make_tmap_sw128(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rows, cols, ld, BK, box_rows);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -669,7 +634,7 @@ cudaError_t launch(const GemmProblem *probs, int nprob, uint32_t *status, cudaSt
             const bool f32 = g.epi == GemmProblem::kZStats || g.epi == GemmProblem::kF32;
             const uint32_t es = f32 ? 4 : 2;
             if (!aligned16(g.d) || g.ldd < g.N || (g.ldd * es) % 16 != 0 ||
-                !make_tmap(&maps.d[i], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, es,
+                !make_tmap_sw128(&maps.d[i], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, es,
                            g.d, g.M, g.N, g.ldd, 128 / es, 32))
                 return cudaErrorInvalidValue;
         }

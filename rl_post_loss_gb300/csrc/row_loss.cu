@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace rlk {
 
@@ -24,12 +25,14 @@ namespace {
 // Rows of at most this many bytes use 256-thread blocks (eight rows per SM, eight
 // 16-byte loads in flight per thread). Longer rows use 1024-thread blocks (two
 // per SM) and keep their first kStageBytes in shared memory from the first pass
-// to the second, which shrinks what must stay in L2. Every row reads its second
-// pass with an L1 evict-first hint, streams its dlogits out with evict-first
-// stores (so they do not push rows still waiting for their second read out of
-// L2), and walks each thread's groups in reverse in the second pass (most
-// recently loaded first). Chosen from GB300 sweeps over 128/256/512/1024
-// threads, staging sizes, unrolling and the cache hints.
+// to the second, which shrinks what must stay in L2: one thread issues bulk
+// copies of that prefix into shared memory as the block starts, the threads
+// fold the rest of the row meanwhile and then the prefix. Every row reads its
+// second pass with an L1 evict-first hint, streams its dlogits out with
+// evict-first stores (so they do not push rows still waiting for their second
+// read out of L2), and walks each thread's groups in reverse in the second
+// pass (most recently loaded first). Chosen from GB300 sweeps over
+// 128/256/512/1024 threads, staging sizes, unrolling and the cache hints.
 constexpr size_t kShortRowBytes = 128 * 1024;
 constexpr int kStageBytes = 96 * 1024;
 
@@ -139,8 +142,9 @@ __device__ __forceinline__ void accumulate(RowStats2 &st, const float (&x)[N]) {
 // by 2^(-FLT_MAX - M) = 0: bit for bit the same as merging an empty part.
 constexpr RowStats2 kRowStart{-FLT_MAX, 0.f, 0.f};
 
-// kStage: the first stage_vecs 16-byte groups of the row are kept in shared memory between the
-// passes (each thread re-reads only the groups it wrote).
+// kStage: the first stage_vecs 16-byte groups of the row arrive in shared memory by bulk copies
+// and stay there between the passes; the bounded wait for them raises RL_ERR_TIMEOUT if it runs
+// out (the row's results are then not valid).
 template <typename T, int kRowThreads, bool kStage>
 __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twopass_kernel(RowParams p, int stage_vecs) {
     using VT = VecTraits<T>;
@@ -161,21 +165,54 @@ __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twop
     const uint32_t meta = __ldg(p.meta + row);
 
     RowStats2 st = kRowStart;
-#pragma unroll kUnroll
-    for (int k = threadIdx.x; k < nvec; k += kRowThreads) {
-        float x[VEC];
-        if (kStage && k < stage_vecs) {
-            const uint4 raw = __ldcs(reinterpret_cast<const uint4 *>(z + (size_t)k * 16));  // not needed in L2 again
-            s_row[k] = raw;
-            decode16<T>(raw, x);
-        } else {
-            VT::load(z + (size_t)k * 16, x);
+    __shared__ __align__(8) uint64_t s_bar;
+    if (kStage) {
+        // the row's first stage_vecs groups arrive in shared memory by bulk copies while the
+        // threads fold the rest of the row
+        const uint32_t bar = ptx::smem_u32(&s_bar);
+        if (threadIdx.x == 0) {
+            ptx::mbar_init(bar, 1);
+            ptx::fence_mbar_init();
+            const uint32_t bytes = (uint32_t)stage_vecs * 16u;
+            ptx::mbar_arrive_expect_tx(bar, bytes);
+            const uint64_t pol = ptx::l2_evict_first_policy();  // read once: not needed in L2 again
+            for (uint32_t off = 0; off < bytes; off += 16384u)
+                ptx::bulk_g2s_hint(ptx::smem_u32(s_row) + off, z + off, min(16384u, bytes - off), bar, pol);
         }
-        accumulate(st, x);
-    }
-    if (tail0 + (int)threadIdx.x < V) {
-        float x[1] = {VT::load1(z, tail0 + threadIdx.x)};
-        accumulate(st, x);
+        __syncthreads();
+#pragma unroll kUnroll
+        for (int k = stage_vecs + (int)threadIdx.x; k < nvec; k += kRowThreads) {
+            float x[VEC];
+            VT::load(z + (size_t)k * 16, x);
+            accumulate(st, x);
+        }
+        if (tail0 + (int)threadIdx.x < V) {
+            float x[1] = {VT::load1(z, tail0 + threadIdx.x)};
+            accumulate(st, x);
+        }
+        if (!ptx::mbar_wait(bar, 0u)) {
+            // the copies did not land in time: flag it (the row's results are not valid) and give
+            // them one more bounded wait, so that none is still in flight when the block exits
+            raise_status(p.status, RL_ERR_TIMEOUT);
+            if (threadIdx.x == 0) ptx::mbar_wait(bar, 0u, 100000000ull);
+        }
+#pragma unroll kUnroll
+        for (int k = threadIdx.x; k < stage_vecs; k += kRowThreads) {
+            float x[VEC];
+            decode16<T>(s_row[k], x);
+            accumulate(st, x);
+        }
+    } else {
+#pragma unroll kUnroll
+        for (int k = threadIdx.x; k < nvec; k += kRowThreads) {
+            float x[VEC];
+            VT::load(z + (size_t)k * 16, x);
+            accumulate(st, x);
+        }
+        if (tail0 + (int)threadIdx.x < V) {
+            float x[1] = {VT::load1(z, tail0 + threadIdx.x)};
+            accumulate(st, x);
+        }
     }
     st = warp_merge_stats2(st);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -213,21 +250,33 @@ __global__ void __launch_bounds__(kRowThreads, 2048 / kRowThreads) row_loss_twop
     const float c = -g;
     const int y = (int)s_y;  // g != 0 implies a valid target
     // Pass 2 walks this thread's groups in reverse: the ones pass 1 loaded last are the likeliest
-    // to still be in L1 / L2 (and, with staging, the oldest ones are the shared-memory prefix).
+    // to still be in L1 / L2; with staging, the groups past the shared-memory prefix first.
+    const int k0 = kStage ? stage_vecs : (int)threadIdx.x;
     const int k_last = (int)threadIdx.x < nvec ? (int)threadIdx.x + ((nvec - 1 - (int)threadIdx.x) / kRowThreads) * kRowThreads : -1;
 #pragma unroll kUnroll
-    for (int k = k_last; k >= (int)threadIdx.x; k -= kRowThreads) {
+    for (int k = k_last; k >= k0; k -= kRowThreads) {
         float x[VEC];
-        if (kStage && k < stage_vecs)
-            decode16<T>(s_row[k], x);
-        else
-            VT::load_last(z + (size_t)k * 16, x);
+        VT::load_last(z + (size_t)k * 16, x);
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
             const float pr = ex2_approx(fmaf(x[j], kLog2e, nlz2));
             x[j] = (k * VEC + j == y) ? g * (1.f - pr) : c * pr;
         }
         VT::store(dz + (size_t)k * 16, x);
+    }
+    if (kStage) {
+        const int kp_last = (int)threadIdx.x < stage_vecs ? (int)threadIdx.x + ((stage_vecs - 1 - (int)threadIdx.x) / kRowThreads) * kRowThreads : -1;
+#pragma unroll kUnroll
+        for (int k = kp_last; k >= (int)threadIdx.x; k -= kRowThreads) {
+            float x[VEC];
+            decode16<T>(s_row[k], x);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                const float pr = ex2_approx(fmaf(x[j], kLog2e, nlz2));
+                x[j] = (k * VEC + j == y) ? g * (1.f - pr) : c * pr;
+            }
+            VT::store(dz + (size_t)k * 16, x);
+        }
     }
     if (tail0 + (int)threadIdx.x < V) {
         const int v = tail0 + threadIdx.x;
