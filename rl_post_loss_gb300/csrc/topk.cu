@@ -26,9 +26,12 @@
 // (shared-memory atomics) never decides anything: the kept set is defined by
 // the total order and the output order by the sort, so the result is
 // bit-identical from run to run. All counts are integers. The CTAs are
-// persistent (two per SM); thread 0 keeps four 16 KB tiles in flight with bulk
-// copies (TMA) into a shared-memory ring, completing on mbarriers whose waits
-// are bounded, and runs ahead into the next row while this one is finished.
+// persistent (two per SM) and warp-specialised: a producer warp keeps four
+// 16 KB tiles in flight with bulk copies (TMA) into a shared-memory ring and
+// runs ahead into the next row while this one is finished; sixteen filter
+// warps do everything else, synchronising among themselves on a named
+// barrier. Stages are handed over on "full" and "empty" mbarriers whose waits
+// are bounded.
 #include <algorithm>
 #include <climits>
 #include <mutex>
@@ -41,7 +44,8 @@ namespace rlk {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 512;           // filter threads (16 warps); one more warp issues the tile copies
+constexpr int kBlock = kThreads + 32;
 constexpr int kPer = 8;                 // scores per thread per tile (two float4)
 constexpr int kTile = kThreads * kPer;  // 4096
 constexpr int kCap = 5120;              // buffer entries
@@ -74,6 +78,19 @@ struct Candidates {
     uint32_t idx[kCap];
 };
 
+// The filter warps' barriers: named barrier 1 over the kThreads filter threads (the producer warp
+// never takes part).
+__device__ __forceinline__ void fbar() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+__device__ __forceinline__ int fbar_or(int pred) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(pred), "n"(kThreads)
+        : "memory");
+    return r;
+}
+
 struct TopkSmem {
     float ring[kStages][kTile];  // tiles of scores, filled by bulk copies
     union {
@@ -82,14 +99,16 @@ struct TopkSmem {
         uint64_t packed[kCap];      // at the end of a row: the selection by bucket, then sorted (see pack_out)
     };
     uint32_t hist[kBins];
-    unsigned long long full[kStages];  // mbarriers: a tile has landed
+    unsigned long long full[kStages];   // mbarriers: a tile has landed
+    unsigned long long empty[kStages];  // mbarriers: every filter warp is done with the stage
     uint32_t warp_tot[kThreads / 32];
     int warp_base[kThreads / 32];      // where each warp's append of the current tile started (INT_MAX: none)
     int count;      // entries in the buffer
     int keyed;      // leading entries that already hold order keys
     int found_bin;  // result of the last histogram search
     int found_before;
-    int failed;     // a bounded wait ran out
+    int failed;     // a bounded wait ran out (read by several warps: volatile accesses)
+    uint32_t issued;  // tiles the producer warp has issued
     int broken;     // an internal check failed (the row's result is invalid; no access left its array)
 };
 
@@ -123,7 +142,7 @@ __device__ void find_bin(TopkSmem &s, uint32_t target, bool from_top) {
         if (lane >= off) incl += o;
     }
     if (lane == 31) s.warp_tot[warp] = incl;
-    __syncthreads();
+    fbar();
     uint32_t before = 0u;
     for (int w = 0; w < warp; ++w) before += s.warp_tot[w];
     uint32_t run = before + incl - local;
@@ -135,7 +154,7 @@ __device__ void find_bin(TopkSmem &s, uint32_t target, bool from_top) {
         }
         run += h[i];
     }
-    __syncthreads();
+    fbar();
 }
 
 // Turns the raw scores appended since the last compaction into order keys. Block-wide; ends with
@@ -143,9 +162,9 @@ __device__ void find_bin(TopkSmem &s, uint32_t target, bool from_top) {
 __device__ void make_keys(TopkSmem &s) {
     const int cnt = s.count;
     for (int i = s.keyed + (int)threadIdx.x; i < cnt; i += kThreads) s.cb.key[i] = order_key(__uint_as_float(s.cb.key[i]));
-    __syncthreads();
+    fbar();
     if (threadIdx.x == 0) s.keyed = cnt;
-    __syncthreads();
+    fbar();
 }
 
 // The outcome of a radix descent over the first `cnt` buffer keys.
@@ -186,13 +205,13 @@ __device__ Descent radix_descent(TopkSmem &s, const uint32_t *keys, int cnt, int
         s.hist[kThreads / 32 + warp] = kmax;
         s.hist[2 * (kThreads / 32) + warp] = vary;
     }
-    __syncthreads();
+    fbar();
     for (int w = 0; w < kThreads / 32; ++w) {
         kmin = min(kmin, s.hist[w]);
         kmax = max(kmax, s.hist[kThreads / 32 + w]);
         vary |= s.hist[2 * (kThreads / 32) + w];
     }
-    __syncthreads();
+    fbar();
     const int low = vary ? __ffs(vary) - 1 : 32;  // bits below `low` are the same in every key
     const uint32_t diff = kmin ^ kmax;
     // the key prefix fixed so far, and how many buffer entries lie strictly above it
@@ -205,20 +224,20 @@ __device__ Descent radix_descent(TopkSmem &s, const uint32_t *keys, int cnt, int
         const int w = min(11, shift - low);
         const int sh = shift - w;
         for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0u;
-        __syncthreads();
+        fbar();
         for (int i0 = tid & ~31; i0 < cnt; i0 += kThreads) {
             const int i = i0 + (tid & 31);
             const uint32_t k = i < cnt ? keys[i] : 0u;
             const bool in = i < cnt && (shift >= 32 || (k >> shift) == prefix);
             hist_add(s.hist, (k >> sh) & ((1u << w) - 1u), in);
         }
-        __syncthreads();
+        fbar();
         find_bin(s, (uint32_t)(target - above), true);
         if (s.found_bin < 0 && tid == 0) s.broken = 1;
         const uint32_t d = (uint32_t)max(s.found_bin, 0);
         const int before = s.found_before;  // entries in the open range above the chosen digit
         const int in_bin = (int)s.hist[d];
-        __syncthreads();
+        fbar();
         prefix = (shift >= 32 ? 0u : (prefix << w)) | d;
         above += before;
         shift = sh;
@@ -264,7 +283,7 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
                     s.found_bin = 0;
                     s.found_before = -1;  // stays -1 only if the invariant broke
                 }
-                __syncthreads();
+                fbar();
                 for (int i0 = tid & ~31; i0 < cnt; i0 += kThreads) {  // warp-uniform trip count: the ballot
                     const int i = i0 + lane;
                     const bool eq = i < cnt && s.cb.key[i] == key_star;
@@ -277,7 +296,7 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
                         if (slot < kBins) s.hist[slot] = s.cb.idx[i];
                     }
                 }
-                __syncthreads();
+                fbar();
                 const int nt = min(s.found_bin, kBins);
                 if (tid == 0 && nt != ties) s.broken = 1;
                 for (int t = tid; t < nt; t += kThreads) {
@@ -287,7 +306,7 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
                     for (int j = 0; j < nt; ++j) r += s.hist[j] < x ? 1 : 0;
                     if (r == need - 1) s.found_before = (int)x;
                 }
-                __syncthreads();
+                fbar();
                 if (tid == 0 && s.found_before < 0) s.broken = 1;
                 ipre = (uint32_t)max(s.found_before, 0);
                 ishift = 0;  // no radix passes
@@ -296,7 +315,7 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
                 const int w = min(11, ishift);
                 const int sh = ishift - w;
                 for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0u;
-                __syncthreads();
+                fbar();
                 for (int i0 = tid & ~31; i0 < cnt; i0 += kThreads) {
                     const int i = i0 + (tid & 31);
                     const bool eq = i < cnt && s.cb.key[i] == key_star;
@@ -304,13 +323,13 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
                     const bool in = eq && (ishift >= 32 || (ix >> ishift) == ipre);
                     hist_add(s.hist, (ix >> sh) & ((1u << w) - 1u), in);
                 }
-                __syncthreads();
+                fbar();
                 find_bin(s, (uint32_t)(need - ibelow), false);
                 if (s.found_bin < 0 && tid == 0) s.broken = 1;
                 ipre = (ishift >= 32 ? 0u : (ipre << w)) | (uint32_t)max(s.found_bin, 0);
                 ibelow += s.found_before;
                 ishift = sh;
-                __syncthreads();
+                fbar();
             }
             idx_star = ipre;
             kept = target;
@@ -333,9 +352,9 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
             keep = mk[j] > key_star || (mk[j] == key_star && mi[j] <= idx_star);
         keepm |= (uint32_t)(i < cnt && keep) << j;
     }
-    __syncthreads();
+    fbar();
     if (tid == 0) s.count = 0;
-    __syncthreads();
+    fbar();
     int pos = atomicAdd(&s.count, __popc(keepm));
 #pragma unroll
     for (int j = 0; j < kMine; ++j) {
@@ -345,7 +364,7 @@ __device__ uint64_t compact(TopkSmem &s, int target, int limit, bool exact, int 
             ++pos;
         }
     }
-    __syncthreads();
+    fbar();
     if (tid == 0) s.keyed = s.count;
     return resolved ? bound : (uint64_t)key_star + 1u;
 }
@@ -394,7 +413,7 @@ __device__ void bitonic_regs(TopkSmem &s, bool by_score) {
                     }
                     in_regs = false;
                 }
-                __syncthreads();
+                fbar();
                 for (int t = tid; t < n2 / 2; t += kThreads) {
                     const int i = 2 * t - (t & (stride - 1));
                     const int jj = i + stride;
@@ -410,7 +429,7 @@ __device__ void bitonic_regs(TopkSmem &s, bool by_score) {
                 continue;
             }
             if (!in_regs) {
-                __syncthreads();
+                fbar();
 #pragma unroll
                 for (int j = 0; j < E; ++j) {
                     k[j] = s.cb.key[E * tid + j];
@@ -454,7 +473,7 @@ __device__ void bitonic_regs(TopkSmem &s, bool by_score) {
             }
         }
     }
-    if (!in_regs) __syncthreads();
+    if (!in_regs) fbar();
     else {
 #pragma unroll
         for (int j = 0; j < E; ++j) {
@@ -462,7 +481,7 @@ __device__ void bitonic_regs(TopkSmem &s, bool by_score) {
             s.cb.idx[E * tid + j] = ix[j];
         }
     }
-    __syncthreads();
+    fbar();
 }
 
 // Bitonic sort of s.key/s.cb.idx[0..n2) (n2 a power of two): by (key desc, idx asc) or by idx asc.
@@ -483,7 +502,7 @@ __device__ void bitonic(TopkSmem &s, int n2, bool by_score) {
                     s.cb.idx[j] = ia;
                 }
             }
-            __syncthreads();
+            fbar();
         }
     }
 }
@@ -528,13 +547,13 @@ __device__ bool bucket_sort(TopkSmem &s, int n, bool by_score) {
         s.hist[kThreads / 32 + warp] = hmax;
         s.hist[2 * (kThreads / 32) + warp] = vary;
     }
-    __syncthreads();  // also: every entry of the buffer is in registers (s.packed overlays it)
+    fbar();  // also: every entry of the buffer is in registers (s.packed overlays it)
     for (int w = 0; w < kThreads / 32; ++w) {
         hmin = min(hmin, s.hist[w]);
         hmax = max(hmax, s.hist[kThreads / 32 + w]);
         vary |= s.hist[2 * (kThreads / 32) + w];
     }
-    __syncthreads();
+    fbar();
     // the digit: up to 11 bits below the common prefix, above the lowest bit that varies
     const uint32_t diff = hmin ^ hmax;
     const int shift = diff ? 32 - __clz(diff) : 0;
@@ -545,10 +564,10 @@ __device__ bool bucket_sort(TopkSmem &s, int n, bool by_score) {
     auto digit = [&](uint64_t cc) { return ((uint32_t)(cc >> 32) >> sh) & dmask; };
 
     for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0u;
-    __syncthreads();
+    fbar();
 #pragma unroll
     for (int j = 0; j < kSortPer; ++j) hist_add(s.hist, digit(c[j]), j * kThreads + tid < n);
-    __syncthreads();
+    fbar();
 
     // bucket starts from the top bin down, and the cost (sum of squared sizes)
     constexpr int per = kBins / kThreads;
@@ -570,7 +589,7 @@ __device__ bool bucket_sort(TopkSmem &s, int n, bool by_score) {
     for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(kFull, sq, off);
     if (lane == 31) s.warp_tot[warp] = incl;
     if (lane == 0) s.warp_base[warp] = (int)sq;
-    __syncthreads();
+    fbar();
     uint32_t run = incl - local, cost = 0u;
     for (int v = 0; v < kThreads / 32; ++v) {
         if (v < warp) run += s.warp_tot[v];
@@ -584,7 +603,7 @@ __device__ bool bucket_sort(TopkSmem &s, int n, bool by_score) {
             run += h[i];
         }
     }
-    __syncthreads();
+    fbar();
     if (!ok) return false;
 
     // scatter by bucket: each entry takes the next slot of its bucket (the order within a bucket is
@@ -595,7 +614,7 @@ __device__ bool bucket_sort(TopkSmem &s, int n, bool by_score) {
         const uint32_t d = digit(c[j]);
         if (valid) s.packed[atomicAdd(&s.hist[d], 1u)] = c[j];
     }
-    __syncthreads();
+    fbar();
     // hist[d] is now the end of bucket d, and hist[d + 1] its start (buckets run from the top bin down)
     for (int i = tid; i < n; i += kThreads) {
         const uint64_t cc = s.packed[i];
@@ -607,7 +626,7 @@ __device__ bool bucket_sort(TopkSmem &s, int n, bool by_score) {
         for (int j = st; j < en; ++j) rank += s.packed[j] > cc ? 1 : 0;
         s.packed[n + st + rank] = cc;
     }
-    __syncthreads();
+    fbar();
     return true;
 }
 
@@ -654,13 +673,13 @@ __device__ bool select_sort_by_score(TopkSmem &s, int kk, int32_t *oi, float *ov
         s.hist[kThreads / 32 + warp] = hmax;
         s.hist[2 * (kThreads / 32) + warp] = vary;
     }
-    __syncthreads();  // also: every entry of the buffer is in registers (s.packed overlays it)
+    fbar();  // also: every entry of the buffer is in registers (s.packed overlays it)
     for (int w = 0; w < kThreads / 32; ++w) {
         hmin = min(hmin, s.hist[w]);
         hmax = max(hmax, s.hist[kThreads / 32 + w]);
         vary |= s.hist[2 * (kThreads / 32) + w];
     }
-    __syncthreads();
+    fbar();
     const uint32_t diff = hmin ^ hmax;
     const int shift = diff ? 32 - __clz(diff) : 0;
     const int low = vary ? __ffs(vary) - 1 : 0;
@@ -671,11 +690,11 @@ __device__ bool select_sort_by_score(TopkSmem &s, int kk, int32_t *oi, float *ov
 
     for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0u;
     if (tid == 0) s.found_bin = -1;
-    __syncthreads();
+    fbar();
 #pragma unroll
     for (int j = 0; j < kPerT; ++j)
         if (j * kThreads + tid < cnt) atomicAdd(&s.hist[digit(c[j])], 1u);
-    __syncthreads();
+    fbar();
 
     // bucket starts from the top bin down, the cost (sum of squared sizes), and the bucket holding
     // the kk-th entry
@@ -698,7 +717,7 @@ __device__ bool select_sort_by_score(TopkSmem &s, int kk, int32_t *oi, float *ov
     for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(kFull, sq, off);
     if (lane == 31) s.warp_tot[warp] = incl;
     if (lane == 0) s.warp_base[warp] = (int)sq;
-    __syncthreads();
+    fbar();
     uint32_t run = incl - local, cost = 0u;
     for (int v = 0; v < kThreads / 32; ++v) {
         if (v < warp) run += s.warp_tot[v];
@@ -714,12 +733,12 @@ __device__ bool select_sort_by_score(TopkSmem &s, int kk, int32_t *oi, float *ov
             run += h[i];
         }
     }
-    __syncthreads();
+    fbar();
     if (!ok) return false;
     const int cut = s.found_bin;
     if (cut < 0) {  // kk entries exist, so some bucket holds the kk-th (a broken invariant otherwise)
         if (tid == 0) s.broken = 1;
-        __syncthreads();
+        fbar();
         return false;
     }
 
@@ -730,7 +749,7 @@ __device__ bool select_sort_by_score(TopkSmem &s, int kk, int32_t *oi, float *ov
         const bool valid = j * kThreads + tid < cnt && d >= (uint32_t)cut;
         if (valid) s.packed[atomicAdd(&s.hist[d], 1u)] = c[j];  // the order within a bucket is free, as above
     }
-    __syncthreads();
+    fbar();
     // hist[d] is now the end of bucket d and hist[d + 1] its start; the cut bucket ends the scatter
     const int kept = (int)s.hist[cut];
     for (int i = tid; i < kept; i += kThreads) {
@@ -749,7 +768,7 @@ __device__ bool select_sort_by_score(TopkSmem &s, int kk, int32_t *oi, float *ov
             if (ov) ov[pos] = score_of(key, ix, x, n);
         }
     }
-    __syncthreads();
+    fbar();
     return true;
 }
 
@@ -921,9 +940,9 @@ __device__ void settle_tile(TopkSmem &s, const float *tile, int t, int n, int k,
     }
     int start = INT_MAX;
     for (int w = 0; w < kThreads / 32; ++w) start = min(start, s.warp_base[w]);
-    __syncthreads();  // every thread has read warp_base
+    fbar();  // every thread has read warp_base
     if (threadIdx.x == 0) s.count = start;
-    __syncthreads();
+    fbar();
     int cnt = start;
     float vals[kPer];
     load_tile_vals(tile, t, n, vals);
@@ -932,9 +951,9 @@ __device__ void settle_tile(TopkSmem &s, const float *tile, int t, int n, int k,
             set_threshold(compact(s, k, limit, false, idx_bits), thr, mode);
         }
         filter_append(s, vals, t, n, thr, mode, j);
-        __syncthreads();
+        fbar();
         cnt = s.count;
-        __syncthreads();  // every thread has read the count before it changes again
+        fbar();  // every thread has read the count before it changes again
     }
 }
 
@@ -983,65 +1002,82 @@ __device__ uint64_t sampled_bound(TopkSmem &s, const float *x, int n, int r) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) kmax = max(kmax, __shfl_xor_sync(kFull, kmax, off));
     if (lane == 0) s.warp_tot[warp] = kmax;
-    __syncthreads();
+    fbar();
     for (int w = 0; w < kThreads / 32; ++w) kmax = max(kmax, s.warp_tot[w]);
     const uint32_t wlo = kmax >= (1u << kWinBits) ? kmax - ((1u << kWinBits) - 1u) : 0u;
     for (int i0 = tid & ~31; i0 < kSample; i0 += kThreads) {
         const uint32_t key = s.sample[i0 + lane];
         hist_add(s.hist, (key - wlo) >> kBinBits, key >= wlo);
     }
-    __syncthreads();  // also: every thread has read warp_tot (find_bin rewrites it)
+    fbar();  // also: every thread has read warp_tot (find_bin rewrites it)
     find_bin(s, (uint32_t)r, true);
     if (s.found_bin >= 0) return (uint64_t)wlo + ((uint64_t)s.found_bin << kBinBits);
     const Descent d = radix_descent(s, s.sample, kSample, r, r + r / 4, false);
     return (uint64_t)d.prefix << d.shift;
 }
 
-// Persistent CTAs, each taking rows blockIdx.x, blockIdx.x + gridDim.x, ... Thread 0 keeps
-// kStages tiles of 4096 scores in flight (bulk copies into a shared-memory ring, one mbarrier
-// per stage), running ahead across row boundaries, and waits for each tile just before the
-// barrier that ends the previous one; every thread filters the landed tile into the candidate
-// buffer.
-__global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
+// Persistent CTAs, each taking rows blockIdx.x, blockIdx.x + gridDim.x, ... A producer warp keeps
+// kStages tiles of 4096 scores in flight (bulk copies into a shared-memory ring, one "full"
+// mbarrier per stage), running ahead across row boundaries, and refills a stage as soon as every
+// filter warp has released it (one "empty" mbarrier per stage). The 16 filter warps wait for each
+// tile themselves (one lane polls, bounded) and filter it into the candidate buffer; their own
+// barrier per tile only decides whether the buffer needs attention.
+__global__ void __launch_bounds__(kBlock, 2) topk_kernel(TopkParams p) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     TopkSmem &s = *reinterpret_cast<TopkSmem *>(smem_raw);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int k = p.k;
     const int idx_bits = p.ld <= (1 << 22) ? 22 : 32;
-    // producer cursor (thread 0): the next tile to copy into the ring, running ahead across rows
-    TileCursor ld_cur{(int)blockIdx.x, 0, blockIdx.x < p.rows ? row_length(p, blockIdx.x) : 0};
-    uint32_t issued = 0u, landed = 0u;  // thread 0: tiles copied so far / known to have landed
-    auto issue_next = [&](int stage) {
-        if (!cursor_settle(p, ld_cur)) return;
-        ++issued;
-        uint32_t bytes;
-        const float *src = cursor_src(p, ld_cur, bytes);
-        const uint32_t bar = ptx::smem_u32(&s.full[stage]);
-        ptx::mbar_arrive_expect_tx(bar, bytes);
-        ptx::bulk_g2s(ptx::smem_u32(s.ring[stage]), src, bytes, bar);  // default L2 policy: 1% faster than evict-first
-        ++ld_cur.tile;
-    };
+    volatile int *failed = &s.failed;
     if (tid == 0) {
-        for (int st = 0; st < kStages; ++st) ptx::mbar_init(ptx::smem_u32(&s.full[st]), 1);
+        for (int st = 0; st < kStages; ++st) {
+            ptx::mbar_init(ptx::smem_u32(&s.full[st]), 1);
+            ptx::mbar_init(ptx::smem_u32(&s.empty[st]), kThreads / 32);
+        }
         ptx::fence_mbar_init();
         s.failed = 0;
         s.broken = 0;
+        s.issued = 0u;
     }
     __syncthreads();
-    // Only thread 0 waits for a tile, just before a barrier: the barrier then releases everybody with
-    // the tile in shared memory (no other thread spins on the mbarrier).
+
+    if (tid >= kThreads) {
+        // ---------------------------------------------------------------- producer warp
+        if (tid == kThreads) {
+            TileCursor cur{(int)blockIdx.x, 0, blockIdx.x < p.rows ? row_length(p, blockIdx.x) : 0};
+            uint32_t it = 0u;
+            while (cursor_settle(p, cur)) {
+                const uint32_t st = it % kStages;
+                // the stage's previous tile has been released by every filter warp
+                if (it >= kStages && !ptx::mbar_wait(ptx::smem_u32(&s.empty[st]), ((it / kStages) & 1u) ^ 1u)) {
+                    *failed = 1;
+                    if (p.status) raise_status(p.status, RL_ERR_TIMEOUT);
+                    break;
+                }
+                if (*failed) break;
+                uint32_t bytes;
+                const float *src = cursor_src(p, cur, bytes);
+                const uint32_t bar = ptx::smem_u32(&s.full[st]);
+                ptx::mbar_arrive_expect_tx(bar, bytes);
+                ptx::bulk_g2s(ptx::smem_u32(s.ring[st]), src, bytes, bar);  // default L2 policy: 1% faster than evict-first
+                ++cur.tile;
+                ++it;
+                *reinterpret_cast<volatile uint32_t *>(&s.issued) = it;
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- filter warps
+    // Waits for tile gi to land (one lane of the warp polls, bounded); after a timeout the tiles are
+    // no longer waited for and the results are not valid (flagged).
     auto wait_tile = [&](uint32_t gi) {
-        if (gi >= issued) return;
-        if (!s.failed && !ptx::mbar_wait(ptx::smem_u32(&s.full[gi % kStages]), (gi / kStages) & 1u)) {
-            s.failed = 1;
+        if (lane == 0 && !*failed && !ptx::mbar_wait(ptx::smem_u32(&s.full[gi % kStages]), (gi / kStages) & 1u)) {
+            *failed = 1;
             if (p.status) raise_status(p.status, RL_ERR_TIMEOUT);
         }
-        if (!s.failed) landed = gi + 1u;
+        __syncwarp();
     };
-    if (tid == 0) {
-        for (int st = 0; st < kStages; ++st) issue_next(st);
-        wait_tile(0u);
-    }
 
     uint32_t g = 0;  // tiles consumed by this CTA
     for (int row = blockIdx.x; row < p.rows; row += gridDim.x) {
@@ -1053,7 +1089,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
             s.count = 0;
             s.keyed = 0;
         }
-        __syncthreads();
+        fbar();
         // incoming scores are kept when their key reaches a lower bound, tested on the score itself
         float thr = -INFINITY;
         int mode = 0;
@@ -1069,6 +1105,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
         const int ntiles = (n + kTile - 1) / kTile;
         for (int t = 0; t < ntiles; ++t, ++g) {
             const int st = (int)(g % kStages);
+            wait_tile(g);
             const float4 *tile4 = reinterpret_cast<const float4 *>(s.ring[st]);
             int after_add;
             {
@@ -1080,25 +1117,25 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
                 }
                 after_add = filter_append(s, vals, t, n, thr, mode, -1, st);
             }
-            if (tid == 0) wait_tile(g + 1u);
-            // The next tile has landed. Whether the buffer needs attention is decided by the barrier
-            // itself (the count passed kSoft iff some warp's append took it past): a thread must not
-            // read s.count here, because a faster warp may already be appending the next tile.
-            if (__syncthreads_or(after_add > kSoft)) {
-                const bool overflow = __syncthreads_or(after_add > kCap) != 0;
+            // Whether the buffer needs attention is decided by the barrier itself (the count passed
+            // kSoft iff some warp's append took it past): a thread must not read s.count here,
+            // because a faster warp may already be appending the next tile.
+            if (fbar_or(after_add > kSoft)) {
+                const bool overflow = fbar_or(after_add > kCap) != 0;
                 settle_tile(s, s.ring[st], t, n, k, idx_bits, overflow, thr, mode);
             }
-            if (tid == 0) issue_next(st);  // the stage is free again
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&s.empty[st]));  // this warp is done with the stage
         }
         // The sampled bound was above the row's kk-th best score (fewer than kk reached it, so no
         // compaction ran): scan the row again from -inf with plain loads (the tile ring has moved
         // on to the next row).
-        if (__syncthreads_or(sampled && s.count < kk)) {
+        if (fbar_or(sampled && s.count < kk)) {
             if (tid == 0) {
                 s.count = 0;
                 s.keyed = 0;
             }
-            __syncthreads();
+            fbar();
             thr = -INFINITY;
             mode = 0;
             for (int t = 0; t < ntiles; ++t) {
@@ -1109,8 +1146,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
                     load_tile_vals(tile, t, n, vals);
                     after_add = filter_append(s, vals, t, n, thr, mode, -1);
                 }
-                if (__syncthreads_or(after_add > kSoft)) {
-                    const bool overflow = __syncthreads_or(after_add > kCap) != 0;
+                if (fbar_or(after_add > kSoft)) {
+                    const bool overflow = fbar_or(after_add > kCap) != 0;
                     settle_tile(s, tile, t, n, k, idx_bits, overflow, thr, mode);
                 }
             }
@@ -1137,7 +1174,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
                     s.cb.key[i] = 0u;
                     s.cb.idx[i] = 0xffffffffu;
                 }
-                __syncthreads();
+                fbar();
                 if (n2 == 2 * kThreads)
                     bitonic_regs<2>(s, by_score);
                 else if (n2 == 4 * kThreads)
@@ -1167,11 +1204,12 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(TopkParams p) {
                 if (ov) ov[i] = -INFINITY;
             }
         }
-        __syncthreads();  // the buffer is reused by the next row
+        fbar();  // the buffer is reused by the next row
     }
     // after a timeout: let the copies that may still be in flight land before the CTA leaves (bounded)
-    if (tid == 0 && s.failed) {
-        for (uint32_t gi = landed; gi < issued; ++gi)
+    if (tid == 0 && *failed) {
+        const uint32_t issued = *reinterpret_cast<volatile uint32_t *>(&s.issued);
+        for (uint32_t gi = issued > (uint32_t)kStages ? issued - kStages : 0u; gi < issued; ++gi)  // the last ones
             ptx::mbar_wait(ptx::smem_u32(&s.full[gi % kStages]), (gi / kStages) & 1u, 100000000ull);
     }
 }
@@ -1204,7 +1242,7 @@ cudaError_t launch_topk(const TopkParams &p, cudaStream_t stream) {
         }
     }
     const int grid = std::min(p.rows, 2 * sms);  // persistent: two CTAs per SM
-    topk_kernel<<<grid, kThreads, sizeof(TopkSmem), stream>>>(p);
+    topk_kernel<<<grid, kBlock, sizeof(TopkSmem), stream>>>(p);
     return cudaGetLastError();
 }
 
