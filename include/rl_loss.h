@@ -296,7 +296,7 @@ typedef struct rl_gae_config {
 } rl_gae_config;
 
 /* Bytes of device workspace rl_gae_advantages needs for num_tokens tokens
- * (a 256-byte header and a 48-byte slot per 8192-token chunk). */
+ * (a 256-byte header and a 64-byte slot per 8192-token chunk). */
 RL_LOSS_API size_t rl_gae_workspace_bytes(int32_t num_tokens);
 
 /* Device pointers: rewards [T], values [T] fp32, mask [T] u8 (nonzero =

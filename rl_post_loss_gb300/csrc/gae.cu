@@ -33,11 +33,14 @@
 // to those stopping points. Every floating-point result depends only on the
 // inputs, never on timing: bit-identical from run to run. Waits are bounded
 // (1 s of %globaltimer by default); one that runs out raises RL_ERR_TIMEOUT
-// and treats the chunk as a response end. The advantages are written in place
-// of the staged rewards and leave by tensor stores (one thread) when the whole
-// chunk lies inside the covered range. The last block past its look-back
-// clears the flags and the ticket (records are only read under a flag set by
-// the same launch), so the workspace is ready for the next launch.
+// and treats the chunk as a response end. A map is published as 64-bit words
+// that each pair a value with the launch's tag, so the look-back reads one in
+// a single round trip. The advantages are written in place of the staged
+// rewards and each warp's rows leave by a tensor store as soon as the warp is
+// done, when the whole chunk lies inside the covered range. The last block
+// past its look-back resets the ticket and the block count and advances the
+// launch epoch (a record counts only under this launch's tag), so the
+// workspace is ready for the next launch with nothing else to clear.
 #include <cuda.h>
 
 #include <atomic>
@@ -79,15 +82,16 @@ struct GaeMap {
 
 // One slot per chunk in the workspace, at an offset that depends only on the
 // chunk index (so a later call with more chunks never reads an earlier call's
-// records as flags). flag: 0 nothing yet, 1 the map is published, 2 the
-// inclusive rollout count too.
+// records as its own). Every published 32-bit value travels in a 64-bit word
+// together with the launch's tag (single-copy atomic), so a reader takes a map
+// in one round trip, all its words at once, and accepts it when every tag is
+// this launch's: no flag, no ordering between the words, and nothing to clear
+// afterwards. Words 0-6: p, q, c, vf, bits, n_resp, n_roll (the map); word 7:
+// the inclusive rollout count, published after the look-back.
 struct ChunkRecord {
-    float p, q, c, vf;
-    uint32_t bits;
-    int32_t n_resp, n_roll, roll_incl;
-    uint32_t flag, pad[3];
+    uint64_t w[8];
 };
-static_assert(sizeof(ChunkRecord) == 48, "record size");
+static_assert(sizeof(ChunkRecord) == 64, "record size");
 constexpr int kWsHeader = 256;
 
 // Tensor maps of the token arrays viewed as [T / 32 rows x 32 floats] (one 128-byte row per
@@ -107,12 +111,14 @@ struct GaeSmall {
     int k, sa, sb, lo, hi;
     float EA, EV;
     int EP, ER;
+    uint32_t epoch;
     float pw[kTok + 1], qpw[kTok + 1];  // gl^k and gamma gl^(k-1), by repeated products
 };
 constexpr int kSmemTotal = kSmemBytes + (int)sizeof(GaeSmall);
 
 struct WsHeader {
     uint32_t ticket, done;
+    uint32_t epoch;  // launches so far (mod 2^32 - 1): the tag of this launch's records is epoch + 1
 };
 
 // The status word is optional for this entry point.
@@ -176,14 +182,14 @@ __device__ __forceinline__ GaeMap warp_suffix(GaeMap x) {
     return x;
 }
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ uint64_t ld_word(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
-__device__ __forceinline__ void st_release(uint32_t *p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_word(uint64_t *p, uint32_t v, uint32_t tag) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(((uint64_t)tag << 32) | v) : "memory");
 }
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -192,10 +198,17 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
-__device__ __forceinline__ GaeMap load_record(const ChunkRecord *rec) {
-    const float4 a = __ldcg(reinterpret_cast<const float4 *>(rec));
-    const int4 b = __ldcg(reinterpret_cast<const int4 *>(rec) + 1);
-    return GaeMap{a.x, a.y, a.z, a.w, (uint32_t)b.x, b.y, b.z};
+// The map of a record, and whether all of its words carry `tag` (else it is not published yet).
+__device__ __forceinline__ bool load_record(const ChunkRecord *rec, uint32_t tag, GaeMap &m) {
+    uint64_t x[7];
+#pragma unroll
+    for (int i = 0; i < 7; ++i) x[i] = ld_word(&rec->w[i]);
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < 7; ++i) ok &= (uint32_t)(x[i] >> 32) == tag;
+    m = GaeMap{__uint_as_float((uint32_t)x[0]), __uint_as_float((uint32_t)x[1]), __uint_as_float((uint32_t)x[2]),
+               __uint_as_float((uint32_t)x[3]), (uint32_t)x[4], (int32_t)(uint32_t)x[5], (int32_t)(uint32_t)x[6]};
+    return ok;
 }
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
@@ -319,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p, con
     if (tid == 0) {
         const uint32_t ticket = atomicAdd(&hdr->ticket, 1u);
         s_k = nchunks - 1 - (int)ticket;
+        sm.epoch = *reinterpret_cast<volatile uint32_t *>(&hdr->epoch);
     }
     s_last[tid] = 0u;
     s_cont[tid] = 0u;
@@ -335,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p, con
     }
     __syncthreads();
     const int k = s_k;
+    const uint32_t epoch = sm.epoch, tag = epoch % 0xffffffffu + 1u;  // never 0 (a zeroed workspace)
     if (!RLK_CHECK(p.status, k < nchunks)) return;
     if (k < 0) {  // a ticket counter left dirty (the workspace was not zeroed): flag and stop
         if (tid == 0) gae_raise(p.status, RL_ERR_INVALID_ARG);
@@ -519,11 +534,15 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p, con
         const GaeMap wi = warp_suffix<kCross>(lane < kThreads / 32 ? s_wtot[lane] : map_identity());
         agg = shfl_map<kCross>(wi, 0);
         if (warp == 1) {
-            if (lane == 0 && k != p.withhold_chunk) {  // publish (the release fence stalls this warp, not the look-back)
-                ChunkRecord *rec = recs + k;
-                *reinterpret_cast<float4 *>(rec) = make_float4(agg.p, agg.q, agg.c, agg.vf);
-                *(reinterpret_cast<int4 *>(rec) + 1) = make_int4((int)agg.bits, agg.n_resp, agg.n_roll, 0);
-                st_release(&rec->flag, 1u);
+            if (lane < 7 && k != p.withhold_chunk) {  // publish: one tagged word per lane
+                const uint32_t v = lane == 0 ? __float_as_uint(agg.p)
+                                 : lane == 1 ? __float_as_uint(agg.q)
+                                 : lane == 2 ? __float_as_uint(agg.c)
+                                 : lane == 3 ? __float_as_uint(agg.vf)
+                                 : lane == 4 ? agg.bits
+                                 : lane == 5 ? (uint32_t)agg.n_resp
+                                             : (uint32_t)agg.n_roll;
+                st_word(&recs[k].w[lane], v, tag);
             }
         } else {
             GaeMap after = shfl_down_map<kCross>(wi, 1);
@@ -542,16 +561,18 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p, con
                 const int j = base + lane;
                 bool ready = j >= nchunks;  // beyond the last chunk: the zero state
                 GaeMap m = map_zero();
-                uint32_t f = 0u;
+                bool incl = false;  // the inclusive rollout count is published too
                 int incl_roll = 0;
                 int fcm = -1, fcr = -1;
                 while (true) {
                     if (!ready) {
-                        f = ld_acquire(&recs[j].flag);
-                        if (f) {
+                        GaeMap mj;
+                        const uint64_t w7 = kCross ? ld_word(&recs[j].w[7]) : 0ull;
+                        if (load_record(recs + j, tag, mj)) {
                             ready = true;
-                            m = load_record(recs + j);
-                            if (kCross && f >= 2u) incl_roll = __ldcg(&recs[j].roll_incl);
+                            m = mj;
+                            incl = kCross && (uint32_t)(w7 >> 32) == tag;
+                            incl_roll = (int)(uint32_t)w7;
                         } else if (global_ns() - t_begin > p.wait_ns) {
                             gae_raise(p.status, RL_ERR_TIMEOUT);
                             ready = true;  // treated as a response end
@@ -559,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p, con
                     }
                     const unsigned rdy = __ballot_sync(kFull, ready);
                     const unsigned stm = __ballot_sync(kFull, ready && (m.bits & kClosed));
-                    const unsigned str = __ballot_sync(kFull, ready && (f >= 2u || !(m.bits & kPassRoll)));
+                    const unsigned str = __ballot_sync(kFull, ready && (incl || !(m.bits & kPassRoll)));
                     const int pre = rdy == kFull ? 32 : __ffs(~rdy) - 1;  // lanes 0..pre-1 are ready
                     fcm = __ffs(stm) - 1;
                     fcr = __ffs(str) - 1;
@@ -574,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p, con
                     need_map = fcm < 0;
                 }
                 if (kCross && need_roll) {
-                    int val = f >= 2u ? incl_roll : m.n_roll;
+                    int val = incl ? incl_roll : m.n_roll;
                     if (fcr >= 0 && lane > fcr) val = 0;
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) val += __shfl_xor_sync(kFull, val, off);
@@ -593,21 +614,18 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p, con
     __syncthreads();
     if (warp == 1) {
         if (lane == 0) {
-            if (kCross && k != p.withhold_chunk) {
-                recs[k].roll_incl = agg.n_roll + ((agg.bits & kPassRoll) ? s_ER : 0);
-                st_release(&recs[k].flag, 2u);
-            }
+            if (kCross && k != p.withhold_chunk)
+                st_word(&recs[k].w[7], (uint32_t)(agg.n_roll + ((agg.bits & kPassRoll) ? s_ER : 0)), tag);
         }
         // past the look-back: the last block to get here leaves the workspace ready for the next launch
         uint32_t d = 0u;
         if (lane == 0) asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(d) : "l"(&hdr->done) : "memory");
         d = __shfl_sync(kFull, d, 0);
-        if (d == (uint32_t)nchunks - 1u) {
-            for (int j = lane; j < nchunks; j += 32) recs[j].flag = 0u;
-            if (lane == 0) {
-                hdr->ticket = 0u;
-                hdr->done = 0u;
-            }
+        if (d == (uint32_t)nchunks - 1u && lane == 0) {
+            // every block has read the epoch (before its look-back): the next launch's tag is new
+            hdr->ticket = 0u;
+            hdr->done = 0u;
+            hdr->epoch = epoch + 1u;
         }
     }
 
@@ -689,17 +707,19 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p, con
         }
     }
 
-    // store: tensor stores of a chunk that lies inside [lo, hi), issued by one thread; else
-    // coalesced 16-byte stores of the rows inside [lo, hi), token by token elsewhere
+    // store: each warp's 32 rows by tensor stores as soon as the warp is done, when the chunk
+    // lies inside [lo, hi); else coalesced 16-byte stores of the rows inside [lo, hi), token by
+    // token elsewhere
     const int a_in = min(max(s_lo - cs, 0), kChunk), b_in = min(max(min(s_hi, ce) - cs, 0), kChunk);
     if (tma && a_in == 0 && b_in == kChunk) {
-        ptx::fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            ptx::tma_store_2d(&maps.adv, 0, k * kThreads, ptx::smem_u32(s_r));
-            if (want_ret) ptx::tma_store_2d(&maps.ret, 0, k * kThreads, ptx::smem_u32(s_v));
+        ptx::fence_proxy_async_smem();  // this thread's row, written above, is visible to the copy
+        __syncwarp();
+        if (lane == 0) {
+            const int y = k * kThreads + warp * 32;
+            ptx::tma_store_2d(&maps.adv, 0, y, ptx::smem_u32(s_r + warp * 32 * kTok));
+            if (want_ret) ptx::tma_store_2d(&maps.ret, 0, y, ptx::smem_u32(s_v + warp * 32 * kTok));
             ptx::bulk_commit_group();
-            ptx::bulk_wait_group_read<0>();  // shared memory is read before the block exits
+            ptx::bulk_wait_group_read<0>();  // shared memory is read before the warp (and block) exits
         }
         return;
     }
@@ -734,9 +754,9 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p, con
     }
 }
 
-// [rows x 32] fp32 view of a token array, boxes of kThreads rows, 128-byte swizzle.
-bool token_map(CUtensorMap *m, const float *base, int64_t rows) {
-    return make_tmap_sw128(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, rows, kTok, kTok, kTok, kThreads);
+// [rows x 32] fp32 view of a token array, boxes of box_rows rows, 128-byte swizzle.
+bool token_map(CUtensorMap *m, const float *base, int64_t rows, uint32_t box_rows) {
+    return make_tmap_sw128(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, rows, kTok, kTok, kTok, box_rows);
 }
 
 template <bool kCross>
@@ -755,8 +775,8 @@ cudaError_t launch_chunks(const GaeParams &p, unsigned nchunks, cudaStream_t str
     GaeMaps maps{};
     const int64_t rows = p.num_tokens / kTok;
     if (p.vec && rows >= kThreads) {
-        maps.ok = token_map(&maps.r, p.rewards, rows) && token_map(&maps.v, p.values, rows) &&
-                  token_map(&maps.adv, p.adv, rows) && (!p.returns || token_map(&maps.ret, p.returns, rows));
+        maps.ok = token_map(&maps.r, p.rewards, rows, kThreads) && token_map(&maps.v, p.values, rows, kThreads) &&
+                  token_map(&maps.adv, p.adv, rows, 32) && (!p.returns || token_map(&maps.ret, p.returns, rows, 32));
         if (!p.returns) maps.ret = maps.adv;
     }
     gae_chunk_kernel<kCross><<<nchunks, kThreads, kSmemTotal, stream>>>(p, maps);

@@ -155,14 +155,13 @@ def test_gae_full_size_and_bit_identical():
 
 
 def _workspace_is_clear(T):
-    """The ticket and done counters and every chunk's flag are zero again."""
+    """The ticket and done counters are zero again (a chunk's record counts only under the tag of
+    the launch that wrote it, so the records need no clearing), and the launch epoch is set."""
     ws = capi.gae_workspace(T, torch.device("cuda", torch.cuda.current_device()))
     torch.cuda.synchronize()
     assert ws.data_ptr() == capi.gae_workspace(T, "cuda").data_ptr()
     words = ws.view(torch.int32).cpu().numpy()
-    slots = (words.size * 4 - 256) // 48
-    flags = words[(256 + 32) // 4::12][:slots]
-    return bool(np.all(words[:2] == 0)) and bool(np.all(flags == 0))
+    return bool(np.all(words[:2] == 0)) and int(words[2]) != 0
 
 
 def test_gae_long_responses_span_many_chunks():
@@ -298,3 +297,25 @@ def test_gae_full_size_repeated_launches_are_bit_identical():
         assert torch.equal(a0.view(torch.int32), a1.view(torch.int32))
     assert st.item() == 0
     assert _workspace_is_clear(gb.num_tokens)
+
+
+def test_records_of_an_earlier_call_are_never_read():
+    """A chunk's published map counts only under the tag of the launch that wrote it: a call on a
+    workspace that holds another batch's records (same token count) must equal the same call on a
+    fresh, zeroed workspace, bit for bit."""
+    a = synthetic.make_gae_batch("cuda", seed=0, lengths=[300000, 3, 140000, 70000], segments=2)
+    b = synthetic.make_gae_batch("cuda", seed=1, lengths=[300000, 3, 140000, 70000], segments=2)
+    T = a.num_tokens
+    ws = torch.zeros(capi.rl_gae_workspace_bytes(T), dtype=torch.uint8, device="cuda")
+    capi.gae(a.rewards, a.values, a.mask, a.cu_seqlens, a.gamma, a.lam, True, rollout_ids=a.rollout_ids, workspace=ws)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = capi.gae(b.rewards, b.values, b.mask, b.cu_seqlens, b.gamma, b.lam, True, rollout_ids=b.rollout_ids,
+                   workspace=ws, device_status=st)
+    fresh = torch.zeros_like(ws)
+    want = capi.gae(b.rewards, b.values, b.mask, b.cu_seqlens, b.gamma, b.lam, True, rollout_ids=b.rollout_ids,
+                    workspace=fresh)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(got.view(torch.int32), want.view(torch.int32))
+    assert not torch.equal(got, capi.gae(a.rewards, a.values, a.mask, a.cu_seqlens, a.gamma, a.lam, True,
+                                          rollout_ids=a.rollout_ids, workspace=fresh))
