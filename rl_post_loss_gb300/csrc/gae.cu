@@ -480,8 +480,12 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p, con
 
     // fold the thread's tokens, right to left
     GaeMap F = map_identity();
-    if (last == 0u) {
-        // no response end among them: only the action tokens' affine steps
+    if (__popc(last) <= 1) {
+        // at most one response end among them (at e): the map is the affine steps of the tokens from
+        // e leftwards, from the zero state the end resets to; the tokens right of it only count
+        const int e = last ? 31 - __clz(last) : -1;
+        const uint32_t left = e < 0 || e == 31 ? 0xffffffffu : (2u << e) - 1u;  // tokens 0..e (all: no end)
+        const uint32_t actl = act & left;
         float c = 0.f, vf = 0.f;
 #pragma unroll
         for (int j = kVec - 1; j >= 0; --j) {
@@ -490,16 +494,25 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p, con
             const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
             for (int u = 3; u >= 0; --u) {
-                if ((act >> (4 * j + u)) & 1u) {
+                if ((actl >> (4 * j + u)) & 1u) {
                     c = fmaf(gl, c, fmaf(gamma, vf, rr[u] - vv[u]));
                     vf = vv[u];
                 }
             }
         }
-        const int na = __popc(act), n = kCross ? __popc(msk) : 0;
-        F = GaeMap{s_pow[na], s_qpow[na], c, vf, (na ? 0u : kPassV) | kPassRoll, n, n};
+        const int na = __popc(actl);
+        if (last == 0u) {
+            const int n = kCross ? __popc(msk) : 0;
+            F = GaeMap{s_pow[na], s_qpow[na], c, vf, (na ? 0u : kPassV) | kPassRoll, n, n};
+        } else {
+            // closed: nothing from the right reaches further left; the rollout count passes the end
+            // only if the rollout goes on past it
+            const bool ce = (cont >> e) & 1u;
+            const int nl = kCross ? __popc(msk & left) : 0, nr = kCross ? __popc(msk & ~left) : 0;
+            F = GaeMap{0.f, 0.f, c, vf, kClosed | (ce ? kPassRoll : 0u), nl, nl + (ce ? nr : 0)};
+        }
     } else {
-        // a response ends among them (rare): token by token
+        // two or more responses end among them (responses shorter than 32 tokens): token by token
 #pragma unroll 1
         for (int i = kTok - 1; i >= 0; --i) {
             const int o = 4 * ((i >> 2) ^ sw) + (i & 3);
@@ -663,6 +676,41 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p, con
                     A = fmaf(gl, A, fmaf(gamma, V, rr[u] - vv[u]));
                     V = vv[u];
                     const float o = !kCross ? A : (single ? A * f1 : apply_scale(A, sc));
+                    out[u] = o;
+                    ret[u] = o + vv[u];
+                }
+            }
+            *reinterpret_cast<float4 *>(wrow_r + 4 * (j ^ sw)) = make_float4(out[0], out[1], out[2], out[3]);
+            if (want_ret)
+                *reinterpret_cast<float4 *>(wrow_v + 4 * (j ^ sw)) = make_float4(ret[0], ret[1], ret[2], ret[3]);
+        }
+    } else if (__popc(last) == 1) {
+        // one response end among them (at e): the tokens right of it with the arriving state and
+        // their response's factor, then from e leftwards from the zero state with their own factor
+        // (the same steps, in the same order, as the token-by-token walk below)
+        const int e = 31 - __clz(last);
+        Scale scR{1.f, 1.f, 1.f, 1.f}, scL{1.f, 1.f, 1.f, 1.f};
+        if (kCross) {
+            const uint32_t right = e == 31 ? 0u : ~((2u << e) - 1u);
+            scR = cross_scale(R - P, sargs);
+            scL = cross_scale(((cont >> e) & 1u) ? R + __popc(msk & right) : 0, sargs);
+        }
+#pragma unroll
+        for (int j = kVec - 1; j >= 0; --j) {
+            const float4 r4 = *reinterpret_cast<const float4 *>(row_r + 4 * (j ^ sw));
+            const float4 v4 = *reinterpret_cast<const float4 *>(row_v + 4 * (j ^ sw));
+            const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, vv[4] = {v4.x, v4.y, v4.z, v4.w};
+            float out[4], ret[4];
+#pragma unroll
+            for (int u = 3; u >= 0; --u) {
+                const int i = 4 * j + u;
+                out[u] = 0.f;
+                ret[u] = 0.f;
+                if (i == e) A = V = 0.f;
+                if ((act >> i) & 1u) {
+                    A = fmaf(gl, A, fmaf(gamma, V, rr[u] - vv[u]));
+                    V = vv[u];
+                    const float o = !kCross ? A : apply_scale(A, i <= e ? scL : scR);
                     out[u] = o;
                     ret[u] = o + vv[u];
                 }
