@@ -110,7 +110,8 @@ def gae_error_bound(gb, ref, act, gamma, lam, cross):
     return bound * 1.0001 + 1e-30
 
 
-@pytest.mark.parametrize("lengths", [[1], [5, 0, 7], [1000, 1024, 1025, 3000], [40] * 64, [20000, 16384]])
+@pytest.mark.parametrize("lengths", [[1], [5, 0, 7], [1000, 1024, 1025, 3000], [40] * 64, [20000, 16384],
+                                     [33, 31, 1, 2, 64, 63, 65, 100, 7, 25] * 30])
 @pytest.mark.parametrize("skip,cross", [(True, False), (False, False), (True, True)])
 def test_gae_layouts(lengths, skip, cross):
     gb = synthetic.make_gae_batch("cuda", lengths=lengths, segments=2)
