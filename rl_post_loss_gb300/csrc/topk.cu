@@ -51,6 +51,8 @@ constexpr int kTile = kThreads * kPer;  // 4096
 constexpr int kCap = 5120;              // buffer entries
 constexpr int kSlice = 512;             // positions per slice of a tile that overflowed the buffer
 constexpr int kSoft = kCap - kSlice;    // a count above this compacts after the tile
+constexpr int kCheck = 8;              // sampled rows: tiles between the checks of the count
+constexpr int kSoftSampled = kCap - kCheck * 64;  // ... and the count that compacts at a check
 constexpr int kBins = 2048;
 constexpr int kStages = 4;              // tiles in flight per CTA (16 KB each)
 constexpr unsigned kFull = 0xffffffffu;
@@ -1103,41 +1105,76 @@ __global__ void __launch_bounds__(kBlock, 2) topk_kernel(TopkParams p) {
             set_threshold(sampled_bound(s, p.scores + (size_t)row * (size_t)p.ld, n, r), thr, mode);
         }
         const int ntiles = (n + kTile - 1) / kTile;
-        for (int t = 0; t < ntiles; ++t, ++g) {
-            const int st = (int)(g % kStages);
-            wait_tile(g);
+        auto ring_vals = [&](int st, float (&vals)[kPer]) {
             const float4 *tile4 = reinterpret_cast<const float4 *>(s.ring[st]);
-            int after_add;
-            {
-                float vals[kPer];
 #pragma unroll
-                for (int j = 0; j < kPer / 4; ++j) {
-                    const float4 v = tile4[j * kThreads + tid];
-                    vals[4 * j] = v.x, vals[4 * j + 1] = v.y, vals[4 * j + 2] = v.z, vals[4 * j + 3] = v.w;
+            for (int j = 0; j < kPer / 4; ++j) {
+                const float4 v = tile4[j * kThreads + tid];
+                vals[4 * j] = v.x, vals[4 * j + 1] = v.y, vals[4 * j + 2] = v.z, vals[4 * j + 3] = v.w;
+            }
+        };
+        if (sampled) {
+            // The sampled bound keeps about 3.5K scores of a 200K-score row, inside the buffer: the
+            // warps stream the row with a block barrier only every kCheck tiles, each releasing a
+            // stage as soon as it is done with it. At a barrier, a count past kSoftSampled compacts
+            // the buffer (raising the bound); an append past the buffer is counted but not written,
+            // and the row is then scanned again below.
+            int grp = 0;  // this warp's count after its last append since the last barrier
+            for (int t = 0; t < ntiles; ++t, ++g) {
+                const int st = (int)(g % kStages);
+                wait_tile(g);
+                {
+                    float vals[kPer];
+                    ring_vals(st, vals);
+                    grp = max(grp, filter_append(s, vals, t, n, thr, mode, -1, st));
                 }
-                after_add = filter_append(s, vals, t, n, thr, mode, -1, st);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&s.empty[st]));  // this warp is done with the stage
+                if ((t % kCheck) == kCheck - 1 && t + 1 < ntiles) {
+                    if (fbar_or(grp > kSoftSampled) && !fbar_or(grp > kCap))
+                        set_threshold(compact(s, k, k + (kSoft - k) / 2, false, idx_bits), thr, mode);
+                    grp = 0;
+                }
             }
-            // Whether the buffer needs attention is decided by the barrier itself (the count passed
-            // kSoft iff some warp's append took it past): a thread must not read s.count here,
-            // because a faster warp may already be appending the next tile.
-            if (fbar_or(after_add > kSoft)) {
-                const bool overflow = fbar_or(after_add > kCap) != 0;
-                settle_tile(s, s.ring[st], t, n, k, idx_bits, overflow, thr, mode);
+        } else {
+            for (int t = 0; t < ntiles; ++t, ++g) {
+                const int st = (int)(g % kStages);
+                wait_tile(g);
+                int after_add;
+                {
+                    float vals[kPer];
+                    ring_vals(st, vals);
+                    after_add = filter_append(s, vals, t, n, thr, mode, -1, st);
+                }
+                // Whether the buffer needs attention is decided by the barrier itself (the count
+                // passed kSoft iff some warp's append took it past): a thread must not read s.count
+                // here, because a faster warp may already be appending the next tile.
+                if (fbar_or(after_add > kSoft)) {
+                    const bool overflow = fbar_or(after_add > kCap) != 0;
+                    settle_tile(s, s.ring[st], t, n, k, idx_bits, overflow, thr, mode);
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&s.empty[st]));  // this warp is done with the stage
             }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&s.empty[st]));  // this warp is done with the stage
         }
-        // The sampled bound was above the row's kk-th best score (fewer than kk reached it, so no
-        // compaction ran): scan the row again from -inf with plain loads (the tile ring has moved
-        // on to the next row).
-        if (fbar_or(sampled && s.count < kk)) {
+        fbar();  // every append of the row is done
+        const int cnt = s.count;
+        // A sampled row is scanned again with plain loads (the tile ring has moved on to the next
+        // row), with a block barrier per tile and the compactions: from -inf if its bound was above
+        // the row's kk-th best score (fewer than kk reached it), from the same bound if the scores
+        // at or above it overflowed the buffer (ties at the bound).
+        const bool from_inf = sampled && cnt < kk, again = from_inf || (sampled && cnt > kCap);
+        if (again) {
+            fbar();  // every thread has read the count
             if (tid == 0) {
                 s.count = 0;
                 s.keyed = 0;
             }
             fbar();
-            thr = -INFINITY;
-            mode = 0;
+            if (from_inf) {
+                thr = -INFINITY;
+                mode = 0;
+            }
             for (int t = 0; t < ntiles; ++t) {
                 const float *tile = p.scores + (size_t)row * (size_t)p.ld + (size_t)t * kTile;
                 int after_add;
