@@ -688,7 +688,19 @@ __device__ bool select_sort_by_score(TopkSmem &s, int kk, int32_t *oi, float *ov
     const int w = min(11, max(shift - low, 0));
     const int sh = shift - w;
     const uint32_t dmask = w ? (1u << w) - 1u : 0u;
-    auto digit = [&](uint64_t cc) { return ((uint32_t)(cc >> 32) >> sh) & dmask; };
+    // When the key bits take fewer than 11 bits of the digit and cover every bit in which the keys
+    // differ, each key bucket holds a single key (low-precision scores tie often), and its entries
+    // are ordered by position alone. The spare iw bits then split it further by position: the
+    // entry at ix gets floor((n - 1 - ix) * (2^iw - 1) / n), which rises as ix falls, as the packed word
+    // does. Float rounding keeps that map monotone, so every bucket is still a range of the order.
+    // (The scale is (2^iw - 1) / n, so that the product stays below 2^iw without a clamp.)
+    const int iw = (shift - low <= 11) ? 11 - w : 0;
+    const float iscale = (float)((1u << iw) - 1u) / (float)max(n, 1);  // 0 when iw is 0
+    auto digit = [&](uint64_t cc) {
+        const uint32_t d = ((uint32_t)(cc >> 32) >> sh) & dmask;
+        const int ix = (int)~(uint32_t)cc;
+        return (d << iw) | (uint32_t)((float)max(n - 1 - ix, 0) * iscale);
+    };
 
     for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0u;
     if (tid == 0) s.found_bin = -1;

@@ -143,7 +143,9 @@ def test_full_size_sampled_rows_and_properties():
 
 # The final pass ranks the selection within buckets of the key's leading bits when the buckets
 # are even enough (sum of squared sizes at most 128 per entry) and falls back to an exact select
-# plus a separate sort otherwise; rows with few distinct values land on either side of that.
+# plus a separate sort otherwise. When every bucket holds a single key, the spare digit bits split
+# the tied entries by position; rows with few distinct values tie heavily, so they take that split
+# in score order and the separate sort in position order.
 @pytest.mark.parametrize("distinct", [3, 40, 1000, 5000])
 @pytest.mark.parametrize("order", ["score", "index"])
 def test_few_distinct_values_long_rows(distinct, order):
