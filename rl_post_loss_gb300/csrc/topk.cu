@@ -844,9 +844,8 @@ __device__ __forceinline__ int tile_elem(int t, int q) {
 // the tile's positions [512 slice, 512 slice + 512). Entries that would land at kCap or beyond are
 // not written. Records where the warp's append started in warp_base and returns the buffer count
 // right after it (0 when the warp appends nothing).
-__device__ __forceinline__ int filter_append(TopkSmem &s, const float (&vals)[kPer], int t, int n, float thr,
-                                             int mode, int slice, int stage = -1) {
-    const int lane = threadIdx.x & 31;
+// Bit q set: value q of this thread's part of tile t is kept (inside the row, key at or above the bound).
+__device__ __forceinline__ uint32_t keep_mask(const float (&vals)[kPer], int t, int n, float thr, int mode) {
     uint32_t keepm = 0u;
     if (mode == 0 && (t + 1) * kTile <= n) {  // a full tile and a plain threshold: one compare per score
 #pragma unroll
@@ -858,6 +857,13 @@ __device__ __forceinline__ int filter_append(TopkSmem &s, const float (&vals)[kP
             keepm |= (uint32_t)keep << q;
         }
     }
+    return keepm;
+}
+
+__device__ __forceinline__ int filter_append(TopkSmem &s, const float (&vals)[kPer], int t, int n, float thr,
+                                             int mode, int slice, int stage = -1) {
+    const int lane = threadIdx.x & 31;
+    uint32_t keepm = keep_mask(vals, t, n, thr, mode);
     if (slice >= 0)  // slice j: threads [128 (j % 4), +128), first (j < 4) or second float4
         keepm &= ((int)threadIdx.x >> 7) == (slice & 3) ? (0x0fu << (4 * (slice >> 2))) : 0u;
     const unsigned m = __ballot_sync(kFull, keepm != 0u);  // the lanes that keep something
@@ -925,6 +931,102 @@ __device__ __forceinline__ int filter_append(TopkSmem &s, const float (&vals)[kP
         }
     }
     return base + total;
+}
+
+// Warp-private appends for rows that start from the sampled bound: warp w owns entries
+// [w kRegion, (w + 1) kRegion) of the buffer and keeps its fill in a register, so an append needs
+// no shared atomic and no broadcast. The fills stay near 3.5K / 16 = 220 on low-precision indexer
+// scores. A check that finds a fill above kRegionSoft gathers the regions and continues with the
+// shared count; entries past a region's end are counted but not written (the row is then scanned
+// again, as for a buffer overflow).
+constexpr int kRegion = kCap / (kThreads / 32);  // 320
+constexpr int kRegionSoft = kRegion - 4 * kCheck;  // 288
+static_assert(kRegion * (kThreads / 32) == kCap, "the regions tile the buffer");
+
+// Appends this thread's kept scores of tile t (held in ring stage `stage`) to its warp's region
+// after `fill` entries; returns the warp's new fill (the same in every lane).
+__device__ __forceinline__ int region_append(TopkSmem &s, const float (&vals)[kPer], int t, int n, float thr,
+                                             int mode, int stage, int fill) {
+    const int lane = threadIdx.x & 31;
+    uint32_t keepm = keep_mask(vals, t, n, thr, mode);
+    const unsigned m = __ballot_sync(kFull, keepm != 0u);
+    if (m == 0u) return fill;
+    uint32_t *rk = s.cb.key + (threadIdx.x >> 5) * kRegion;
+    uint32_t *ri = s.cb.idx + (threadIdx.x >> 5) * kRegion;
+    const int base = t * kTile + 4 * (int)threadIdx.x;  // the row position of value 0; value q adds off(q)
+    auto put = [&](int pos, uint32_t bits) {
+        const int q = __ffs(bits) - 1;
+        const int off = 4 * kThreads * (q >> 2) + (q & 3);
+        if (pos < kRegion) {
+            rk[pos] = __float_as_uint(s.ring[stage][4 * (int)threadIdx.x + off]);  // raw bits, keyed later
+            ri[pos] = (uint32_t)(base + off);
+        }
+    };
+    // every keeping lane's first score: its place among the keeping lanes
+    if (keepm) put(fill + __popc(m & ((1u << lane) - 1u)), keepm);
+    int next = fill + __popc(m);
+    keepm &= keepm - 1u;
+    if (__any_sync(kFull, keepm != 0u)) {
+        // lanes that keep several scores of the tile: the rest after every first, in lane order
+        const int c = __popc(keepm);
+        int incl = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(kFull, incl, off);
+            if (lane >= off) incl += o;
+        }
+        int pos = next + incl - c;
+        next += __shfl_sync(kFull, incl, 31);
+        while (keepm) {
+            put(pos++, keepm);
+            keepm &= keepm - 1u;
+        }
+    }
+    return next;
+}
+
+// Moves the regions' entries (fill = the calling warp's fill, at most kRegion) to the front of the
+// buffer in warp order and sets the count to their total. Every append must be done. Block-wide;
+// ends with a barrier.
+__device__ void gather_regions(TopkSmem &s, int fill) {
+    constexpr int kPerT = kCap / kThreads;
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (lane == 0) s.warp_tot[tid >> 5] = (uint32_t)min(fill, kRegion);
+    fbar();
+    // lane v: warp v's fill and where its entries go
+    const int f = lane < kThreads / 32 ? (int)s.warp_tot[lane] : 0;
+    int incl = f;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += o;
+    }
+    const int start = incl - f;
+    const int total = __shfl_sync(kFull, incl, 31);
+    uint32_t key[kPerT], idx[kPerT];
+    int dst[kPerT];
+#pragma unroll
+    for (int j = 0; j < kPerT; ++j) {
+        const int i = j * kThreads + tid;
+        const int w = i / kRegion, r = i - w * kRegion;
+        const int fw = __shfl_sync(kFull, f, w), sw = __shfl_sync(kFull, start, w);
+        dst[j] = r < fw ? sw + r : -1;
+        key[j] = s.cb.key[i];
+        idx[j] = s.cb.idx[i];
+    }
+    fbar();
+#pragma unroll
+    for (int j = 0; j < kPerT; ++j) {
+        if (dst[j] >= 0) {
+            s.cb.key[dst[j]] = key[j];
+            s.cb.idx[dst[j]] = idx[j];
+        }
+    }
+    if (tid == 0) {
+        s.count = total;
+        s.keyed = 0;
+    }
+    fbar();
 }
 
 // This thread's kPer scores of tile t, read from `tile` (the tile's first score, in the ring or in
@@ -1131,21 +1233,50 @@ __global__ void __launch_bounds__(kBlock, 2) topk_kernel(TopkParams p) {
             // stage as soon as it is done with it. At a barrier, a count past kSoftSampled compacts
             // the buffer (raising the bound); an append past the buffer is counted but not written,
             // and the row is then scanned again below.
-            int grp = 0;  // this warp's count after its last append since the last barrier
+            // The warps start in their own regions of the buffer (region_append). A check that finds
+            // a region nearly full, with nothing dropped yet, gathers the regions and continues with
+            // the shared count, compacting as above.
+            int grp = 0;   // shared count: this warp's count after its last append since the last barrier
+            int fill = 0;  // regions: this warp's fill
+            bool regions = true;
             for (int t = 0; t < ntiles; ++t, ++g) {
                 const int st = (int)(g % kStages);
                 wait_tile(g);
                 {
                     float vals[kPer];
                     ring_vals(st, vals);
-                    grp = max(grp, filter_append(s, vals, t, n, thr, mode, -1, st));
+                    if (regions)
+                        fill = region_append(s, vals, t, n, thr, mode, st, fill);
+                    else
+                        grp = max(grp, filter_append(s, vals, t, n, thr, mode, -1, st));
                 }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&s.empty[st]));  // this warp is done with the stage
                 if ((t % kCheck) == kCheck - 1 && t + 1 < ntiles) {
-                    if (fbar_or(grp > kSoftSampled) && !fbar_or(grp > kCap))
+                    if (regions) {
+                        if (fbar_or(fill > kRegionSoft) && !fbar_or(fill > kRegion)) {
+                            gather_regions(s, fill);
+                            regions = false;
+                            if (s.count > kSoftSampled)
+                                set_threshold(compact(s, k, k + (kSoft - k) / 2, false, idx_bits), thr, mode);
+                        }
+                    } else if (fbar_or(grp > kSoftSampled) && !fbar_or(grp > kCap)) {
                         set_threshold(compact(s, k, k + (kSoft - k) / 2, false, idx_bits), thr, mode);
+                    }
                     grp = 0;
+                }
+            }
+            if (regions) {
+                if (fbar_or(fill > kRegion)) {
+                    // a region dropped entries: scan the row again below, from -inf if fewer than kk
+                    // scores reached the bound, else from the same bound
+                    if (lane == 0) s.warp_tot[tid >> 5] = (uint32_t)fill;
+                    fbar();
+                    int total = 0;
+                    for (int w = 0; w < kThreads / 32; ++w) total += (int)s.warp_tot[w];
+                    if (tid == 0) s.count = total < kk ? total : kCap + 1;
+                } else {
+                    gather_regions(s, fill);
                 }
             }
         } else {
@@ -1174,7 +1305,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_kernel(TopkParams p) {
         // A sampled row is scanned again with plain loads (the tile ring has moved on to the next
         // row), with a block barrier per tile and the compactions: from -inf if its bound was above
         // the row's kk-th best score (fewer than kk reached it), from the same bound if the scores
-        // at or above it overflowed the buffer (ties at the bound).
+        // at or above it overflowed the buffer (ties at the bound) or a warp's region.
         const bool from_inf = sampled && cnt < kk, again = from_inf || (sampled && cnt > kCap);
         if (again) {
             fbar();  // every thread has read the count

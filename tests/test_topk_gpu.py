@@ -155,6 +155,31 @@ def test_few_distinct_values_long_rows(distinct, order):
     _run_and_check(torch.from_numpy(s).cuda(), None, 2048, order)
 
 
+def _warp_skewed_row(n, nhigh, tiles, seed):
+    """Standard normal scores, nhigh of them raised by 6 at positions that the first filter warp
+    reads (offsets [0, 128) and [2048, 2176) of each 4096-score tile) within the given tiles."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(n).astype(np.float32)
+    cand = np.array([t * 4096 + o for t in tiles for o in list(range(128)) + list(range(2048, 2176))
+                     if t * 4096 + o < n])
+    x[rng.choice(cand, nhigh, replace=False)] += np.float32(6.0)
+    return x
+
+
+# Rows that start from the sampled bound append to warp-private regions of the buffer (320
+# entries each). These rows put most of the kept scores on one warp's positions: its fill passes
+# 288 at a check with room left, after which the row continues with the shared count (460 raised
+# scores); and its region overflows with more than k scores at or above the bound (900 in 4 tiles
+# that no sample run touches: the row is scanned again from the same bound), with fewer (1500 in
+# the first 7 tiles: scanned again from -inf), and between two checks (250).
+@pytest.mark.parametrize("order", ["score", "index"])
+def test_rows_skewed_onto_one_warp(order):
+    n = 200000
+    rows = [_warp_skewed_row(n, 460, range(49), 31), _warp_skewed_row(n, 900, (1, 2, 4, 5), 33),
+            _warp_skewed_row(n, 1500, range(7), 31), _warp_skewed_row(n, 250, range(49), 31)]
+    _run_and_check(torch.from_numpy(np.stack(rows)).cuda(), None, 2048, order)
+
+
 # k on both sides of the largest selection the bucket ranking orders (2560) and of the power of
 # two the bitonic fallback pads to.
 @pytest.mark.parametrize("k", [2559, 2560, 2561, 3000])
