@@ -647,39 +647,45 @@ __device__ __forceinline__ float score_of(uint32_t key, uint32_t ix, const float
 // ranking to pay (the caller then selects and sorts separately). Block-wide; ends with a barrier.
 __device__ bool select_sort_by_score(TopkSmem &s, int kk, int32_t *oi, float *ov, const float *x, int n) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int cnt = s.count;
+    const int cnt = s.count, keyed = s.keyed;
     if (kk == 0) return true;
     constexpr int kPerT = kCap / kThreads;
+    // entries at or past `keyed` still hold raw score bits: keyed here, in registers
+    auto key_at = [&](int i) {
+        const uint32_t v = s.cb.key[i];
+        return i < keyed ? v : order_key(__uint_as_float(v));
+    };
     uint64_t c[kPerT];
-    const uint32_t h0 = s.cb.key[0];
+    const uint32_t h0 = key_at(0);
     uint32_t hmin = 0xffffffffu, hmax = 0u, vary = 0u;
 #pragma unroll
     for (int j = 0; j < kPerT; ++j) {
-        const int i = j * kThreads + tid;
-        c[j] = i < cnt ? pack_out(s.cb.key[i], s.cb.idx[i], true) : 0ull;
-        if (i < cnt) {
-            const uint32_t h = (uint32_t)(c[j] >> 32);
-            hmin = min(hmin, h);
-            hmax = max(hmax, h);
-            vary |= h ^ h0;
+        c[j] = 0ull;
+        if (j * kThreads < cnt) {  // the same for the whole block: slots past the count are skipped
+            const int i = j * kThreads + tid;
+            if (i < cnt) {
+                c[j] = pack_out(key_at(i), s.cb.idx[i], true);
+                const uint32_t h = (uint32_t)(c[j] >> 32);
+                hmin = min(hmin, h);
+                hmax = max(hmax, h);
+                vary |= h ^ h0;
+            }
         }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        hmin = min(hmin, __shfl_xor_sync(kFull, hmin, off));
-        hmax = max(hmax, __shfl_xor_sync(kFull, hmax, off));
-        vary |= __shfl_xor_sync(kFull, vary, off);
-    }
+    hmin = __reduce_min_sync(kFull, hmin);
+    hmax = __reduce_max_sync(kFull, hmax);
+    vary = __reduce_or_sync(kFull, vary);
     if (lane == 0) {
         s.hist[warp] = hmin;
         s.hist[kThreads / 32 + warp] = hmax;
         s.hist[2 * (kThreads / 32) + warp] = vary;
     }
     fbar();  // also: every entry of the buffer is in registers (s.packed overlays it)
-    for (int w = 0; w < kThreads / 32; ++w) {
-        hmin = min(hmin, s.hist[w]);
-        hmax = max(hmax, s.hist[kThreads / 32 + w]);
-        vary |= s.hist[2 * (kThreads / 32) + w];
+    {
+        const bool has = lane < kThreads / 32;
+        hmin = __reduce_min_sync(kFull, has ? s.hist[lane] : 0xffffffffu);
+        hmax = __reduce_max_sync(kFull, has ? s.hist[kThreads / 32 + lane] : 0u);
+        vary = __reduce_or_sync(kFull, has ? s.hist[2 * (kThreads / 32) + lane] : 0u);
     }
     fbar();
     const uint32_t diff = hmin ^ hmax;
@@ -707,7 +713,7 @@ __device__ bool select_sort_by_score(TopkSmem &s, int kk, int32_t *oi, float *ov
     fbar();
 #pragma unroll
     for (int j = 0; j < kPerT; ++j)
-        if (j * kThreads + tid < cnt) atomicAdd(&s.hist[digit(c[j])], 1u);
+        if (j * kThreads < cnt && j * kThreads + tid < cnt) atomicAdd(&s.hist[digit(c[j])], 1u);
     fbar();
 
     // bucket starts from the top bin down, the cost (sum of squared sizes), and the bucket holding
@@ -732,11 +738,10 @@ __device__ bool select_sort_by_score(TopkSmem &s, int kk, int32_t *oi, float *ov
     if (lane == 31) s.warp_tot[warp] = incl;
     if (lane == 0) s.warp_base[warp] = (int)sq;
     fbar();
-    uint32_t run = incl - local, cost = 0u;
-    for (int v = 0; v < kThreads / 32; ++v) {
-        if (v < warp) run += s.warp_tot[v];
-        cost += (uint32_t)s.warp_base[v];
-    }
+    uint32_t run = incl - local;
+    const bool has = lane < kThreads / 32;
+    run += __reduce_add_sync(kFull, has && lane < warp ? s.warp_tot[lane] : 0u);
+    const uint32_t cost = __reduce_add_sync(kFull, has ? (uint32_t)s.warp_base[lane] : 0u);
     const bool ok = cost <= (uint32_t)kSortBudget * (uint32_t)cnt;
     if (ok) {
 #pragma unroll
@@ -759,9 +764,11 @@ __device__ bool select_sort_by_score(TopkSmem &s, int kk, int32_t *oi, float *ov
     // scatter the buckets at or above the cut
 #pragma unroll
     for (int j = 0; j < kPerT; ++j) {
-        const uint32_t d = digit(c[j]);
-        const bool valid = j * kThreads + tid < cnt && d >= (uint32_t)cut;
-        if (valid) s.packed[atomicAdd(&s.hist[d], 1u)] = c[j];  // the order within a bucket is free, as above
+        if (j * kThreads < cnt) {
+            const uint32_t d = digit(c[j]);
+            const bool valid = j * kThreads + tid < cnt && d >= (uint32_t)cut;
+            if (valid) s.packed[atomicAdd(&s.hist[d], 1u)] = c[j];  // the order within a bucket is free, as above
+        }
     }
     fbar();
     // hist[d] is now the end of bucket d and hist[d + 1] its start; the cut bucket ends the scatter
@@ -1336,12 +1343,12 @@ __global__ void __launch_bounds__(kBlock, 2) topk_kernel(TopkParams p) {
         const float *x = p.scores + (size_t)row * (size_t)p.ld;
         int32_t *oi = p.out_idx + (size_t)row * (size_t)p.ldo;
         float *ov = p.out_val ? p.out_val + (size_t)row * (size_t)p.ldo : nullptr;
-        make_keys(s);
         // by score: select the best min(k, n) and order them in one pass of buckets when the
-        // buckets are even enough
+        // buckets are even enough (keying the entries that still hold raw bits in registers)
         const bool direct = by_score && select_sort_by_score(s, kk, oi, ov, x, n);
         bool bucketed = false;
         if (!direct) {
+            make_keys(s);
             // exactly the best min(k, n)
             if (s.count > kk) compact(s, kk, kk, true, idx_bits);
             // order them: by buckets of the key (or position) when they are even enough, else with
