@@ -1142,9 +1142,11 @@ __device__ uint64_t sampled_bound(TopkSmem &s, const float *x, int n, int r) {
 // Persistent CTAs, each taking rows blockIdx.x, blockIdx.x + gridDim.x, ... A producer warp keeps
 // kStages tiles of 4096 scores in flight (bulk copies into a shared-memory ring, one "full"
 // mbarrier per stage), running ahead across row boundaries, and refills a stage as soon as every
-// filter warp has released it (one "empty" mbarrier per stage). The 16 filter warps wait for each
-// tile themselves (one lane polls, bounded) and filter it into the candidate buffer; their own
-// barrier per tile only decides whether the buffer needs attention.
+// filter thread has released it (one "empty" mbarrier per stage, one arrival per thread, so no
+// warp has to reconverge for one lane to arrive). The 16 filter warps wait for each tile
+// themselves (every lane tests the mbarrier; one lane polls, bounded, when they do not all see it
+// complete) and filter it into the candidate buffer; their own barriers only decide whether the
+// buffer needs attention.
 __global__ void __launch_bounds__(kBlock, 2) topk_kernel(TopkParams p) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     TopkSmem &s = *reinterpret_cast<TopkSmem *>(smem_raw);
@@ -1155,7 +1157,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_kernel(TopkParams p) {
     if (tid == 0) {
         for (int st = 0; st < kStages; ++st) {
             ptx::mbar_init(ptx::smem_u32(&s.full[st]), 1);
-            ptx::mbar_init(ptx::smem_u32(&s.empty[st]), kThreads / 32);
+            ptx::mbar_init(ptx::smem_u32(&s.empty[st]), kThreads);
         }
         ptx::fence_mbar_init();
         s.failed = 0;
@@ -1171,7 +1173,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_kernel(TopkParams p) {
             uint32_t it = 0u;
             while (cursor_settle(p, cur)) {
                 const uint32_t st = it % kStages;
-                // the stage's previous tile has been released by every filter warp
+                // the stage's previous tile has been released by every filter thread
                 if (it >= kStages && !ptx::mbar_wait(ptx::smem_u32(&s.empty[st]), ((it / kStages) & 1u) ^ 1u)) {
                     *failed = 1;
                     if (p.status) raise_status(p.status, RL_ERR_TIMEOUT);
@@ -1192,10 +1194,13 @@ __global__ void __launch_bounds__(kBlock, 2) topk_kernel(TopkParams p) {
     }
 
     // ---------------------------------------------------------------- filter warps
-    // Waits for tile gi to land (one lane of the warp polls, bounded); after a timeout the tiles are
-    // no longer waited for and the results are not valid (flagged).
+    // Waits for tile gi to land: every lane tests the stage's mbarrier once, and if they do not all
+    // see it complete, one lane polls (bounded); after a timeout the tiles are no longer waited for
+    // and the results are not valid (flagged).
     auto wait_tile = [&](uint32_t gi) {
-        if (lane == 0 && !*failed && !ptx::mbar_wait(ptx::smem_u32(&s.full[gi % kStages]), (gi / kStages) & 1u)) {
+        const uint32_t bar = ptx::smem_u32(&s.full[gi % kStages]), parity = (gi / kStages) & 1u;
+        if (__all_sync(kFull, ptx::mbar_try_wait(bar, parity))) return;  // the common case: every lane sees it
+        if (lane == 0 && !*failed && !ptx::mbar_wait(bar, parity)) {
             *failed = 1;
             if (p.status) raise_status(p.status, RL_ERR_TIMEOUT);
         }
@@ -1257,8 +1262,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_kernel(TopkParams p) {
                     else
                         grp = max(grp, filter_append(s, vals, t, n, thr, mode, -1, st));
                 }
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&s.empty[st]));  // this warp is done with the stage
+                ptx::mbar_arrive(ptx::smem_u32(&s.empty[st]));  // this thread is done with the stage
                 if ((t % kCheck) == kCheck - 1 && t + 1 < ntiles) {
                     if (regions) {
                         if (fbar_or(fill > kRegionSoft) && !fbar_or(fill > kRegion)) {
@@ -1303,8 +1307,7 @@ __global__ void __launch_bounds__(kBlock, 2) topk_kernel(TopkParams p) {
                     const bool overflow = fbar_or(after_add > kCap) != 0;
                     settle_tile(s, s.ring[st], t, n, k, idx_bits, overflow, thr, mode);
                 }
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&s.empty[st]));  // this warp is done with the stage
+                ptx::mbar_arrive(ptx::smem_u32(&s.empty[st]));  // this thread is done with the stage
             }
         }
         fbar();  // every append of the row is done
