@@ -969,8 +969,18 @@ __device__ __forceinline__ int region_append(TopkSmem &s, const float (&vals)[kP
             ri[pos] = (uint32_t)(base + off);
         }
     };
-    // every keeping lane's first score: its place among the keeping lanes
-    if (keepm) put(fill + __popc(m & ((1u << lane) - 1u)), keepm);
+    {
+        // every keeping lane's first score: its place among the keeping lanes. Straight-line code
+        // for the whole warp (the read-back address is valid for any q) and predicated stores.
+        const int q = __ffs(keepm) - 1;
+        const int off = 4 * kThreads * ((q >> 2) & 1) + (q & 3);
+        const int pos = fill + __popc(m & ((1u << lane) - 1u));
+        const uint32_t bits = __float_as_uint(s.ring[stage][4 * (int)threadIdx.x + off]);
+        if (keepm != 0u && pos < kRegion) {
+            rk[pos] = bits;  // raw bits, keyed later
+            ri[pos] = (uint32_t)(base + off);
+        }
+    }
     int next = fill + __popc(m);
     keepm &= keepm - 1u;
     if (__any_sync(kFull, keepm != 0u)) {
