@@ -984,6 +984,20 @@ __device__ __forceinline__ int region_append(TopkSmem &s, const float (&vals)[kP
     int next = fill + __popc(m);
     keepm &= keepm - 1u;
     if (__any_sync(kFull, keepm != 0u)) {
+        const uint32_t more = keepm & (keepm - 1u);
+        if (!__any_sync(kFull, more != 0u)) {
+            // no lane keeps more than two: each second score after every first, in lane order
+            const unsigned b = __ballot_sync(kFull, keepm != 0u);
+            const int q = __ffs(keepm) - 1;
+            const int off = 4 * kThreads * ((q >> 2) & 1) + (q & 3);
+            const int pos = next + __popc(b & ((1u << lane) - 1u));
+            const uint32_t bits = __float_as_uint(s.ring[stage][4 * (int)threadIdx.x + off]);
+            if (keepm != 0u && pos < kRegion) {
+                rk[pos] = bits;
+                ri[pos] = (uint32_t)(base + off);
+            }
+            return next + __popc(b);
+        }
         // lanes that keep several scores of the tile: the rest after every first, in lane order
         const int c = __popc(keepm);
         int incl = c;
