@@ -93,6 +93,9 @@ struct ChunkRecord {
 };
 static_assert(sizeof(ChunkRecord) == 64, "record size");
 constexpr int kWsHeader = 256;
+// Start offset between the first wave's blocks on an SM (measured on the 16.8M-token workload:
+// 2.5-3.5 us gave 62.1-62.7 us per launch against 65.6 unstaggered; 1.5 us 63.8-64.2; 5 us 65.5).
+constexpr uint32_t kStaggerNs = 3000;
 
 // Tensor maps of the token arrays viewed as [T / 32 rows x 32 floats] (one 128-byte row per
 // thread's 32 tokens), boxes of 256 rows (a chunk) with the 128-byte swizzle: the same XOR layout
@@ -330,6 +333,15 @@ __global__ void __launch_bounds__(kThreads, 3) gae_chunk_kernel(GaeParams p, con
     ChunkRecord *recs = reinterpret_cast<ChunkRecord *>(static_cast<char *>(p.workspace) + kWsHeader);
 
     if (tid == 0) {
+        // The blocks of a wave otherwise stay in step for the whole launch: all stage their chunks
+        // at once (HBM saturated), then all fold, look back and re-walk (HBM idle). The first
+        // wave's blocks on an SM start a few microseconds apart, before they take their tickets,
+        // so the chunk order is unchanged and so is every result.
+        if (p.stagger_ns != 0u && blockIdx.x < (unsigned)(p.stagger_sms * p.stagger_slots)) {
+            const unsigned long long slot = blockIdx.x / (unsigned)p.stagger_sms;
+            const unsigned long long t_start = global_ns(), dt = slot * p.stagger_ns;
+            while (global_ns() - t_start < dt) __nanosleep(500);
+        }
         const uint32_t ticket = atomicAdd(&hdr->ticket, 1u);
         s_k = nchunks - 1 - (int)ticket;
         sm.epoch = *reinterpret_cast<volatile uint32_t *>(&hdr->epoch);
@@ -808,8 +820,9 @@ bool token_map(CUtensorMap *m, const float *base, int64_t rows, uint32_t box_row
 }
 
 template <bool kCross>
-cudaError_t launch_chunks(const GaeParams &p, unsigned nchunks, cudaStream_t stream) {
+cudaError_t launch_chunks(GaeParams p, unsigned nchunks, cudaStream_t stream) {
     static std::atomic<uint64_t> configured{0};  // one bit per device
+    static int sms[64], slots[64];               // per device: SMs, and blocks resident per SM
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -818,8 +831,20 @@ cudaError_t launch_chunks(const GaeParams &p, unsigned nchunks, cudaStream_t str
         e = cudaFuncSetAttribute(gae_chunk_kernel<kCross>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemTotal);
         if (e != cudaSuccess) return e;
+        int n = 0, occ = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gae_chunk_kernel<kCross>, kThreads, kSmemTotal);
+        if (e != cudaSuccess) return e;
+        sms[dev & 63] = n;
+        slots[dev & 63] = occ;
         configured.fetch_or(bit);
     }
+    // stagger only launches of several waves: the first wave's delay (up to 2 x 3 us with three
+    // blocks per SM) is paid once
+    p.stagger_sms = sms[dev & 63];
+    p.stagger_slots = slots[dev & 63];
+    p.stagger_ns = (p.stagger_slots > 1 && (int64_t)nchunks >= 4ll * p.stagger_sms * p.stagger_slots) ? kStaggerNs : 0u;
     GaeMaps maps{};
     const int64_t rows = p.num_tokens / kTok;
     if (p.vec && rows >= kThreads) {

@@ -27,6 +27,10 @@ struct GaeParams {
     uint32_t *status;
     uint64_t wait_ns;          // bound on each wait for a neighbouring chunk's map (1 s)
     int32_t withhold_chunk;    // failure injection: this chunk never publishes its map (-1: none)
+    // set by launch_gae: the first wave's blocks on an SM start stagger_ns apart (0: no stagger);
+    // block b of that wave is taken to run in slot b / stagger_sms of its SM
+    uint32_t stagger_ns;
+    int32_t stagger_sms, stagger_slots;
 };
 
 // Row-wise deterministic top-k (see topk.cu).
