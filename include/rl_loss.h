@@ -416,13 +416,13 @@ RL_LOSS_API rl_status rl_loss_launch_count(rl_loss_t handle, int64_t *count);
  * that max_tokens / max_seqs are ignored: calls accept at most 262144 tokens
  * and 8192 responses and return RL_ERR_CAPACITY beyond that, before launching
  * anything. The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture. Every call on a device shares the one array and leaves
- * its contents behind (the status word is cleared at the start of each call),
- * so calls that overlap on the GPU (two streams, two threads) race and must be
- * serialised by the caller. `device_status` (optional, a device pointer to one
- * uint32) receives this call's status bits as rl_loss_get_device_status would
- * report them. Everything else (arguments, layouts, outputs, errors) is as for
+ * (cudaGetSymbolAddress) with that device current. Every call on a device
+ * shares the one array and leaves its contents behind (the status word is
+ * cleared at the start of each call), so calls that overlap on the GPU (two
+ * streams, two threads) race and must be serialised by the caller.
+ * `device_status` (optional, a device pointer to one uint32) receives this
+ * call's status bits as rl_loss_get_device_status would report them.
+ * Everything else (arguments, layouts, outputs, errors) is as for
  * rl_loss_forward_backward. */
 RL_LOSS_API rl_status rl_loss_forward_backward_noalloc(const rl_loss_config *config, const rl_loss_inputs *inputs,
                                                        const rl_loss_outputs *outputs, uint32_t *device_status,
