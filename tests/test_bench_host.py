@@ -45,3 +45,25 @@ def test_single_process_helpers():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5  # no process group: identity
     assert bench.replica_throughput(100, 2, 1, 1000.0) == pytest.approx(200.0)
+
+
+def test_profile_summaries_carry_traffic_and_source_hash():
+    """Every ncu summary the benchmark reads a traffic figure from exists, gives the figure and the
+    hash of the kernel sources it was taken on, and names only committed files in its command; the
+    sources it hashes exist. (Whether the hash matches the current sources decides whether the
+    benchmark reports the figure or null; that is not asserted here.)"""
+    import re
+    import bench
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    names = set(re.findall(r'kernel_traffic\("(\w+)", (?:args\.case|(\d+)|"(\w+)")\)',
+                           open(os.path.join(root, "bench.py")).read()))
+    assert names, "no profile lookups found in bench.py"
+    for kernel, num, label in names:
+        for name in ([f"{kernel}_case{c}.md" for c in (1, 2, 3)] if not (num or label)
+                     else [f"{kernel}_case{num}.md" if num else f"{kernel}_{label}.md"]):
+            text = open(os.path.join(root, "profiles", name)).read()
+            assert re.search(r"traffic_bytes_per_launch:\s*[0-9.eE+]+", text), name
+            assert re.search(r"source_sha256:\s*[0-9a-f]{64}", text), name
+            assert "_work/" not in text, name
+        for src in bench.KERNEL_SOURCES[kernel]:
+            assert os.path.exists(os.path.join(root, "rl_post_loss_gb300", "csrc", src)), src
